@@ -1,0 +1,131 @@
+"""CPU oracle for the prefill -> decode KV-cache relayout.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference legs of ``bench.py`` may import this package. The CUDA
+library in ``prefill_decode_paged_gb300`` never imports it, and it imports
+nothing from there.
+
+Two independent definitions live here:
+
+* ``kv_oracle.c`` (loaded through ctypes): the per-element loop nest over
+  (request, layer, component, token, head, dim) that follows pd.py's
+  ``prefill()`` gather and ``admit()`` slot formula on the page
+  "PD 分离与 KV 传输" (section "实现"), with the TP head split of section
+  "布局转换".
+* ``pd_pages.py`` (numpy): the same hand-off written the way pd.py stages it,
+  a gather of each layer into a contiguous ``[seq, kv_heads, head_dim]`` array
+  followed by a write through a list of decode slots. It is only used on
+  small inputs, as a cross-check of the C loop nest.
+
+Parity status: every function is pinned (see ``tests/test_oracle_pins.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libkv_oracle.so")
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``kv_oracle.c`` with gcc into a shared library; return its path."""
+    if not force and out == _LIB_PATH and os.path.exists(out) and (
+            os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, src],
+                   check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.kvo_bytes_per_token.restype = i64
+    lib.kvo_bytes_per_token.argtypes = [i32, i32, i32, i32, i32]
+    lib.kvo_transfer_bytes.restype = i64
+    lib.kvo_transfer_bytes.argtypes = [i32, i32, i32, i32, i32, i32, p]
+    lib.kvo_relayout.restype = ctypes.c_int
+    lib.kvo_relayout.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                 i64, i64, p, p, i32, p, p, p, p, p]
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the oracle library (building it first if needed).
+
+    ``path`` loads another build of the same source (the mutation tests use
+    this); the default build is cached.
+    """
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def bytes_per_token(num_layers, num_components, kv_heads, head_dim, elem_bytes, lib=None):
+    lib = lib or load()
+    return int(lib.kvo_bytes_per_token(num_layers, num_components, kv_heads, head_dim,
+                                       elem_bytes))
+
+
+def transfer_bytes(num_layers, num_components, kv_heads, head_dim, elem_bytes, seq_lens,
+                   lib=None):
+    lib = lib or load()
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    return int(lib.kvo_transfer_bytes(num_layers, num_components, kv_heads, head_dim,
+                                      elem_bytes, len(lens), lens.ctypes.data))
+
+
+def _ptr_array(arrays, writable: bool):
+    ptrs = (ctypes.c_void_p * max(1, len(arrays)))()
+    for i, a in enumerate(arrays):
+        if not a.flags.c_contiguous or (writable and not a.flags.writeable):
+            raise ValueError("oracle pools must be C-contiguous (and writable on the dst side)")
+        ptrs[i] = a.ctypes.data
+    return ptrs
+
+
+def relayout(src_pools, dst_pools, *, num_layers, num_components, kv_heads, head_dim,
+             elem_bytes, src_tp, dst_tp, src_block, dst_block, src_num_blocks,
+             dst_num_blocks, seq_lens, src_off, src_bt, dst_off, dst_bt,
+             layer_begin=0, layer_end=None, lib=None):
+    """Run the C oracle in place on numpy pools (one array per TP shard).
+
+    ``src_off``/``dst_off`` are CSR offsets (int64, length R+1) into the flat
+    block tables ``src_bt``/``dst_bt`` (int32). Layers [layer_begin,
+    layer_end) are processed; the pools may also be single-layer slices, with
+    ``num_layers=1`` and the layer range [0, 1).
+    """
+    lib = lib or load()
+    if layer_end is None:
+        layer_end = num_layers
+    if len(src_pools) != src_tp or len(dst_pools) != dst_tp:
+        raise ValueError("one pool per TP shard is required")
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    so = np.ascontiguousarray(src_off, dtype=np.int64)
+    sb = np.ascontiguousarray(src_bt, dtype=np.int32)
+    do = np.ascontiguousarray(dst_off, dtype=np.int64)
+    db = np.ascontiguousarray(dst_bt, dtype=np.int32)
+    # keep the (possibly empty) tables alive and non-null for the C side
+    sb = sb if sb.size else np.zeros(1, np.int32)
+    db = db if db.size else np.zeros(1, np.int32)
+    sp = _ptr_array(src_pools, False)
+    dp = _ptr_array(dst_pools, True)
+    rc = lib.kvo_relayout(layer_begin, layer_end, num_layers, num_components, kv_heads,
+                          head_dim, elem_bytes, src_tp, dst_tp, src_block, dst_block,
+                          src_num_blocks, dst_num_blocks, sp, dp, len(lens),
+                          lens.ctypes.data, so.ctypes.data, sb.ctypes.data, do.ctypes.data,
+                          db.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the geometry (status {rc})")

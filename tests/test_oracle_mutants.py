@@ -1,0 +1,87 @@
+"""Plant plausible mistakes in a copy of the C oracle and check that the pins catch them.
+
+Each mutant is a textual edit of ``oracle/kv_oracle.c`` compiled into a
+temporary library; a compact battery of the pins in ``test_oracle_pins.py``
+runs against it in a child process (a mutant may read out of bounds and
+crash, which also counts as caught). The unmodified source must pass the same
+battery.
+"""
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "kv_oracle.c")
+
+MUTANTS = {
+    "src_shard_by_dst_heads": ("const int64_t sp = h / src_heads;",
+                               "const int64_t sp = h / dst_heads;"),
+    "dst_local_head_by_src_heads": ("const int64_t dh = h % dst_heads;",
+                                    "const int64_t dh = h % src_heads;"),
+    "src_table_index_by_dst_block": ("src_bt[src_off[r] + t / src_block]",
+                                     "src_bt[src_off[r] + t / dst_block]"),
+    "dst_offset_by_src_block": ("const int64_t doff = t % dst_block;",
+                                "const int64_t doff = t % src_block;"),
+    "src_row_stride_by_dst_block": ("* src_block + soff)", "* dst_block + soff)"),
+    "dropped_local_head": ("* src_heads + sh) * D + e;", "* src_heads) * D + e;"),
+    "layer_component_transposed": ("((((l * C + c) * dst_num_blocks",
+                                   "((((c * C + l) * dst_num_blocks"),
+    "last_token_dropped": ("for (int64_t t = 0; t < n; ++t)",
+                           "for (int64_t t = 0; t + 1 < n; ++t)"),
+    "low_byte_only": ("for (int32_t b = 0; b < elem_bytes; ++b)",
+                      "for (int32_t b = 0; b < 1; ++b)"),
+    "count_without_components": ("return (int64_t)num_layers * num_components * kv_heads",
+                                 "return (int64_t)num_layers * kv_heads"),
+    "first_request_only": ("for (int32_t r = 0; r < num_requests; ++r) {",
+                           "for (int32_t r = 0; r < 1 && r < num_requests; ++r) {"),
+}
+
+BATTERY = textwrap.dedent("""
+    import sys
+    sys.path[:0] = [{root!r}, {tests!r}]
+    import oracle, test_oracle_pins as P
+    lib = oracle.load({lib!r})
+    P.test_llama70b_4k_prompt_is_1_34_gb_and_27_ms(lib)
+    P.test_deepseek_mla_4k_prompt_is_0_29_gb_and_6_ms(lib)
+    P.test_relayout_moves_exactly_the_counted_bytes(lib)
+    P.test_tiny_tagged_every_tag_lands_once_in_its_decode_slot(lib)
+    for tp in [(1, 1), (1, 2), (2, 1), (2, 2)]:
+        P.test_enumerate_block_sizes_and_tp(lib, tp)
+    for case in ["tp4_to_tp8", "tp4_to_tp2_ragged", "tp3_to_tp2_odd_blocks"]:
+        P.test_relayout_then_inverse_is_identity(lib, case)
+""")
+
+
+def _battery(lib_path):
+    code = BATTERY.format(root=ROOT, tests=os.path.join(ROOT, "tests"), lib=lib_path)
+    return subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                          timeout=300)
+
+
+def _build(tmp_path, name, text):
+    src = tmp_path / f"{name}.c"
+    src.write_text(text)
+    return oracle.build(force=True, src=str(src), out=str(tmp_path / f"lib{name}.so"))
+
+
+def test_unmutated_oracle_passes_the_battery(tmp_path):
+    with open(SRC) as f:
+        lib = _build(tmp_path, "control", f.read())
+    res = _battery(lib)
+    assert res.returncode == 0, res.stderr[-3000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique in the oracle"
+    lib = _build(tmp_path, name, text.replace(old, new))
+    res = _battery(lib)
+    assert res.returncode != 0, f"mutant {name} survived the pins"
