@@ -1,0 +1,517 @@
+#!/usr/bin/env python3
+"""Throughput of the prefill -> decode KV relayout on GB300.
+
+One step = one whole-prompt hand-off of a batch (every layer, component, head
+and token of every prompt: gather through the prefill block table, TP head
+re-shard, scatter through the decode block table), one kernel launch through
+the C ABI, with the pools resident in HBM. The default workload is the
+Llama-3-70B KV shape with one 4096-token prompt, prefill TP4 (block 16) ->
+decode TP8 (block 32): 1.34 GB read and 1.34 GB written per step.
+
+Printed: one JSON line (rank 0). ``value`` is the whole-job relayout
+throughput in GB/s of algorithmic bytes (read + written), device-timed with
+CUDA events over exactly K steps after W warm-up steps, max over ranks.
+Extra keys: the per-layer launch mode (eager and CUDA-graph), ``e2e`` (the
+same metric through the public API with the pools in pinned host memory and
+both copies inside the timed region), ``roofline`` (HBM), ``cpu_baseline``
+(the CPU oracle on a bounded sample of the same workload) and the SM clocks
+sampled during the timed regions.
+
+``--impl reference`` times the CPU oracle instead (the only reference this
+method has: the pages ship no implementation of it).
+
+Multi-GPU (torchrun): every rank runs its own replica on its own GPU (the
+hand-off of one batch never crosses GPUs); timing is barrier-bracketed and
+the slowest rank's time is used, so ``value`` is weak-scaling throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV relayout GB/s (read+write) and % of GB300 HBM peak; ms per 4K-token 70B prompt"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("relayout.cu", "kvr_index.h", "plan.h", "plan.cpp")
+WORKLOAD_TEXT = {
+    "llama70b": ("Llama-3-70B KV shape: 80 layers, 8 KV heads, head_dim 128, bf16 K/V; "
+                 "1 x 4096-token prompt; prefill TP4 (2 heads/shard, block 16) -> decode TP8 "
+                 "(1 head/shard, block 32); pools 1.25x the blocks needed"),
+    "llama8b": ("Llama-3-8B KV shape: 32 layers, 8 KV heads, head_dim 128, bf16; 16 prompts "
+                "U[512,4096]; block 16 -> 32; TP1 -> TP1"),
+    "qwen32k": ("Qwen3-32B KV shape: 64 layers, 8 KV heads, head_dim 128, bf16; 4 x 32768 "
+                "tokens; prefill TP4 block 16 -> decode TP2 block 64"),
+    "qwen32k_ragged": ("Qwen3-32B KV shape, 4 prompts of 32768 - U[1,63] tokens; TP4 block 16 "
+                       "-> TP2 block 64"),
+    "dsv3mla": ("DeepSeek-V3 MLA latent: 61 layers, one 576-dim bf16 latent per token; 64 "
+                "prompts lognormal(median 4096) clipped to [1024, 16384]; block 64 -> 16; TP1"),
+    "tiny": "tiny: 2 layers, 2 KV heads, head_dim 64, fp16 bits; 1 x 100 tokens; 16 -> 32",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="llama70b",
+                   choices=["llama70b", "llama8b", "qwen32k", "qwen32k_ragged", "dsv3mla",
+                            "tiny"])
+    p.add_argument("--layers", type=int, default=None,
+                   help="use only the first N layers of the workload (small profiling cases)")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=12.0,
+                   help="CPU seconds for the oracle baseline sample")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args(argv)
+
+
+# -- ranks -----------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local, world
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x on every rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, world: int, max_seconds: float):
+    """Aggregate GB/s: every rank moved the same bytes; the slowest rank sets the time."""
+    return bytes_per_step_per_rank * steps * world / max_seconds / 1e9
+
+
+# -- clocks ------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; kept only for our GPU."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 10:
+                continue
+            if self.uuid and self.uuid not in parts[1]:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.rows.append(dict(t=ts, sm=float(parts[2]), sm_max=float(parts[3]),
+                                      power=_num(parts[4]), active=parts[5],
+                                      reasons=dict(zip(REASON_NAMES, parts[6:10]))))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, windows):
+        """Median SM clock and the throttle reasons seen inside the given (t0, t1) windows."""
+        inside = [r for r in self.rows if any(t0 - 0.05 <= r["t"] <= t1 + 0.05
+                                               for t0, t1 in windows)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample fell inside the timed regions"}
+        reasons = sorted({k for r in inside for k, v in r["reasons"].items()
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["sm_max"] for r in inside),
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((r["power"] for r in inside if r["power"] is not None),
+                                   default=None)}
+
+
+def _num(s):
+    try:
+        return float(s)
+    except ValueError:
+        return None
+
+
+# -- roofline inputs ----------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "prefill_decode_paged_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str, layers: int):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"relayout_{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_full_launch:\s*([0-9]+)", text)
+    if not src or not tr or src.group(1) != kernel_source_hash():
+        return None, path
+    return int(tr.group(1)) * layers // _full_layers(config), path
+
+
+def _full_layers(config):
+    import workloads as wl
+    return wl.get(config).num_layers
+
+
+# -- the CPU oracle -------------------------------------------------------------------
+
+def oracle_sample(w, src_layers, budget_s, reps_cap=1000):
+    """Time the oracle, as it stands, on the given layers of the workload until the
+    budget is spent (at least once). Returns (bytes moved, seconds, layers per pass)."""
+    import dataclasses
+
+    import oracle
+    n = len(src_layers[0])
+    wk = dataclasses.replace(w, num_layers=n)
+    dst = wk.dst_pools_numpy()
+    per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim * \
+        w.elem_bytes
+    moved, spent, reps = 0, 0.0, 0
+    while reps < reps_cap and (reps == 0 or spent < budget_s):
+        t = time.perf_counter()
+        oracle.relayout(src_layers, dst, **wk.geometry())
+        spent += time.perf_counter() - t
+        moved += 2 * per_layer * n
+        reps += 1
+    return moved, spent, n, reps
+
+
+def cpu_threads_used():
+    return 1  # the oracle is a single-threaded loop nest
+
+
+# -- our arm --------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    from prefill_decode_paged_gb300 import RelayoutPlan
+
+    rank, local, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the relayout only runs on the GPU")
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+
+    w = wl.get(args.config)
+    if args.layers:
+        w = w.with_layers(args.layers)
+    src = w.src_pools_torch(dev)
+    dst = w.dst_pools_torch(dev)
+    plan = RelayoutPlan(src, dst, **w.geometry())
+    bytes_step = plan.bytes_read + plan.bytes_written
+    stream = torch.cuda.current_stream(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    windows = []
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t_host = time.time()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        windows.append((t_host, time.time()))
+        ms = ev0.elapsed_time(ev1)
+        barrier(world)
+        return max_over_ranks(ms, world, dev)
+
+    K = args.steps
+    # whole-prompt: one launch per step
+    ms_all = timed(lambda: plan.run_all(stream), K)
+    # per-layer, eager: L launches per step from Python
+    L = w.num_layers
+
+    def per_layer():
+        for layer in range(L):
+            plan.run_layer(layer, stream)
+    k_layer = max(1, K // 4)
+    ms_layer = timed(per_layer, k_layer)
+    # per-layer, the L launches captured once in a CUDA graph and replayed
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cap):
+        for layer in range(L):
+            plan.run_layer(layer)
+    stream.wait_stream(cap)
+    ms_graph = timed(g.replay, K)
+
+    # e2e: pools in pinned host memory, copies and plan creation inside the region
+    e2e = None
+    if not args.no_e2e:
+        h_src = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in src]
+        h_dst = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dst]
+        for h, t in zip(h_src, src):
+            h.copy_(t)
+        meta_bytes = 16 * sum(-(-int(n) // w.dst_block) for n in w.seq_lens) + \
+            4 * sum(-(-int(n) // w.src_block) for n in w.seq_lens)
+        h2d = sum(t.numel() * t.element_size() for t in h_src) + meta_bytes
+        d2h = sum(t.numel() * t.element_size() for t in h_dst)
+
+        def e2e_step():
+            for h, t in zip(h_src, src):
+                t.copy_(h, non_blocking=True)
+            with RelayoutPlan(src, dst, **w.geometry()) as p:
+                p.run_all(stream)
+                for h, t in zip(h_dst, dst):
+                    h.copy_(t, non_blocking=True)
+                torch.cuda.synchronize(dev)
+
+        for _ in range(min(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t0 = time.perf_counter()
+        th = time.time()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        sec = time.perf_counter() - t0
+        windows.append((th, time.time()))
+        barrier(world)
+        sec = max_over_ranks(sec, world, dev)
+        e2e = {"value": round(whole_job_gbs(bytes_step, args.e2e_steps, world, sec), 2),
+               "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps,
+               "ms_per_step": round(sec * 1e3 / args.e2e_steps, 4),
+               "what": "per step: pinned-host -> HBM copy of every prefill shard pool, "
+                       "kv_relayout_plan (validate + upload tables), kv_relayout_all, "
+                       "HBM -> pinned-host copy of every decode shard pool, synchronize; "
+                       "wall clock"}
+        del h_src, h_dst
+
+    clock = None
+    if clocks:
+        time.sleep(0.25)
+        clocks.stop()
+        clock = clocks.summary(windows)
+
+    # CPU oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_layers = max(1, min(L, 8))
+        src_layers = [np.ascontiguousarray(t[:n_layers].cpu().numpy().view(w.int_dtype()))
+                      for t in src]
+        moved, sec, nl, reps = oracle_sample(w, src_layers, args.cpu_budget_s)
+        cpu = {"value": round(moved / sec / 1e9, 4), "unit": "GB/s", "cores": cpu_threads_used(),
+               "kind": "oracle",
+               "sample": f"{reps} pass(es) of the oracle over the first {nl} of {L} layers of "
+                         f"the same workload ({moved} bytes read+written in {sec:.1f} s), "
+                         f"host copies of the same prefill pools",
+               "host_cpus": os.cpu_count()}
+
+    hbm_peak, peak_src = measured_hbm_peak()
+    avg_launch_ms = ms_all / K
+    achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
+    traffic, _ = profiled_traffic(args.config, w.num_layers)
+    prompts = w.num_requests
+    value = whole_job_gbs(bytes_step, K, world, ms_all * 1e-3)
+    layer_gbs = whole_job_gbs(bytes_step, k_layer, world, ms_layer * 1e-3)
+    graph_gbs = whole_job_gbs(bytes_step, K, world, ms_graph * 1e-3)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_all / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.values == "randn" else f"u{8 * w.elem_bytes}",
+        "data": "synthetic (seeded randn bf16 pools, seeded random block tables)",
+        "config": {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
+                   "mode": "whole-prompt (all layers, one launch per step)",
+                   "prompts_per_step": prompts, "tokens_per_step": int(w.seq_lens.sum()),
+                   "bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (no flush)" if bytes_step > 2 * 129e6 else
+                         "working set fits in L2 (launch-bound case)",
+                   "parallelism": f"replica per GPU x{world}"},
+        "ms_per_prompt": round(ms_all / K / prompts, 5),
+        "pct_of_hbm_peak": round(100 * achieved / hbm_peak, 2),
+        "pct_of_nominal_hbm": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+        "per_layer": {
+            "eager": {"gbs": round(layer_gbs, 2), "ms_per_prompt": round(ms_layer / k_layer, 5),
+                      "us_per_launch": round(ms_layer * 1e3 / k_layer / L, 3),
+                      "launches_per_step": L, "steps": k_layer},
+            "cuda_graph": {"gbs": round(graph_gbs, 2),
+                           "ms_per_prompt": round(ms_graph / K, 5),
+                           "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
+                           "launches_per_step": L, "steps": K},
+        },
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} (copy, read+write)",
+                     "kernel": "kvr_relayout_kernel",
+                     "algorithmic_bytes_per_launch": bytes_step},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clock,
+    }
+    plan.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# -- reference arm: the CPU oracle ----------------------------------------------------------
+
+def run_reference(args):
+    import numpy as np
+
+    import workloads as wl
+    rank, local, world = dist_env()
+    if rank != 0:
+        return
+    w = wl.get(args.config)
+    if args.layers:
+        w = w.with_layers(args.layers)
+    # per step: a bounded sample of layers, sized so W + K steps take about two minutes
+    probe = w.with_layers(1)
+    src1 = probe.src_pools_numpy()
+    _, t1, _, _ = oracle_sample(probe, [a for a in src1], 0.0, reps_cap=1)
+    per_layer_s = max(t1, 1e-4)
+    total = args.steps + args.warmup
+    n = int(max(1, min(w.num_layers, 120.0 / (total * per_layer_s))))
+    wk = w.with_layers(n)
+    src = wk.src_pools_numpy()
+    for _ in range(args.warmup):
+        oracle_sample(wk, src, 0.0, reps_cap=1)
+    moved, spent = 0, 0.0
+    for _ in range(args.steps):
+        m, s, _, _ = oracle_sample(wk, src, 0.0, reps_cap=1)
+        moved += m
+        spent += s
+    gbs = moved / spent / 1e9
+    step_ms = spent * 1e3 / args.steps
+    cpu = {"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle", "cores": cpu_threads_used(),
+           "sample": f"each step: the oracle over the first {n} of {w.num_layers} layers of the "
+                     f"workload (all prompts, all heads)", "host_cpus": os.cpu_count()}
+    out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
+                      "sample_layers_per_step": n},
+           "cpu_baseline": cpu,
+           "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * kv_relayout.h -- C ABI of the prefill -> decode KV-cache relayout on one GPU.
+ *
+ * What it computes. Page "PD 分离与 KV 传输" (ai-infra-handbooks,
+ * serving/distributed/pd-disagg):
+ *   - section "实现" (pd.py prefill()/admit()): the prefill instance's K/V of
+ *     a prompt is gathered through the prefill block table (block size Bp) and
+ *     written through the decode block table (block size Bd): token p goes to
+ *     decode slot block_ids[p / Bd] * Bd + p % Bd, for p < n only;
+ *   - section "布局转换": when the TP degrees differ, a KV head moves from the
+ *     prefill card that holds it to the decode card that holds it (a split
+ *     for Tp < Td, a merge for Tp > Td);
+ *   - section "流程" and the "KV-Cache 传输:方案与时延" section of
+ *     "推理 INFRA 方法论（6）": the decode side allocates its blocks first and
+ *     the prefill side writes straight into them, whole prompt or layer by
+ *     layer as layers finish.
+ * All shard pools live in the HBM of the current GPU; there is no second
+ * device, collective or network. Elements are moved as raw bits (no dtype
+ * conversion; NaN payloads and -0 are preserved).
+ *
+ * Pool layout. Each TP shard of each side is ONE contiguous device buffer of
+ *   [num_layers][num_components][num_blocks][block_size][kv_heads / tp][head_dim]
+ * elements of elem_bytes bytes. Components: 2 = K then V planes, 1 = a single
+ * latent plane (MLA). Shard s holds the contiguous head range
+ * [s * H / tp, (s + 1) * H / tp).
+ *
+ * Block tables. CSR over requests: request r owns table entries
+ * bt[off[r]] .. bt[off[r + 1] - 1]; entry k is the physical block holding the
+ * request's tokens [k * B, (k + 1) * B). Only the first ceil(n_r / B) entries
+ * of each request are used (a decode table may reserve more, e.g. for the
+ * first generated token; those are never touched). One table per side, shared
+ * by all shard pools of that side. Prefill block ids may repeat (a shared
+ * prefix); used decode block ids may not.
+ *
+ * Ownership. The caller owns the pools, the streams and all host arrays; host
+ * arrays may be freed as soon as kv_relayout_plan() returns. The library
+ * owns a plan and its small device metadata buffer (work list and prefill
+ * block ids), freed by kv_relayout_plan_destroy(). The library never
+ * allocates, frees or chooses pool blocks.
+ *
+ * Errors. Every call returns a status; no C++ exception crosses this ABI.
+ * Launch calls are asynchronous, never synchronize, and report only launch
+ * errors (KVR_ERR_CUDA). A plan is immutable: launches of one plan from
+ * several threads are safe, but launches that overlap in time on different
+ * streams must not write the same decode blocks (the caller orders them).
+ */
+#ifndef KV_RELAYOUT_H_
+#define KV_RELAYOUT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest TP degree (number of shard pools) on either side. */
+#define KVR_MAX_TP 16
+
+typedef enum kvr_status {
+    KVR_OK = 0,
+    KVR_ERR_INVALID_ARG = -1,   /* NULL pointer, non-positive size, bad offsets, negative length */
+    KVR_ERR_UNSUPPORTED = -2,   /* elem_bytes not 1/2/4, H % tp != 0, tp > KVR_MAX_TP, too large */
+    KVR_ERR_ALIGNMENT = -3,     /* a pool not 16-byte aligned, or head_dim * elem_bytes % 16 != 0 */
+    KVR_ERR_BLOCK_RANGE = -4,   /* a used block id outside [0, num_blocks) */
+    KVR_ERR_TABLE_SHORT = -5,   /* a request has fewer than ceil(n / B) table entries */
+    KVR_ERR_DST_ALIAS = -6,     /* a decode block id used twice */
+    KVR_ERR_LAYER_RANGE = -7,   /* layer outside [0, num_layers) */
+    KVR_ERR_CUDA = -8,          /* a CUDA runtime call failed (no device, launch error, ...) */
+    KVR_ERR_NOMEM = -9,         /* host or device allocation of the plan failed */
+    KVR_ERR_POOL_OVERLAP = -10  /* a decode pool overlaps another decode pool or a prefill pool */
+} kvr_status;
+
+typedef struct kvr_desc {
+    int32_t num_layers;        /* L >= 1 */
+    int32_t num_components;    /* C: 2 (K, V) or 1 (MLA latent) */
+    int32_t kv_heads;          /* H >= 1: global KV heads (1 for an MLA latent) */
+    int32_t head_dim;          /* D >= 1: elements per head row */
+    int32_t elem_bytes;        /* es: 1, 2 or 4 */
+    int32_t src_tp;            /* Tp: prefill shard pools, 1..KVR_MAX_TP, divides H */
+    int32_t dst_tp;            /* Td: decode shard pools, 1..KVR_MAX_TP, divides H */
+    int32_t src_block_size;    /* Bp >= 1 tokens per prefill block */
+    int32_t dst_block_size;    /* Bd >= 1 tokens per decode block */
+    int64_t src_num_blocks;    /* Np >= 1 blocks in each prefill shard pool */
+    int64_t dst_num_blocks;    /* Nd >= 1 blocks in each decode shard pool */
+    const void *const *src_pools;   /* host array [Tp] of device pointers, 16-B aligned */
+    void *const *dst_pools;         /* host array [Td] of device pointers, 16-B aligned */
+    int32_t num_requests;           /* R >= 0 */
+    const int32_t *seq_lens;        /* host [R], n_r >= 0 (0 = nothing to move) */
+    const int64_t *src_bt_offsets;  /* host [R + 1], non-decreasing, >= 0 */
+    const int32_t *src_bt;          /* host, prefill block ids */
+    const int64_t *dst_bt_offsets;  /* host [R + 1], non-decreasing, >= 0 */
+    const int32_t *dst_bt;          /* host, decode block ids */
+} kvr_desc;
+
+typedef struct kvr_plan kvr_plan;
+
+/*
+ * Validate *desc on the host and compute the bytes one full relayout reads
+ * and writes (each = sum_r n_r * L * C * H * D * es, the page's "KV per token
+ * times prompt length", section "传输的代价"). Makes no CUDA call and
+ * dereferences no device pointer. Either output pointer may be NULL.
+ */
+kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
+                                  int64_t *bytes_written);
+
+/*
+ * Validate *desc (as above), build the work list on the host and upload it
+ * with the prefill block ids to the current device (one allocation, one
+ * synchronous copy). *out is set to the new plan, or to NULL on failure.
+ */
+kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
+
+/*
+ * Move layer `layer` of every request: one kernel launch on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream). Asynchronous. Calling
+ * it for every layer gives the same bytes as kv_relayout_all(). The current
+ * device must be the plan's device.
+ */
+kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream);
+
+/* Move all layers of every request: one kernel launch on `stream`. */
+kvr_status kv_relayout_all(const kvr_plan *plan, void *stream);
+
+/* Bytes one kv_relayout_all() reads and writes (per layer: divide by L). */
+kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
+                                  int64_t *bytes_written);
+
+/* Free the plan and its device buffer (NULL is a no-op). Synchronizes the
+ * device buffer's release like cudaFree: call it after the launches that use
+ * the plan have been ordered before any reuse of that memory. */
+void kv_relayout_plan_destroy(kvr_plan *plan);
+
+/* Static, human-readable name of a status. */
+const char *kv_relayout_strerror(kvr_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV_RELAYOUT_H_ */

@@ -1,0 +1,10 @@
+"""GB300-native prefill -> decode KV-cache relayout (one fused sm_103a kernel behind a C ABI).
+
+Public API (see ``include/kv_relayout.h`` for the C ABI it binds):
+
+* :class:`RelayoutPlan` -- validate a batch and upload its work list;
+  ``run_all()`` moves every layer in one launch, ``run_layer(l)`` one layer.
+* :func:`desc_bytes` -- host-only validation and byte count.
+"""
+from .kv_relayout import (KVRelayoutError, RelayoutPlan, desc_bytes, library,  # noqa: F401
+                          LIB_PATH, STATUS, EXPORTS)

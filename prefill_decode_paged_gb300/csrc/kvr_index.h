@@ -1,0 +1,129 @@
+// kvr_index.h -- work decomposition and address arithmetic of the relayout kernel.
+//
+// Compiled both by nvcc (into the kernel) and by a host compiler (plan
+// construction; the test emulator that walks every launch on the CPU), so it
+// holds plain structs and inline functions only.
+//
+// Work decomposition. A work ITEM is one (request, decode logical block j):
+// the request's tokens [j*Bd, j*Bd + ntok), ntok = min(Bd, n - j*Bd), for all
+// components and all KV heads. One launch covers (layers of the launch) x
+// items x slices TASKS, one CTA per task; a slice is a contiguous part of the
+// item's 16-byte chunks, so a per-layer launch with few items still fills the
+// GPU. Inside an item, chunk q is ordered [token o][component c][head h]
+// [chunk of the head row], so consecutive threads read and write consecutive
+// 16-byte pieces of one head row, and the rows of one token follow each other.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define KVR_HD __host__ __device__ __forceinline__
+#else
+#define KVR_HD inline
+#endif
+
+#ifndef KVR_MAX_TP
+#define KVR_MAX_TP 16
+#endif
+
+// Division by a run-time invariant d >= 1 for dividends n < 2^31, by one
+// 32x32->64 multiply and a shift (Granlund & Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, Theorem 4.2 with
+// N = 31): with l = ceil(log2 d) and m = ceil(2^(31+l) / d), which fits in
+// 32 bits, floor(n / d) = floor(n * m / 2^(31+l)) for all 0 <= n < 2^31.
+struct KvrDiv {
+    uint32_t d;
+    uint32_t mul;
+    uint32_t shift;
+
+    KVR_HD uint32_t div(uint32_t n) const {
+        return (uint32_t)(((uint64_t)n * mul) >> shift);
+    }
+};
+
+inline KvrDiv kvr_make_div(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t num = 1ull << (31 + l);
+    KvrDiv r;
+    r.d = d;
+    r.mul = (uint32_t)((num + d - 1) / d);
+    r.shift = 31 + l;
+    return r;
+}
+
+// One work item: a decode logical block of one request. 16 bytes.
+struct KvrItem {
+    int32_t sbt_off;    // index of the request's first prefill block id in the flat table
+    int32_t dst_block;  // physical decode block id
+    int32_t t0;         // first token of the item (a multiple of Bd)
+    int32_t ntok;       // tokens in the item, 1..Bd
+};
+
+struct KvrGeom {
+    int32_t C, H, Hp, Hd, Bp, Bd;
+    int32_t row_bytes;          // D * es, a multiple of 16
+    int32_t row_chunks;         // row_bytes / 16
+    KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp;
+    int64_t src_blk_bytes;      // Bp * Hp * row_bytes
+    int64_t dst_blk_bytes;      // Bd * Hd * row_bytes
+    int64_t src_plane_bytes;    // Np * src_blk_bytes: one (layer, component) plane
+    int64_t dst_plane_bytes;    // Nd * dst_blk_bytes
+};
+
+// Kernel parameter block (passed by value as a __grid_constant__).
+struct KvrArgs {
+    KvrGeom g;
+    const KvrItem *items;
+    const int32_t *sbt;                 // flat prefill block ids
+    const unsigned char *src[KVR_MAX_TP];
+    unsigned char *dst[KVR_MAX_TP];
+    int32_t layer0;                     // first layer of this launch
+    int32_t slices;                     // tasks per item
+    uint32_t tasks_per_layer;           // n_items * slices
+    KvrDiv div_tasks_per_layer, div_slices;
+};
+
+// Task -> (layer, item index, chunk range [q0, q1) of the item).
+KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,
+                     KvrItem *item, uint32_t *q0, uint32_t *q1) {
+    const uint32_t lt = a.div_tasks_per_layer.div(task);
+    const uint32_t rem = task - lt * a.tasks_per_layer;
+    const uint32_t idx = a.div_slices.div(rem);
+    const uint32_t slice = rem - idx * (uint32_t)a.slices;
+    const KvrItem it = items[idx];
+    const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.H * a.g.row_chunks;
+    *layer = a.layer0 + (int32_t)lt;
+    *item = it;
+    *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);
+    *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
+}
+
+// Chunk q of an item -> (prefill shard, byte offset) and (decode shard, byte offset).
+KVR_HD void kvr_chunk(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
+                      uint32_t q, uint32_t *sp, int64_t *soff, uint32_t *dp, int64_t *doff) {
+    const uint32_t row = g.div_rc.div(q);
+    const uint32_t ch = q - row * (uint32_t)g.row_chunks;
+    const uint32_t oc = g.div_H.div(row);
+    const uint32_t h = row - oc * (uint32_t)g.H;
+    const uint32_t o = g.div_C.div(oc);
+    const uint32_t c = oc - o * (uint32_t)g.C;
+    // prefill side: logical block t / Bp of the request, row t % Bp in it
+    const uint32_t t = (uint32_t)it.t0 + o;
+    const uint32_t sbi = g.div_Bp.div(t);
+    const uint32_t so = t - sbi * (uint32_t)g.Bp;
+    const int64_t sb = sbt[it.sbt_off + (int32_t)sbi];
+    // head h: prefill shard h / Hp (local h % Hp), decode shard h / Hd (local h % Hd)
+    const uint32_t s_sh = g.div_Hp.div(h);
+    const uint32_t s_loc = h - s_sh * (uint32_t)g.Hp;
+    const uint32_t d_sh = g.div_Hd.div(h);
+    const uint32_t d_loc = h - d_sh * (uint32_t)g.Hd;
+    const int64_t plane = (int64_t)layer * g.C + c;
+    *sp = s_sh;
+    *dp = d_sh;
+    *soff = plane * g.src_plane_bytes + sb * g.src_blk_bytes +
+            ((int64_t)so * g.Hp + s_loc) * g.row_bytes + (int64_t)ch * 16;
+    // the item starts at a decode block boundary: the decode row is o itself
+    *doff = plane * g.dst_plane_bytes + (int64_t)it.dst_block * g.dst_blk_bytes +
+            ((int64_t)o * g.Hd + d_loc) * g.row_bytes + (int64_t)ch * 16;
+}

@@ -1,0 +1,251 @@
+// plan.cpp -- descriptor validation, byte counts and the work list (host only).
+//
+// The checks follow what the hand-off on the page "PD 分离与 KV 传输"
+// (sections "实现" and "布局转换") needs to be well defined: each prompt
+// position has a prefill block and a decode block (tables long enough, ids in
+// range), no two positions land on the same decode slot (no decode block used
+// twice), and every head belongs to exactly one shard on each side (H
+// divisible by both TP degrees).
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "plan.h"
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// a * b * ... without overflowing int64; false when the product does not fit.
+bool mul_fits(std::initializer_list<int64_t> xs, int64_t *out) {
+    __int128 p = 1;
+    for (int64_t x : xs) {
+        p *= x;
+        if (p > (__int128)INT64_MAX) return false;
+    }
+    *out = (int64_t)p;
+    return true;
+}
+
+bool overlaps(uintptr_t a, int64_t na, uintptr_t b, int64_t nb) {
+    return a < b + (uint64_t)nb && b < a + (uint64_t)na;
+}
+
+kvr_status check_table(int32_t R, const int32_t *lens, const int64_t *off, const int32_t *bt,
+                       int32_t block, int64_t num_blocks) {
+    if (R > 0 && (off == nullptr || lens == nullptr)) return KVR_ERR_INVALID_ARG;
+    if (R > 0 && off[0] < 0) return KVR_ERR_INVALID_ARG;
+    for (int32_t r = 0; r < R; ++r) {
+        if (lens[r] < 0) return KVR_ERR_INVALID_ARG;
+        if (off[r + 1] < off[r]) return KVR_ERR_INVALID_ARG;
+    }
+    for (int32_t r = 0; r < R; ++r) {
+        const int64_t need = ceil_div(lens[r], block);
+        if (off[r + 1] - off[r] < need) return KVR_ERR_TABLE_SHORT;
+        if (need > 0 && bt == nullptr) return KVR_ERR_INVALID_ARG;
+        for (int64_t k = 0; k < need; ++k) {
+            const int32_t id = bt[off[r] + k];
+            if (id < 0 || (int64_t)id >= num_blocks) return KVR_ERR_BLOCK_RANGE;
+        }
+    }
+    return KVR_OK;
+}
+
+int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count) {
+    const int64_t target = (int64_t)std::max(sm_count, 1) * KVR_TARGET_CTAS_PER_SM;
+    if (tasks_unsliced <= 0 || tasks_unsliced >= target) return 1;
+    const int64_t want = ceil_div(target, tasks_unsliced);
+    const int64_t most = std::max<int64_t>(1, avg_chunks / KVR_MIN_SLICE_CHUNKS);
+    return (int32_t)std::min(want, most);
+}
+
+}  // namespace
+
+kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
+                               int64_t *bytes_out) {
+    if (d == nullptr) return KVR_ERR_INVALID_ARG;
+    const int32_t L = d->num_layers, C = d->num_components, H = d->kv_heads, D = d->head_dim;
+    const int32_t es = d->elem_bytes, Tp = d->src_tp, Td = d->dst_tp;
+    const int32_t Bp = d->src_block_size, Bd = d->dst_block_size, R = d->num_requests;
+    const int64_t Np = d->src_num_blocks, Nd = d->dst_num_blocks;
+
+    if (L < 1 || (C != 1 && C != 2) || H < 1 || D < 1 || Tp < 1 || Td < 1 || Bp < 1 ||
+        Bd < 1 || Np < 1 || Nd < 1 || R < 0)
+        return KVR_ERR_INVALID_ARG;
+    if (es != 1 && es != 2 && es != 4) return KVR_ERR_UNSUPPORTED;
+    if (Tp > KVR_MAX_TP || Td > KVR_MAX_TP) return KVR_ERR_UNSUPPORTED;
+    if (H % Tp != 0 || H % Td != 0) return KVR_ERR_UNSUPPORTED;
+    int64_t row_bytes = 0;
+    if (!mul_fits({D, es}, &row_bytes) || row_bytes > INT32_MAX) return KVR_ERR_UNSUPPORTED;
+    if (row_bytes % 16 != 0) return KVR_ERR_ALIGNMENT;
+    const int32_t Hp = H / Tp, Hd = H / Td;
+
+    // pool extents
+    int64_t src_pool = 0, dst_pool = 0, src_blk = 0, dst_blk = 0;
+    if (!mul_fits({(int64_t)L, C, Np, Bp, Hp, row_bytes}, &src_pool) ||
+        !mul_fits({(int64_t)L, C, Nd, Bd, Hd, row_bytes}, &dst_pool))
+        return KVR_ERR_UNSUPPORTED;
+    mul_fits({(int64_t)Bp, Hp, row_bytes}, &src_blk);
+    mul_fits({(int64_t)Bd, Hd, row_bytes}, &dst_blk);
+    // one item's 16-byte chunks must stay below 2^31 (32-bit chunk indices)
+    int64_t item_chunks = 0;
+    if (!mul_fits({(int64_t)Bd, C, H, row_bytes / 16}, &item_chunks) || item_chunks > INT32_MAX)
+        return KVR_ERR_UNSUPPORTED;
+
+    if (d->src_pools == nullptr || d->dst_pools == nullptr) return KVR_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < Tp; ++s)
+        if (d->src_pools[s] == nullptr) return KVR_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < Td; ++s)
+        if (d->dst_pools[s] == nullptr) return KVR_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < Tp; ++s)
+        if ((uintptr_t)d->src_pools[s] % 16 != 0) return KVR_ERR_ALIGNMENT;
+    for (int32_t s = 0; s < Td; ++s)
+        if ((uintptr_t)d->dst_pools[s] % 16 != 0) return KVR_ERR_ALIGNMENT;
+
+    kvr_status st = check_table(R, d->seq_lens, d->src_bt_offsets, d->src_bt, Bp, Np);
+    if (st != KVR_OK) return st;
+    st = check_table(R, d->seq_lens, d->dst_bt_offsets, d->dst_bt, Bd, Nd);
+    if (st != KVR_OK) return st;
+
+    // no decode block may receive two prompts' (or one prompt's two) tokens
+    int64_t tokens = 0, items = 0, used_src = 0;
+    std::vector<int32_t> used;
+    try {
+        for (int32_t r = 0; r < R; ++r) {
+            tokens += d->seq_lens[r];
+            const int64_t nd = ceil_div(d->seq_lens[r], Bd);
+            items += nd;
+            used_src += ceil_div(d->seq_lens[r], Bp);
+            for (int64_t k = 0; k < nd; ++k) used.push_back(d->dst_bt[d->dst_bt_offsets[r] + k]);
+        }
+        std::sort(used.begin(), used.end());
+    } catch (const std::bad_alloc &) {
+        return KVR_ERR_NOMEM;
+    }
+    if (std::adjacent_find(used.begin(), used.end()) != used.end()) return KVR_ERR_DST_ALIAS;
+
+    // decode pools must not overlap each other or any prefill pool
+    for (int32_t a = 0; a < Td; ++a) {
+        const uintptr_t pa = (uintptr_t)d->dst_pools[a];
+        for (int32_t b = a + 1; b < Td; ++b)
+            if (overlaps(pa, dst_pool, (uintptr_t)d->dst_pools[b], dst_pool))
+                return KVR_ERR_POOL_OVERLAP;
+        for (int32_t b = 0; b < Tp; ++b)
+            if (overlaps(pa, dst_pool, (uintptr_t)d->src_pools[b], src_pool))
+                return KVR_ERR_POOL_OVERLAP;
+    }
+
+    int64_t bytes = 0;
+    if (!mul_fits({tokens, (int64_t)L, C, H, row_bytes}, &bytes)) return KVR_ERR_UNSUPPORTED;
+    if (bytes_out) *bytes_out = bytes;
+    if (hp == nullptr) return KVR_OK;
+
+    // launch sizes: CTAs = layers x items x slices must fit a 32-bit grid
+    if (items > INT32_MAX || used_src > INT32_MAX || (int64_t)L * items > INT32_MAX)
+        return KVR_ERR_UNSUPPORTED;
+
+    KvrGeom &g = hp->g;
+    g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
+    g.row_bytes = (int32_t)row_bytes;
+    g.row_chunks = (int32_t)(row_bytes / 16);
+    g.div_rc = kvr_make_div((uint32_t)g.row_chunks);
+    g.div_H = kvr_make_div((uint32_t)H);
+    g.div_C = kvr_make_div((uint32_t)C);
+    g.div_Hp = kvr_make_div((uint32_t)Hp);
+    g.div_Hd = kvr_make_div((uint32_t)Hd);
+    g.div_Bp = kvr_make_div((uint32_t)Bp);
+    g.src_blk_bytes = src_blk;
+    g.dst_blk_bytes = dst_blk;
+    g.src_plane_bytes = src_pool / ((int64_t)L * C);
+    g.dst_plane_bytes = dst_pool / ((int64_t)L * C);
+    hp->num_layers = L;
+    hp->src_tp = Tp;
+    hp->dst_tp = Td;
+    for (int32_t s = 0; s < Tp; ++s) hp->src[s] = d->src_pools[s];
+    for (int32_t s = 0; s < Td; ++s) hp->dst[s] = d->dst_pools[s];
+    hp->bytes = bytes;
+
+    try {
+        hp->items.clear();
+        hp->sbt.clear();
+        hp->items.reserve((size_t)items);
+        hp->sbt.reserve((size_t)used_src);
+        for (int32_t r = 0; r < R; ++r) {
+            const int32_t n = d->seq_lens[r];
+            if (n == 0) continue;
+            const int32_t off = (int32_t)hp->sbt.size();
+            const int64_t ns = ceil_div(n, Bp);
+            for (int64_t k = 0; k < ns; ++k) hp->sbt.push_back(d->src_bt[d->src_bt_offsets[r] + k]);
+            for (int32_t j = 0; (int64_t)j * Bd < n; ++j) {
+                KvrItem it;
+                it.sbt_off = off;
+                it.dst_block = d->dst_bt[d->dst_bt_offsets[r] + j];
+                it.t0 = j * Bd;
+                it.ntok = std::min(Bd, n - j * Bd);
+                hp->items.push_back(it);
+            }
+        }
+    } catch (const std::bad_alloc &) {
+        return KVR_ERR_NOMEM;
+    }
+
+    const int64_t n_items = (int64_t)hp->items.size();
+    const int64_t avg_chunks = n_items ? (bytes / L / 16) / n_items : 0;
+    hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count);
+    hp->slices_all = choose_slices((int64_t)L * n_items, avg_chunks, sm_count);
+    while ((int64_t)L * n_items * hp->slices_all > INT32_MAX && hp->slices_all > 1)
+        --hp->slices_all;
+    return KVR_OK;
+}
+
+KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,
+                        int32_t layer0, int32_t slices) {
+    KvrArgs a;
+    memset(&a, 0, sizeof(a));
+    a.g = hp.g;
+    a.items = dev_items;
+    a.sbt = dev_sbt;
+    for (int32_t s = 0; s < hp.src_tp; ++s) a.src[s] = (const unsigned char *)hp.src[s];
+    for (int32_t s = 0; s < hp.dst_tp; ++s) a.dst[s] = (unsigned char *)hp.dst[s];
+    a.layer0 = layer0;
+    a.slices = slices;
+    a.tasks_per_layer = (uint32_t)(hp.items.size() * (size_t)slices);
+    a.div_tasks_per_layer = kvr_make_div(a.tasks_per_layer ? a.tasks_per_layer : 1);
+    a.div_slices = kvr_make_div((uint32_t)slices);
+    return a;
+}
+
+extern "C" kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
+                                             int64_t *bytes_written) {
+    int64_t b = 0;
+    kvr_status st;
+    try {
+        st = kvr_build_host_plan(desc, 0, nullptr, &b);
+    } catch (...) {
+        return KVR_ERR_NOMEM;
+    }
+    if (st != KVR_OK) return st;
+    if (bytes_read) *bytes_read = b;
+    if (bytes_written) *bytes_written = b;
+    return KVR_OK;
+}
+
+extern "C" const char *kv_relayout_strerror(kvr_status s) {
+    switch (s) {
+        case KVR_OK: return "ok";
+        case KVR_ERR_INVALID_ARG: return "invalid argument";
+        case KVR_ERR_UNSUPPORTED: return "unsupported geometry";
+        case KVR_ERR_ALIGNMENT: return "pool or head row not 16-byte aligned";
+        case KVR_ERR_BLOCK_RANGE: return "block id out of range";
+        case KVR_ERR_TABLE_SHORT: return "block table shorter than the prompt";
+        case KVR_ERR_DST_ALIAS: return "decode block id used twice";
+        case KVR_ERR_LAYER_RANGE: return "layer out of range";
+        case KVR_ERR_CUDA: return "CUDA runtime error";
+        case KVR_ERR_NOMEM: return "out of memory";
+        case KVR_ERR_POOL_OVERLAP: return "decode pool overlaps another pool";
+    }
+    return "unknown status";
+}

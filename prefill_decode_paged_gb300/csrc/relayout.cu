@@ -1,0 +1,177 @@
+// relayout.cu -- fused gather -> head re-shard -> scatter of paged KV cache (sm_103a).
+//
+// One kernel does the whole hand-off of the page "PD 分离与 KV 传输"
+// (ai-infra-handbooks, serving/distributed/pd-disagg; sections "实现" and
+// "布局转换"): each 16-byte chunk of a head row is read from the prefill
+// shard that holds the head, at the row the prefill block table gives for
+// the token, and written to the decode shard that holds the head, at the row
+// the decode block table gives. There is no intermediate buffer: the gather,
+// the TP re-shard and the scatter are one load and one store per chunk.
+//
+// It is pure data movement (no arithmetic on the values, no tensor cores),
+// bound by HBM bandwidth: every chunk is read once and written once, so the
+// DRAM traffic floor is 2 x (KV bytes of the prompts). The kernel keeps
+// KVR_UNROLL independent 16-byte loads in flight per thread before their
+// stores, uses streaming cache hints on both sides (neither the prefill rows
+// nor the decode rows are touched again by this kernel), and opts into
+// programmatic dependent launch so back-to-back per-layer launches overlap
+// their launch latency with the previous launch's tail.
+#include <cuda_runtime.h>
+
+#include <new>
+
+#include "kv_relayout.h"
+#include "kvr_index.h"
+#include "plan.h"
+
+struct kvr_plan {
+    KvrHostPlan host;
+    void *dev_meta = nullptr;       // items, then prefill block ids
+    const KvrItem *dev_items = nullptr;
+    const int32_t *dev_sbt = nullptr;
+    int device = 0;
+};
+
+namespace {
+
+__device__ __forceinline__ uint4 load_stream(const unsigned char *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(KVR_THREADS)
+    kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
+    // Wait for the grid this launch follows in its stream (a no-op without
+    // programmatic dependent launch), then let the next launch start early.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    int32_t layer;
+    KvrItem it;
+    uint32_t q0, q1;
+    kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
+
+    for (uint32_t base = q0 + threadIdx.x; base < q1; base += KVR_UNROLL * KVR_THREADS) {
+        uint4 v[KVR_UNROLL];
+        unsigned char *to[KVR_UNROLL];
+#pragma unroll
+        for (int k = 0; k < KVR_UNROLL; ++k) {
+            const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+            to[k] = nullptr;
+            if (q < q1) {
+                uint32_t sp, dp;
+                int64_t soff, doff;
+                kvr_chunk(a.g, layer, it, a.sbt, q, &sp, &soff, &dp, &doff);
+                v[k] = load_stream(a.src[sp] + soff);
+                to[k] = a.dst[dp] + doff;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KVR_UNROLL; ++k)
+            if (to[k] != nullptr) store_stream(to[k], v[k]);
+    }
+}
+
+kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
+                  void *stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
+    if (dev != p->device) return KVR_ERR_INVALID_ARG;
+    const KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, layer0, slices);
+    const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
+    if (grid == 0) return KVR_OK;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(KVR_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel, a) == cudaSuccess ? KVR_OK
+                                                                            : KVR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
+    if (out == nullptr) return KVR_ERR_INVALID_ARG;
+    *out = nullptr;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVR_ERR_CUDA;
+
+    kvr_plan *p = new (std::nothrow) kvr_plan();
+    if (p == nullptr) return KVR_ERR_NOMEM;
+    kvr_status st;
+    try {
+        st = kvr_build_host_plan(desc, sms, &p->host, nullptr);
+    } catch (...) {
+        st = KVR_ERR_NOMEM;
+    }
+    if (st != KVR_OK) {
+        delete p;
+        return st;
+    }
+    p->device = dev;
+    const size_t items_bytes = p->host.items.size() * sizeof(KvrItem);
+    const size_t sbt_bytes = p->host.sbt.size() * sizeof(int32_t);
+    if (items_bytes + sbt_bytes > 0) {
+        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            delete p;
+            return KVR_ERR_NOMEM;
+        }
+        unsigned char *base = (unsigned char *)p->dev_meta;
+        if (cudaMemcpy(base, p->host.items.data(), items_bytes, cudaMemcpyHostToDevice) !=
+                cudaSuccess ||
+            cudaMemcpy(base + items_bytes, p->host.sbt.data(), sbt_bytes,
+                       cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaFree(p->dev_meta);
+            delete p;
+            return KVR_ERR_CUDA;
+        }
+        p->dev_items = (const KvrItem *)base;
+        p->dev_sbt = (const int32_t *)(base + items_bytes);
+    }
+    *out = p;
+    return KVR_OK;
+}
+
+extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= plan->host.num_layers) return KVR_ERR_LAYER_RANGE;
+    return launch(plan, layer, 1, plan->host.slices_layer, stream);
+}
+
+extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    return launch(plan, 0, plan->host.num_layers, plan->host.slices_all, stream);
+}
+
+extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
+                                             int64_t *bytes_written) {
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    if (bytes_read) *bytes_read = plan->host.bytes;
+    if (bytes_written) *bytes_written = plan->host.bytes;
+    return KVR_OK;
+}
+
+extern "C" void kv_relayout_plan_destroy(kvr_plan *plan) {
+    if (plan == nullptr) return;
+    if (plan->dev_meta != nullptr) cudaFree(plan->dev_meta);
+    delete plan;
+}

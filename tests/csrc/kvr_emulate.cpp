@@ -1,0 +1,142 @@
+// kvr_emulate.cpp -- test harness: runs the relayout kernel's work decomposition on the CPU.
+//
+// Links the library's own plan code (plan.cpp) and includes the kernel's index
+// header (kvr_index.h), then walks every CTA and thread of a launch exactly as
+// the kernel's loop does, on HOST buffers. Every computed address is checked
+// against its pool before it is used. This is how the kernel's grid and index
+// arithmetic are checked on the CPU; it is not part of the library.
+#include <stdint.h>
+#include <string.h>
+
+#include "kv_relayout.h"
+#include "kvr_index.h"
+#include "plan.h"
+
+namespace {
+
+struct Extents {
+    int64_t src_bytes, dst_bytes;
+};
+
+Extents pool_extents(const kvr_desc *d) {
+    const int64_t row = (int64_t)d->head_dim * d->elem_bytes;
+    Extents e;
+    e.src_bytes = (int64_t)d->num_layers * d->num_components * d->src_num_blocks *
+                  d->src_block_size * (d->kv_heads / d->src_tp) * row;
+    e.dst_bytes = (int64_t)d->num_layers * d->num_components * d->dst_num_blocks *
+                  d->dst_block_size * (d->kv_heads / d->dst_tp) * row;
+    return e;
+}
+
+// Walk one launch. copy != 0: move the bytes (host pools); otherwise only check.
+// Returns the number of out-of-bounds or misaligned chunk addresses (all skipped),
+// or a negative kvr_status. *chunks receives the number of chunks visited.
+int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chunks) {
+    KvrHostPlan hp;
+    kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
+    if (st != KVR_OK) return st;
+    const int all = layer < 0;
+    const int32_t slices = all ? hp.slices_all : hp.slices_layer;
+    const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), all ? 0 : layer, slices);
+    const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
+    const Extents ext = pool_extents(d);
+    int64_t bad = 0, visited = 0;
+    for (uint64_t task = 0; task < grid; ++task) {
+        int32_t l;
+        KvrItem it;
+        uint32_t q0, q1;
+        kvr_task(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
+        if (q0 > q1 || l < 0 || l >= hp.num_layers) {
+            ++bad;
+            continue;
+        }
+        for (uint32_t tid = 0; tid < KVR_THREADS; ++tid) {
+            for (uint32_t base = q0 + tid; base < q1; base += KVR_UNROLL * KVR_THREADS) {
+                for (int k = 0; k < KVR_UNROLL; ++k) {
+                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                    if (q >= q1) continue;
+                    uint32_t sp, dp;
+                    int64_t soff, doff;
+                    kvr_chunk(a.g, l, it, a.sbt, q, &sp, &soff, &dp, &doff);
+                    ++visited;
+                    if (sp >= (uint32_t)hp.src_tp || dp >= (uint32_t)hp.dst_tp || soff < 0 ||
+                        doff < 0 || soff + 16 > ext.src_bytes || doff + 16 > ext.dst_bytes ||
+                        ((uintptr_t)hp.src[sp] + soff) % 16 != 0 ||
+                        ((uintptr_t)hp.dst[dp] + doff) % 16 != 0) {
+                        ++bad;
+                        continue;
+                    }
+                    if (copy)
+                        memcpy((unsigned char *)hp.dst[dp] + doff,
+                               (const unsigned char *)hp.src[sp] + soff, 16);
+                }
+            }
+        }
+    }
+    if (chunks) *chunks = visited;
+    return bad;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Relayout on host pools through the kernel's decomposition. layer < 0: all layers.
+int64_t emu_relayout(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
+    return walk(d, sm_count, layer, 1, chunks);
+}
+
+// Bounds/alignment check of every address of a launch (pools are never touched).
+int64_t emu_check(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
+    return walk(d, sm_count, layer, 0, chunks);
+}
+
+// Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer].
+int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
+    KvrHostPlan hp;
+    kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
+    if (st != KVR_OK) return st;
+    const int64_t n = (int64_t)hp.items.size();
+    out[0] = n;
+    out[1] = hp.slices_all;
+    out[2] = hp.slices_layer;
+    out[3] = n * hp.slices_all * hp.num_layers;
+    out[4] = n * hp.slices_layer;
+    return 0;
+}
+
+// KvrDiv against the hardware divide for one divisor, at the dividends most
+// likely to break a multiply-shift division (around multiples of d, the top of
+// the 31-bit range) plus a strided sweep. Returns the number of mismatches.
+int64_t emu_fastdiv_check_one(uint32_t d, uint32_t stride) {
+    int64_t bad = 0;
+    const KvrDiv f = kvr_make_div(d);
+    auto chk = [&](uint64_t n) {
+        if (n >= (1ull << 31)) return;
+        if (f.div((uint32_t)n) != (uint32_t)n / d) ++bad;
+    };
+    for (uint64_t k = 0; k < 64; ++k) {
+        chk(k);
+        chk(k * d);
+        chk(k * d + d - 1);
+        chk(k * d + 1);
+    }
+    const uint64_t top = (1ull << 31) - 1;
+    for (uint64_t k = 0; k < 64 && k <= top / d; ++k) {
+        const uint64_t m = (top / d - k) * d;
+        chk(m);
+        chk(m + d - 1);
+        if (m) chk(m - 1);
+        chk(top - k);
+    }
+    for (uint64_t n = d; n < (1ull << 31); n += (uint64_t)stride + d) chk(n);
+    return bad;
+}
+
+// Divisors 1..d_max.
+int64_t emu_fastdiv_check(uint32_t d_max, uint32_t stride) {
+    int64_t bad = 0;
+    for (uint32_t d = 1; d <= d_max; ++d) bad += emu_fastdiv_check_one(d, stride);
+    return bad;
+}
+}

@@ -1,0 +1,134 @@
+"""GPU behaviour of the C ABI: errors are statuses, streams, graphs, repeated launches."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from gpu_util import run, to_device, to_host
+from prefill_decode_paged_gb300 import KVRelayoutError, RelayoutPlan
+
+pytestmark = pytest.mark.gpu
+
+
+def _small():
+    return wl.custom("api", 7, num_layers=4, num_components=2, kv_heads=8, head_dim=64,
+                     elem_bytes=2, src_tp=4, dst_tp=2, src_block=16, dst_block=64,
+                     seq_lens=[500, 3, 129])
+
+
+def _ref(w, src_np):
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src_np, ref, **w.geometry())
+    return ref
+
+
+def test_bad_calls_return_statuses_and_leave_the_context_usable():
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        for bad in (-1, w.num_layers, 1 << 30):
+            with pytest.raises(KVRelayoutError) as e:
+                plan.run_layer(bad)
+            assert e.value.name == "KVR_ERR_LAYER_RANGE"
+    g = w.geometry()
+    g["dst_bt"] = w.dst_bt.copy()
+    g["dst_bt"][1] = g["dst_bt"][0]
+    with pytest.raises(KVRelayoutError) as e:
+        RelayoutPlan(src, dst, **g)
+    assert e.value.name == "KVR_ERR_DST_ALIAS"
+    with pytest.raises(KVRelayoutError) as e:
+        RelayoutPlan(src, [dst[0], dst[0]], **w.geometry())
+    assert e.value.name == "KVR_ERR_POOL_OVERLAP"
+    misaligned = [src[0].view(torch.uint8)[8:].data_ptr()] + [t.data_ptr() for t in src[1:]]
+    with pytest.raises(KVRelayoutError) as e:
+        RelayoutPlan(misaligned, dst, **w.geometry())
+    assert e.value.name == "KVR_ERR_ALIGNMENT"
+    run(w, src, dst)
+    for a, b in zip(_ref(w, src_np), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)
+
+
+def test_per_layer_on_a_side_stream_in_reverse_order():
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        with torch.cuda.stream(side):
+            for layer in reversed(range(w.num_layers)):
+                plan.run_layer(layer)            # binding default: the current (side) stream
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+    for a, b in zip(_ref(w, src_np), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)
+
+
+def test_layer_launch_ordered_after_the_producer_kernel():
+    """The prefill side writes a layer with an ordinary kernel, the relayout of that
+    layer follows on the same stream: it must see the new values."""
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        for layer in range(w.num_layers):
+            for t in src:
+                t[layer].bitwise_not_()          # "compute" layer l on the prefill side
+            plan.run_layer(layer)
+        torch.cuda.synchronize()
+    flipped = [~a for a in src_np]
+    for a, b in zip(_ref(w, flipped), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)
+
+
+def test_captured_in_a_cuda_graph_and_replayed():
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    plan = RelayoutPlan(src, dst, **w.geometry())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for layer in range(w.num_layers):
+            plan.run_layer(layer)
+    for t in dst:
+        t.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(_ref(w, src_np), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)
+    plan.close()
+
+
+def test_empty_batch_and_repeated_launches():
+    import torch
+    w = wl.custom("z", 8, num_layers=2, num_components=2, kv_heads=2, head_dim=8, elem_bytes=2,
+                  src_tp=1, dst_tp=1, src_block=16, dst_block=32, seq_lens=[0, 0])
+    src = to_device(w.src_pools_numpy(), 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        assert plan.bytes_read == plan.bytes_written == 0
+        plan.run_all()
+        plan.run_layer(1)
+        torch.cuda.synchronize()
+    assert all(bool((t == -1).all()) for t in dst)
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        for _ in range(3):
+            plan.run_all()
+        torch.cuda.synchronize()
+    for a, b in zip(_ref(w, src_np), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)

@@ -1,0 +1,292 @@
+"""Host-side tests of the C ABI (no GPU): exports, validation, byte counts, and the
+kernel's work decomposition walked on the CPU against the oracle."""
+import ctypes
+import dataclasses
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from cases import CASES
+from kvcheck import check_dst, expected_from_src
+from prefill_decode_paged_gb300 import build as kbuild
+from prefill_decode_paged_gb300 import kv_relayout as kr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kv_relayout.h")
+EMU_SRC = os.path.join(ROOT, "tests", "csrc", "kvr_emulate.cpp")
+EMU_LIB = os.path.join(ROOT, "tests", "_build", "libkvr_emulate.so")
+SMS = 152
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    kbuild.build()
+    return kr.library()
+
+
+@pytest.fixture(scope="session")
+def emu():
+    os.makedirs(os.path.dirname(EMU_LIB), exist_ok=True)
+    srcs = [EMU_SRC, os.path.join(kbuild.CSRC, "plan.cpp")]
+    stale = not os.path.exists(EMU_LIB) or any(
+        os.path.getmtime(f) > os.path.getmtime(EMU_LIB)
+        for f in kbuild._inputs() + [EMU_SRC])
+    if stale:
+        subprocess.run(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-I", kbuild.INCLUDE,
+                        "-I", kbuild.CSRC, *srcs, "-o", EMU_LIB], check=True)
+    lib = ctypes.CDLL(EMU_LIB)
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.emu_relayout.restype = i64
+    lib.emu_relayout.argtypes = [p, ctypes.c_int, i32, p]
+    lib.emu_check.restype = i64
+    lib.emu_check.argtypes = [p, ctypes.c_int, i32, p]
+    lib.emu_plan_info.restype = i32
+    lib.emu_plan_info.argtypes = [p, ctypes.c_int, p]
+    lib.emu_fastdiv_check.restype = i64
+    lib.emu_fastdiv_check.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    lib.emu_fastdiv_check_one.restype = i64
+    lib.emu_fastdiv_check_one.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv_relayout_\w+)\s*\(", text)))
+
+
+def fake_pools(w, base=1 << 40, gap=1 << 20):
+    """Distinct, non-overlapping, 16-B aligned device addresses (never dereferenced)."""
+    src, dst, at = [], [], base
+    for _ in range(w.src_tp):
+        src.append(at)
+        at += (w.src_pool_bytes() + gap) // 256 * 256 + 256
+    for _ in range(w.dst_tp):
+        dst.append(at)
+        at += (w.dst_pool_bytes() + gap) // 256 * 256 + 256
+    return src, dst
+
+
+def status_of(fn):
+    try:
+        fn()
+    except kr.KVRelayoutError as e:
+        return e.name
+    return "KVR_OK"
+
+
+# -- exports ---------------------------------------------------------------------
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    names = declared_functions()
+    assert set(names) == set(kr.EXPORTS)
+    for n in names:
+        assert hasattr(cuda_lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", kr.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kv_relayout_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_strerror_names_every_status(cuda_lib):
+    for code in kr.STATUS:
+        assert cuda_lib.kv_relayout_strerror(code)
+    assert cuda_lib.kv_relayout_strerror(12345) == b"unknown status"
+
+
+# -- validation (host only: kv_relayout_desc_bytes never touches the device) -----
+
+def _geo(w, **over):
+    g = w.geometry()
+    g.update(over)
+    return g
+
+
+def test_desc_bytes_are_the_pages_kv_per_token_times_length(cuda_lib):
+    for name, per_token in (("llama70b", 327680), ("qwen32k", 262144), ("dsv3mla", 70272),
+                            ("llama8b", 131072)):
+        w = wl.get(name)
+        s, d = fake_pools(w)
+        r, wr = kr.desc_bytes(s, d, **w.geometry())
+        assert r == wr == per_token * int(w.seq_lens.sum())
+    w = wl.llama70b()
+    s, d = fake_pools(w)
+    assert kr.desc_bytes(s, d, **w.geometry())[0] == 1_342_177_280
+
+
+def test_every_error_is_a_status(cuda_lib):
+    w = wl.custom("v", 5, num_layers=2, num_components=2, kv_heads=8, head_dim=64, elem_bytes=2,
+                  src_tp=4, dst_tp=8, src_block=16, dst_block=32, seq_lens=[100, 40, 0])
+    s, d = fake_pools(w)
+    ok = lambda **o: (lambda: kr.desc_bytes(o.pop("src", s), o.pop("dst", d), **_geo(w, **o)))
+    assert status_of(ok()) == "KVR_OK"
+    # scalar ranges
+    assert status_of(ok(num_layers=0)) == "KVR_ERR_INVALID_ARG"
+    assert status_of(ok(num_components=3)) == "KVR_ERR_INVALID_ARG"
+    assert status_of(ok(src_block=0)) == "KVR_ERR_INVALID_ARG"
+    assert status_of(ok(dst_num_blocks=0)) == "KVR_ERR_INVALID_ARG"
+    assert status_of(ok(elem_bytes=3)) == "KVR_ERR_UNSUPPORTED"
+    assert status_of(ok(elem_bytes=8)) == "KVR_ERR_UNSUPPORTED"
+    assert status_of(ok(dst_tp=3, dst=d[:3])) == "KVR_ERR_UNSUPPORTED"       # 8 % 3
+    assert status_of(ok(kv_heads=32, src_tp=32)) == "KVR_ERR_UNSUPPORTED"    # > KVR_MAX_TP
+    # alignment
+    assert status_of(ok(head_dim=4)) == "KVR_ERR_ALIGNMENT"                  # 8-byte rows
+    assert status_of(ok(src=[s[0] + 8] + s[1:])) == "KVR_ERR_ALIGNMENT"
+    assert status_of(ok(dst=d[:7] + [d[7] + 4])) == "KVR_ERR_ALIGNMENT"
+    # null pools
+    assert status_of(ok(src=s[:3] + [0])) == "KVR_ERR_INVALID_ARG"
+    # tables
+    lens = w.seq_lens.copy(); lens[1] = -1
+    assert status_of(ok(seq_lens=lens)) == "KVR_ERR_INVALID_ARG"
+    lens = w.seq_lens.copy(); lens[0] = 200                                  # table too short
+    assert status_of(ok(seq_lens=lens)) == "KVR_ERR_TABLE_SHORT"
+    soff = w.src_off.copy(); soff[2] = soff[1] - 1
+    assert status_of(ok(src_off=soff)) == "KVR_ERR_INVALID_ARG"
+    sbt = w.src_bt.copy(); sbt[3] = w.src_num_blocks
+    assert status_of(ok(src_bt=sbt)) == "KVR_ERR_BLOCK_RANGE"
+    dbt = w.dst_bt.copy(); dbt[0] = -1
+    assert status_of(ok(dst_bt=dbt)) == "KVR_ERR_BLOCK_RANGE"
+    dbt = w.dst_bt.copy(); dbt[w.dst_off[1]] = dbt[0]                        # two requests
+    assert status_of(ok(dst_bt=dbt)) == "KVR_ERR_DST_ALIAS"
+    dbt = w.dst_bt.copy(); dbt[1] = dbt[0]                                   # one request
+    assert status_of(ok(dst_bt=dbt)) == "KVR_ERR_DST_ALIAS"
+    # pool overlaps
+    assert status_of(ok(dst=[d[0]] * 8)) == "KVR_ERR_POOL_OVERLAP"
+    assert status_of(ok(dst=[s[1]] + d[1:])) == "KVR_ERR_POOL_OVERLAP"
+    assert status_of(ok(dst=[s[0] + 16] + d[1:])) == "KVR_ERR_POOL_OVERLAP"
+
+
+def test_permitted_edge_cases(cuda_lib):
+    w = wl.custom("e", 6, num_layers=2, num_components=2, kv_heads=8, head_dim=64, elem_bytes=2,
+                  src_tp=4, dst_tp=8, src_block=16, dst_block=32, seq_lens=[96, 40, 0])
+    s, d = fake_pools(w)
+    # reserved-but-unused decode entries may be anything, prefill ids may repeat
+    assert w.dst_off[1] == 4 and w.dst_off[3] - w.dst_off[2] == 1
+    dbt = w.dst_bt.copy()
+    dbt[w.dst_off[1] - 1] = 10 ** 6          # request 0: the block reserved for token 97
+    dbt[w.dst_off[3] - 1] = dbt[0]           # request 2 (empty prompt): its reserved block
+    assert status_of(lambda: kr.desc_bytes(s, d, **_geo(w, dst_bt=dbt))) == "KVR_OK"
+    sbt = w.src_bt.copy(); sbt[w.src_off[1]] = sbt[0]
+    assert status_of(lambda: kr.desc_bytes(s, d, **_geo(w, src_bt=sbt))) == "KVR_OK"
+    # prefill pools may overlap each other (read only)
+    assert status_of(lambda: kr.desc_bytes([s[0]] * 4, d, **w.geometry())) == "KVR_OK"
+    # empty batch and all-zero lengths
+    e = dict(w.geometry(), seq_lens=[], src_off=[0], src_bt=[], dst_off=[0], dst_bt=[])
+    assert kr.desc_bytes(s, d, **e) == (0, 0)
+    z = dict(w.geometry(), seq_lens=[0, 0], src_off=[0, 0, 0], src_bt=[], dst_off=[0, 0, 0],
+             dst_bt=[])
+    assert kr.desc_bytes(s, d, **z) == (0, 0)
+
+
+def test_plan_without_a_gpu_fails_loudly(cuda_lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    w = wl.tiny()
+    s, d = fake_pools(w)
+    with pytest.raises(kr.KVRelayoutError) as e:
+        kr.RelayoutPlan(s, d, **w.geometry())
+    assert e.value.name == "KVR_ERR_CUDA"
+
+
+# -- the kernel's decomposition, walked on the CPU ----------------------------------
+
+def _host_desc(w, src, dst):
+    return kr._Desc([a.ctypes.data for a in src], [a.ctypes.data for a in dst], **w.geometry())
+
+
+def _emu_run(emu, w, src, dst, layer=-1, sms=SMS):
+    d = _host_desc(w, src, dst)
+    n = ctypes.c_int64()
+    bad = emu.emu_relayout(ctypes.byref(d.desc), sms, layer, ctypes.byref(n))
+    assert bad == 0, f"{bad} chunk addresses out of bounds or misaligned"
+    return n.value
+
+
+def _aligned(shape, dtype):
+    """Host array whose data starts on a 16-byte boundary (as device pools do)."""
+    nbytes = int(np.prod(shape)) * np.dtype(dtype).itemsize
+    raw = np.empty(nbytes + 16, dtype=np.uint8)
+    off = (-raw.ctypes.data) % 16
+    return raw[off:off + nbytes].view(dtype).reshape(shape)
+
+
+def _pools(w, filled):
+    out = []
+    for a in filled:
+        b = _aligned(a.shape, a.dtype)
+        b[...] = a
+        out.append(b)
+    return out
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("sms", [1, SMS])
+def test_emulated_kernel_matches_oracle(emu, case, sms):
+    w = CASES[case]()
+    src = _pools(w, w.src_pools_numpy())
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src, ref, **w.geometry())
+    whole = _pools(w, w.dst_pools_numpy())
+    n = _emu_run(emu, w, src, whole, sms=sms)
+    assert n * 16 == oracle.transfer_bytes(w.num_layers, w.num_components, w.kv_heads,
+                                           w.head_dim, w.elem_bytes, w.seq_lens)
+    for a, b in zip(ref, whole):
+        np.testing.assert_array_equal(a, b)
+    per = _pools(w, w.dst_pools_numpy())
+    for l in range(w.num_layers):
+        _emu_run(emu, w, src, per, layer=l, sms=sms)
+    for a, b in zip(ref, per):
+        np.testing.assert_array_equal(a, b)
+    check_dst(w, whole, expected_from_src(w, src), w._sentinel_value(0xFF))
+
+
+@pytest.mark.parametrize("name", ["llama8b", "llama70b", "qwen32k", "qwen32k_ragged",
+                                  "dsv3mla"])
+def test_full_size_launches_stay_in_bounds(emu, name):
+    """Every address of the full-size launches, against the full pool extents.
+
+    The whole-prompt launch is walked in full for the 70B workload; for the
+    others the per-layer launches of the first and last layer are walked (the
+    layer only adds a plane offset, so these bound every layer), plus the
+    whole-prompt launch of a two-layer copy of the same batch.
+    """
+    w = wl.get(name)
+    s, d = fake_pools(w)
+    desc = kr._Desc(s, d, **w.geometry())
+    per_layer = w.seq_lens.sum() * w.num_components * w.kv_heads * w.head_dim * w.elem_bytes
+    n = ctypes.c_int64()
+    layers = [-1] if name == "llama70b" else [0, w.num_layers - 1]
+    for l in layers:
+        assert emu.emu_check(ctypes.byref(desc.desc), SMS, l, ctypes.byref(n)) == 0
+        assert n.value * 16 == (per_layer * (w.num_layers if l < 0 else 1))
+    w2 = w.with_layers(2)
+    s2, d2 = fake_pools(w2)
+    desc2 = kr._Desc(s2, d2, **w2.geometry())
+    assert emu.emu_check(ctypes.byref(desc2.desc), SMS, -1, ctypes.byref(n)) == 0
+    assert n.value * 16 == per_layer * 2
+
+
+def test_fast_division_matches_hardware_division(emu):
+    assert emu.emu_fastdiv_check(4096, 1 << 22) == 0
+    for d in (4097, 12345, 65535, 65536, 65537, 1 << 20, (1 << 20) + 1, 3 << 28,
+              (1 << 30) + 3, (1 << 31) - 1):
+        assert emu.emu_fastdiv_check_one(d, 1 << 16) == 0, d
+
+
+def test_launch_shapes(emu):
+    """Per-layer launches are sliced to fill the GPU; whole-prompt launches are not."""
+    info = (ctypes.c_int64 * 5)()
+    for name, n_items in (("llama70b", 128), ("qwen32k", 2048)):
+        w = wl.get(name)
+        s, d = fake_pools(w)
+        desc = kr._Desc(s, d, **w.geometry())
+        assert emu.emu_plan_info(ctypes.byref(desc.desc), SMS, info) == 0
+        assert info[0] == n_items
+        assert info[4] >= SMS                      # a per-layer launch covers every SM
+        assert info[3] == n_items * w.num_layers * info[1]
