@@ -79,6 +79,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="CPU seconds for the oracle baseline sample")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--modes", default="all,layer,graph",
+                   help="measurements to run: all (whole-prompt, the step), layer (per-layer "
+                        "eager launches), graph (per-layer launches replayed from a CUDA graph)")
     return p.parse_args(argv)
 
 
@@ -320,23 +323,26 @@ def run_ours(args):
     K = args.steps
     # whole-prompt: one launch per step
     ms_all = timed(lambda: plan.run_all(stream), K)
-    # per-layer, eager: L launches per step from Python
+    modes = set(args.modes.split(","))
     L = w.num_layers
-
-    def per_layer():
-        for layer in range(L):
-            plan.run_layer(layer, stream)
+    ms_layer = ms_graph = None
     k_layer = max(1, K // 4)
-    ms_layer = timed(per_layer, k_layer)
-    # per-layer, the L launches captured once in a CUDA graph and replayed
-    g = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.graph(g, stream=cap):
-        for layer in range(L):
-            plan.run_layer(layer)
-    stream.wait_stream(cap)
-    ms_graph = timed(g.replay, K)
+    if "layer" in modes:
+        # per-layer, eager: L launches per step from Python
+        def per_layer():
+            for layer in range(L):
+                plan.run_layer(layer, stream)
+        ms_layer = timed(per_layer, k_layer)
+    if "graph" in modes:
+        # per-layer, the L launches captured once in a CUDA graph and replayed
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for layer in range(L):
+                plan.run_layer(layer)
+        stream.wait_stream(cap)
+        ms_graph = timed(g.replay, K)
 
     # e2e: pools in pinned host memory, copies and plan creation inside the region
     e2e = None
@@ -408,8 +414,6 @@ def run_ours(args):
     traffic, _ = profiled_traffic(args.config, w.num_layers)
     prompts = w.num_requests
     value = whole_job_gbs(bytes_step, K, world, ms_all * 1e-3)
-    layer_gbs = whole_job_gbs(bytes_step, k_layer, world, ms_layer * 1e-3)
-    graph_gbs = whole_job_gbs(bytes_step, K, world, ms_graph * 1e-3)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -434,13 +438,16 @@ def run_ours(args):
         "pct_of_hbm_peak": round(100 * achieved / hbm_peak, 2),
         "pct_of_nominal_hbm": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "per_layer": {
-            "eager": {"gbs": round(layer_gbs, 2), "ms_per_prompt": round(ms_layer / k_layer, 5),
-                      "us_per_launch": round(ms_layer * 1e3 / k_layer / L, 3),
-                      "launches_per_step": L, "steps": k_layer},
-            "cuda_graph": {"gbs": round(graph_gbs, 2),
-                           "ms_per_prompt": round(ms_graph / K, 5),
-                           "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
-                           "launches_per_step": L, "steps": K},
+            "eager": None if ms_layer is None else {
+                "gbs": round(whole_job_gbs(bytes_step, k_layer, world, ms_layer * 1e-3), 2),
+                "ms_per_prompt": round(ms_layer / k_layer / prompts, 5),
+                "us_per_launch": round(ms_layer * 1e3 / k_layer / L, 3),
+                "launches_per_step": L, "steps": k_layer},
+            "cuda_graph": None if ms_graph is None else {
+                "gbs": round(whole_job_gbs(bytes_step, K, world, ms_graph * 1e-3), 2),
+                "ms_per_prompt": round(ms_graph / K / prompts, 5),
+                "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
+                "launches_per_step": L, "steps": K},
         },
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,

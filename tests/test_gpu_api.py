@@ -42,7 +42,7 @@ def test_bad_calls_return_statuses_and_leave_the_context_usable():
     with pytest.raises(KVRelayoutError) as e:
         RelayoutPlan(src, [dst[0], dst[0]], **w.geometry())
     assert e.value.name == "KVR_ERR_POOL_OVERLAP"
-    misaligned = [src[0].view(torch.uint8)[8:].data_ptr()] + [t.data_ptr() for t in src[1:]]
+    misaligned = [src[0].data_ptr() + 8] + [t.data_ptr() for t in src[1:]]
     with pytest.raises(KVRelayoutError) as e:
         RelayoutPlan(misaligned, dst, **w.geometry())
     assert e.value.name == "KVR_ERR_ALIGNMENT"
