@@ -67,7 +67,8 @@ typedef enum kvr_status {
     KVR_ERR_LAYER_RANGE = -7,   /* layer outside [0, num_layers) */
     KVR_ERR_CUDA = -8,          /* a CUDA runtime call failed (no device, launch error, ...) */
     KVR_ERR_NOMEM = -9,         /* host or device allocation of the plan failed */
-    KVR_ERR_POOL_OVERLAP = -10  /* a decode pool overlaps another decode pool or a prefill pool */
+    KVR_ERR_POOL_OVERLAP = -10, /* a decode pool overlaps another decode pool or a prefill pool */
+    KVR_ERR_SCRATCH_LIMIT = -11 /* kv_relayout_all_prealloc: work list larger than its scratch */
 } kvr_status;
 
 typedef struct kvr_desc {
@@ -132,6 +133,39 @@ void kv_relayout_plan_destroy(kvr_plan *plan);
 
 /* Static, human-readable name of a status. */
 const char *kv_relayout_strerror(kvr_status status);
+
+/* Size of the device scratch array kv_relayout_all_prealloc() works in. */
+#define KVR_PREALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * kv_relayout_all(), for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this call; it exists for integration.
+ * Some callers cannot call cudaMalloc when they hand KV over: a serving
+ * engine that has carved (nearly) all of HBM into its KV block pools up front
+ * has no room left for a new allocation, and a latency-critical loop cannot
+ * afford cudaMalloc/cudaFree, which may synchronize the whole device and so
+ * stall the other streams. kv_relayout_plan() allocates a small device buffer
+ * for the work list; this call allocates nothing: it validates *desc exactly
+ * like kv_relayout_plan(), copies the work list (16 bytes per request and
+ * decode block) and the used prefill block ids (4 bytes each) into a
+ * fixed device array of KVR_PREALLOC_SCRATCH_BYTES (1 MiB) that the library
+ * reserves on every GPU that loads it, until the process exits, and launches
+ * the same kernel as kv_relayout_all() on `stream` (asynchronous).
+ *
+ *  - A work list larger than the array is rejected with
+ *    KVR_ERR_SCRATCH_LIMIT before anything is copied or launched; use
+ *    kv_relayout_plan() for such batches.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (with the device current) and caches it; make that first call
+ *    before any stream capture begins.
+ *  - Every call on a device shares the one array. Calls whose copies and
+ *    kernels overlap on the GPU (different streams, not ordered by the
+ *    caller) race on it and may move the wrong rows: issue them on one stream
+ *    or order them with events.
+ *  - The host arrays of *desc may be freed when the call returns.
+ */
+kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *stream);
 
 #ifdef __cplusplus
 }

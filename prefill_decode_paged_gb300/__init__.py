@@ -5,6 +5,8 @@ Public API (see ``include/kv_relayout.h`` for the C ABI it binds):
 * :class:`RelayoutPlan` -- validate a batch and upload its work list;
   ``run_all()`` moves every layer in one launch, ``run_layer(l)`` one layer.
 * :func:`desc_bytes` -- host-only validation and byte count.
+* :func:`relayout_all_prealloc` -- ``run_all`` without any device allocation, for
+  callers that cannot allocate (work lists up to 1 MiB).
 """
 from .kv_relayout import (KVRelayoutError, RelayoutPlan, desc_bytes, library,  # noqa: F401
-                          LIB_PATH, STATUS, EXPORTS)
+                          LIB_PATH, STATUS, EXPORTS, relayout_all_prealloc)

@@ -246,6 +246,7 @@ extern "C" const char *kv_relayout_strerror(kvr_status s) {
         case KVR_ERR_CUDA: return "CUDA runtime error";
         case KVR_ERR_NOMEM: return "out of memory";
         case KVR_ERR_POOL_OVERLAP: return "decode pool overlaps another pool";
+        case KVR_ERR_SCRATCH_LIMIT: return "work list larger than the preallocated scratch";
     }
     return "unknown status";
 }

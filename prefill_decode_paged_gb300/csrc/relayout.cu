@@ -175,3 +175,98 @@ extern "C" void kv_relayout_plan_destroy(kvr_plan *plan) {
     if (plan->dev_meta != nullptr) cudaFree(plan->dev_meta);
     delete plan;
 }
+
+// ---------------------------------------------------------------------------
+// kv_relayout_all_prealloc: the whole-prompt relayout without any device
+// allocation. The kernel's scratch (the work list and the used prefill block
+// ids, normally in the plan's cudaMalloc'd buffer) lives in the file-scope
+// array below instead. Every GPU that loads this library holds the array
+// until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+#define KVR_PREALLOC_MAX_DEVICES 64
+
+static __device__ __align__(256) unsigned char g_kvr_prealloc_scratch[KVR_PREALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct PreallocScratch {
+    bool ready = false;
+    unsigned char *addr = nullptr;   // device address of g_kvr_prealloc_scratch
+    int sms = 0;
+};
+
+PreallocScratch g_prealloc[KVR_PREALLOC_MAX_DEVICES];
+std::mutex g_prealloc_mu;
+
+// Once per device, with that device current: the array's device address. In
+// host code the array's name is only a host-side stand-in, so the kernel must
+// be given this address, never the name.
+kvr_status prealloc_setup(int dev, PreallocScratch *out) {
+    std::lock_guard<std::mutex> lock(g_prealloc_mu);
+    PreallocScratch &s = g_prealloc[dev];
+    if (!s.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kvr_prealloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return KVR_ERR_CUDA;
+        }
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return KVR_ERR_CUDA;
+        s.addr = (unsigned char *)p;
+        s.sms = sms;
+        s.ready = true;
+    }
+    *out = s;
+    return KVR_OK;
+}
+
+}  // namespace
+
+extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
+    if (dev < 0 || dev >= KVR_PREALLOC_MAX_DEVICES) return KVR_ERR_UNSUPPORTED;
+    PreallocScratch sc;
+    kvr_status st = prealloc_setup(dev, &sc);
+    if (st != KVR_OK) return st;
+
+    KvrHostPlan hp;
+    try {
+        st = kvr_build_host_plan(desc, sc.sms, &hp, nullptr);
+    } catch (...) {
+        st = KVR_ERR_NOMEM;
+    }
+    if (st != KVR_OK) return st;
+    const size_t items_bytes = hp.items.size() * sizeof(KvrItem);
+    const size_t sbt_bytes = hp.sbt.size() * sizeof(int32_t);
+    if (items_bytes + sbt_bytes > KVR_PREALLOC_SCRATCH_BYTES) return KVR_ERR_SCRATCH_LIMIT;
+    if (items_bytes == 0) return KVR_OK;
+
+    // The whole array is overwritten up to what this call reads, so nothing
+    // needs clearing; the copies are ordered before the launch on `stream`.
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(sc.addr, hp.items.data(), items_bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(sc.addr + items_bytes, hp.sbt.data(), sbt_bytes,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return KVR_ERR_CUDA;
+
+    const KvrArgs a = kvr_launch_args(hp, (const KvrItem *)sc.addr,
+                                      (const int32_t *)(sc.addr + items_bytes), 0, hp.slices_all);
+    const uint64_t grid = (uint64_t)hp.num_layers * a.tasks_per_layer;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(KVR_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel, a) == cudaSuccess ? KVR_OK
+                                                                            : KVR_ERR_CUDA;
+}

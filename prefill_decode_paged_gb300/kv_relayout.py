@@ -20,11 +20,12 @@ STATUS = {
     0: "KVR_OK", -1: "KVR_ERR_INVALID_ARG", -2: "KVR_ERR_UNSUPPORTED",
     -3: "KVR_ERR_ALIGNMENT", -4: "KVR_ERR_BLOCK_RANGE", -5: "KVR_ERR_TABLE_SHORT",
     -6: "KVR_ERR_DST_ALIAS", -7: "KVR_ERR_LAYER_RANGE", -8: "KVR_ERR_CUDA",
-    -9: "KVR_ERR_NOMEM", -10: "KVR_ERR_POOL_OVERLAP",
+    -9: "KVR_ERR_NOMEM", -10: "KVR_ERR_POOL_OVERLAP", -11: "KVR_ERR_SCRATCH_LIMIT",
 }
+PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_all", "kv_relayout_plan_bytes", "kv_relayout_plan_destroy",
-           "kv_relayout_strerror")
+           "kv_relayout_strerror", "kv_relayout_all_prealloc")
 
 
 class KVRelayoutError(RuntimeError):
@@ -76,6 +77,8 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_plan_destroy.argtypes = [p]
         lib.kv_relayout_strerror.restype = ctypes.c_char_p
         lib.kv_relayout_strerror.argtypes = [i32]
+        lib.kv_relayout_all_prealloc.restype = i32
+        lib.kv_relayout_all_prealloc.argtypes = [p, p]
         _lib = lib
     return _lib
 
@@ -136,6 +139,24 @@ def desc_bytes(src_pools, dst_pools, **geometry):
     if st != 0:
         raise KVRelayoutError(st, "kv_relayout_desc_bytes")
     return r.value, w.value
+
+
+def relayout_all_prealloc(src_pools, dst_pools, stream=None, **geometry):
+    """All layers in one launch without any device allocation.
+
+    For callers that cannot call cudaMalloc while handing KV over (an engine
+    whose HBM is already carved into KV pools, a loop that cannot afford the
+    device-wide synchronization of cudaMalloc/cudaFree). The work list goes
+    into a fixed 1 MiB device array the library keeps on every GPU it runs on;
+    larger work lists raise ``KVR_ERR_SCRATCH_LIMIT`` (use :class:`RelayoutPlan`).
+    The first call on a device sets the array up and should come before any
+    stream capture. Calls share the array: calls that overlap on the GPU (on
+    different, unordered streams) race.
+    """
+    d = _Desc(src_pools, dst_pools, **geometry)
+    st = library().kv_relayout_all_prealloc(ctypes.byref(d.desc), _stream_handle(stream))
+    if st != 0:
+        raise KVRelayoutError(st, "kv_relayout_all_prealloc")
 
 
 def _stream_handle(stream) -> int | None:
