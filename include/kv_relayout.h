@@ -147,8 +147,8 @@ const char *kv_relayout_strerror(kvr_status status);
  * afford cudaMalloc/cudaFree, which may synchronize the whole device and so
  * stall the other streams. kv_relayout_plan() allocates a small device buffer
  * for the work list; this call allocates nothing: it validates *desc exactly
- * like kv_relayout_plan(), copies the work list (16 bytes per request and
- * decode block) and the used prefill block ids (4 bytes each) into a
+ * like kv_relayout_plan(), copies the work list (16 bytes per token tile of
+ * a request) and the used prefill and decode block ids (4 bytes each) into a
  * fixed device array of KVR_PREALLOC_SCRATCH_BYTES (1 MiB) that the library
  * reserves on every GPU that loads it, until the process exits, and launches
  * the same kernel as kv_relayout_all() on `stream` (asynchronous).

@@ -4,13 +4,17 @@
 // construction; the test emulator that walks every launch on the CPU), so it
 // holds plain structs and inline functions only.
 //
-// Work decomposition. A work ITEM is one (request, decode logical block j):
-// the request's tokens [j*Bd, j*Bd + ntok), ntok = min(Bd, n - j*Bd), for all
-// components and all KV heads. One launch covers (layers of the launch) x
-// items x slices TASKS, one CTA per task; a slice is a contiguous part of the
-// item's 16-byte chunks, so a per-layer launch with few items still fills the
-// GPU. Inside an item, chunk q is ordered [token o][component c][head h]
-// [chunk of the head row], so consecutive threads read and write consecutive
+// Work decomposition. A work ITEM is one tile of one request's tokens,
+// [t0, t0 + ntok), for all components and all KV heads. Tiles start at
+// multiples of the tile size T, itself a multiple of the decode block size
+// Bd (T = Bd unless decode blocks are small, then several decode blocks per
+// tile). One launch covers (layers of the launch) x items x slices TASKS, one
+// CTA per task; a slice is a contiguous part of the item's 16-byte chunks, so
+// a per-layer launch with few items still fills the GPU.
+//
+// Inside an item, ROW r (one head row of D * es bytes) is ordered
+// [token o][component c][head h], and chunk q = r * row_chunks + k is the
+// k-th 16-byte piece of row r. Consecutive threads read and write consecutive
 // 16-byte pieces of one head row, and the rows of one token follow each other.
 #pragma once
 
@@ -52,19 +56,19 @@ inline KvrDiv kvr_make_div(uint32_t d) {
     return r;
 }
 
-// One work item: a decode logical block of one request. 16 bytes.
+// One work item: a token tile of one request. 16 bytes.
 struct KvrItem {
     int32_t sbt_off;    // index of the request's first prefill block id in the flat table
-    int32_t dst_block;  // physical decode block id
-    int32_t t0;         // first token of the item (a multiple of Bd)
-    int32_t ntok;       // tokens in the item, 1..Bd
+    int32_t dbt_off;    // index of the request's first decode block id in the flat table
+    int32_t t0;         // first token of the tile (a multiple of the tile size)
+    int32_t ntok;       // tokens in the tile, >= 1
 };
 
 struct KvrGeom {
     int32_t C, H, Hp, Hd, Bp, Bd;
     int32_t row_bytes;          // D * es, a multiple of 16
     int32_t row_chunks;         // row_bytes / 16
-    KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp;
+    KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp, div_Bd;
     int64_t src_blk_bytes;      // Bp * Hp * row_bytes
     int64_t dst_blk_bytes;      // Bd * Hd * row_bytes
     int64_t src_plane_bytes;    // Np * src_blk_bytes: one (layer, component) plane
@@ -76,6 +80,7 @@ struct KvrArgs {
     KvrGeom g;
     const KvrItem *items;
     const int32_t *sbt;                 // flat prefill block ids
+    const int32_t *dbt;                 // flat decode block ids
     const unsigned char *src[KVR_MAX_TP];
     unsigned char *dst[KVR_MAX_TP];
     int32_t layer0;                     // first layer of this launch
@@ -84,7 +89,7 @@ struct KvrArgs {
     KvrDiv div_tasks_per_layer, div_slices;
 };
 
-// Task -> (layer, item index, chunk range [q0, q1) of the item).
+// Task -> (layer, item, chunk range [q0, q1) of the item).
 KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,
                      KvrItem *item, uint32_t *q0, uint32_t *q1) {
     const uint32_t lt = a.div_tasks_per_layer.div(task);
@@ -99,20 +104,24 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
 }
 
-// Chunk q of an item -> (prefill shard, byte offset) and (decode shard, byte offset).
-KVR_HD void kvr_chunk(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
-                      uint32_t q, uint32_t *sp, int64_t *soff, uint32_t *dp, int64_t *doff) {
-    const uint32_t row = g.div_rc.div(q);
-    const uint32_t ch = q - row * (uint32_t)g.row_chunks;
-    const uint32_t oc = g.div_H.div(row);
-    const uint32_t h = row - oc * (uint32_t)g.H;
+// Row r of an item -> (prefill shard, byte offset of the row) and
+// (decode shard, byte offset of the row).
+KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
+                    const int32_t *dbt, uint32_t r, uint32_t *sp, int64_t *soff, uint32_t *dp,
+                    int64_t *doff) {
+    const uint32_t oc = g.div_H.div(r);
+    const uint32_t h = r - oc * (uint32_t)g.H;
     const uint32_t o = g.div_C.div(oc);
     const uint32_t c = oc - o * (uint32_t)g.C;
-    // prefill side: logical block t / Bp of the request, row t % Bp in it
     const uint32_t t = (uint32_t)it.t0 + o;
+    // prefill side: logical block t / Bp of the request, row t % Bp in it
     const uint32_t sbi = g.div_Bp.div(t);
     const uint32_t so = t - sbi * (uint32_t)g.Bp;
     const int64_t sb = sbt[it.sbt_off + (int32_t)sbi];
+    // decode side: logical block t / Bd, row t % Bd
+    const uint32_t dbi = g.div_Bd.div(t);
+    const uint32_t dof = t - dbi * (uint32_t)g.Bd;
+    const int64_t db = dbt[it.dbt_off + (int32_t)dbi];
     // head h: prefill shard h / Hp (local h % Hp), decode shard h / Hd (local h % Hd)
     const uint32_t s_sh = g.div_Hp.div(h);
     const uint32_t s_loc = h - s_sh * (uint32_t)g.Hp;
@@ -122,8 +131,7 @@ KVR_HD void kvr_chunk(const KvrGeom &g, int32_t layer, const KvrItem &it, const 
     *sp = s_sh;
     *dp = d_sh;
     *soff = plane * g.src_plane_bytes + sb * g.src_blk_bytes +
-            ((int64_t)so * g.Hp + s_loc) * g.row_bytes + (int64_t)ch * 16;
-    // the item starts at a decode block boundary: the decode row is o itself
-    *doff = plane * g.dst_plane_bytes + (int64_t)it.dst_block * g.dst_blk_bytes +
-            ((int64_t)o * g.Hd + d_loc) * g.row_bytes + (int64_t)ch * 16;
+            ((int64_t)so * g.Hp + s_loc) * g.row_bytes;
+    *doff = plane * g.dst_plane_bytes + db * g.dst_blk_bytes +
+            ((int64_t)dof * g.Hd + d_loc) * g.row_bytes;
 }

@@ -111,13 +111,12 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     if (st != KVR_OK) return st;
 
     // no decode block may receive two prompts' (or one prompt's two) tokens
-    int64_t tokens = 0, items = 0, used_src = 0;
+    int64_t tokens = 0, used_src = 0;
     std::vector<int32_t> used;
     try {
         for (int32_t r = 0; r < R; ++r) {
             tokens += d->seq_lens[r];
             const int64_t nd = ceil_div(d->seq_lens[r], Bd);
-            items += nd;
             used_src += ceil_div(d->seq_lens[r], Bp);
             for (int64_t k = 0; k < nd; ++k) used.push_back(d->dst_bt[d->dst_bt_offsets[r] + k]);
         }
@@ -143,8 +142,20 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     if (bytes_out) *bytes_out = bytes;
     if (hp == nullptr) return KVR_OK;
 
+    // token tiles: whole decode blocks, about KVR_TARGET_ITEM_BYTES per layer
+    const int64_t blk_bytes_all_heads = (int64_t)Bd * C * H * row_bytes;
+    int64_t per_tile = std::max<int64_t>(1, KVR_TARGET_ITEM_BYTES / blk_bytes_all_heads);
+    per_tile = std::min<int64_t>(per_tile, INT32_MAX / ((int64_t)Bd * C * H * (row_bytes / 16)));
+    const int64_t tile = std::max<int64_t>(1, per_tile) * Bd;
+
     // launch sizes: CTAs = layers x items x slices must fit a 32-bit grid
-    if (items > INT32_MAX || used_src > INT32_MAX || (int64_t)L * items > INT32_MAX)
+    int64_t n_items = 0, used_dst = 0;
+    for (int32_t r = 0; r < R; ++r) {
+        n_items += ceil_div(d->seq_lens[r], tile);
+        used_dst += ceil_div(d->seq_lens[r], Bd);
+    }
+    if (n_items > INT32_MAX || used_src > INT32_MAX || used_dst > INT32_MAX ||
+        (int64_t)L * n_items > INT32_MAX)
         return KVR_ERR_UNSUPPORTED;
 
     KvrGeom &g = hp->g;
@@ -157,6 +168,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     g.div_Hp = kvr_make_div((uint32_t)Hp);
     g.div_Hd = kvr_make_div((uint32_t)Hd);
     g.div_Bp = kvr_make_div((uint32_t)Bp);
+    g.div_Bd = kvr_make_div((uint32_t)Bd);
     g.src_blk_bytes = src_blk;
     g.dst_blk_bytes = dst_blk;
     g.src_plane_bytes = src_pool / ((int64_t)L * C);
@@ -164,6 +176,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     hp->num_layers = L;
     hp->src_tp = Tp;
     hp->dst_tp = Td;
+    hp->tile = (int32_t)tile;
     for (int32_t s = 0; s < Tp; ++s) hp->src[s] = d->src_pools[s];
     for (int32_t s = 0; s < Td; ++s) hp->dst[s] = d->dst_pools[s];
     hp->bytes = bytes;
@@ -171,20 +184,25 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     try {
         hp->items.clear();
         hp->sbt.clear();
-        hp->items.reserve((size_t)items);
+        hp->dbt.clear();
+        hp->items.reserve((size_t)n_items);
         hp->sbt.reserve((size_t)used_src);
+        hp->dbt.reserve((size_t)used_dst);
         for (int32_t r = 0; r < R; ++r) {
             const int32_t n = d->seq_lens[r];
             if (n == 0) continue;
-            const int32_t off = (int32_t)hp->sbt.size();
-            const int64_t ns = ceil_div(n, Bp);
-            for (int64_t k = 0; k < ns; ++k) hp->sbt.push_back(d->src_bt[d->src_bt_offsets[r] + k]);
-            for (int32_t j = 0; (int64_t)j * Bd < n; ++j) {
+            const int32_t soff = (int32_t)hp->sbt.size();
+            const int32_t doff = (int32_t)hp->dbt.size();
+            for (int64_t k = 0; k < ceil_div(n, Bp); ++k)
+                hp->sbt.push_back(d->src_bt[d->src_bt_offsets[r] + k]);
+            for (int64_t k = 0; k < ceil_div(n, Bd); ++k)
+                hp->dbt.push_back(d->dst_bt[d->dst_bt_offsets[r] + k]);
+            for (int64_t t0 = 0; t0 < n; t0 += tile) {
                 KvrItem it;
-                it.sbt_off = off;
-                it.dst_block = d->dst_bt[d->dst_bt_offsets[r] + j];
-                it.t0 = j * Bd;
-                it.ntok = std::min(Bd, n - j * Bd);
+                it.sbt_off = soff;
+                it.dbt_off = doff;
+                it.t0 = (int32_t)t0;
+                it.ntok = (int32_t)std::min<int64_t>(tile, n - t0);
                 hp->items.push_back(it);
             }
         }
@@ -192,7 +210,6 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
         return KVR_ERR_NOMEM;
     }
 
-    const int64_t n_items = (int64_t)hp->items.size();
     const int64_t avg_chunks = n_items ? (bytes / L / 16) / n_items : 0;
     hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count);
     hp->slices_all = choose_slices((int64_t)L * n_items, avg_chunks, sm_count);
@@ -202,12 +219,13 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
 }
 
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,
-                        int32_t layer0, int32_t slices) {
+                        const int32_t *dev_dbt, int32_t layer0, int32_t slices) {
     KvrArgs a;
     memset(&a, 0, sizeof(a));
     a.g = hp.g;
     a.items = dev_items;
     a.sbt = dev_sbt;
+    a.dbt = dev_dbt;
     for (int32_t s = 0; s < hp.src_tp; ++s) a.src[s] = (const unsigned char *)hp.src[s];
     for (int32_t s = 0; s < hp.dst_tp; ++s) a.dst[s] = (unsigned char *)hp.dst[s];
     a.layer0 = layer0;

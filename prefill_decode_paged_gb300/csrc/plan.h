@@ -8,22 +8,40 @@
 #include "kv_relayout.h"
 #include "kvr_index.h"
 
-// Launch shape of the relayout kernel.
+// Launch shape of the relayout kernel (each may be overridden at build time).
+#ifndef KVR_THREADS
 #define KVR_THREADS 256          // threads per CTA
+#endif
+#ifndef KVR_UNROLL
 #define KVR_UNROLL 8             // 16-byte loads in flight per thread before its stores
+#endif
+#ifndef KVR_ROW_WINDOW
+#define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once
+#endif
 // A launch aims at this many CTAs per SM; items are sliced until it does,
 // but no slice gets fewer than KVR_MIN_SLICE_CHUNKS 16-byte chunks.
+#ifndef KVR_TARGET_CTAS_PER_SM
 #define KVR_TARGET_CTAS_PER_SM 8
+#endif
+#ifndef KVR_MIN_SLICE_CHUNKS
 #define KVR_MIN_SLICE_CHUNKS 512
+#endif
+// Token tiles hold whole decode blocks and grow (in whole decode blocks)
+// until a tile moves about this many bytes per layer.
+#ifndef KVR_TARGET_ITEM_BYTES
+#define KVR_TARGET_ITEM_BYTES (64 * 1024)
+#endif
 
 struct KvrHostPlan {
     KvrGeom g;
     int32_t num_layers = 0;
     int32_t src_tp = 0, dst_tp = 0;
+    int32_t tile = 0;                  // tokens per work item (a multiple of Bd)
     const void *src[KVR_MAX_TP] = {};
     void *dst[KVR_MAX_TP] = {};
-    std::vector<KvrItem> items;        // (request, decode logical block) work items
+    std::vector<KvrItem> items;        // (request, token tile) work items
     std::vector<int32_t> sbt;          // used prefill block ids, request after request
+    std::vector<int32_t> dbt;          // used decode block ids, request after request
     int64_t bytes = 0;                 // bytes read (= bytes written) by one full relayout
     int32_t slices_all = 1;            // slices per item, whole-prompt launch
     int32_t slices_layer = 1;          // slices per item, per-layer launch
@@ -34,6 +52,7 @@ struct KvrHostPlan {
 kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
                                int64_t *bytes);
 
-// Kernel arguments of one launch: layers [layer0, layer0 + 1) or all layers.
+// Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,
-                        const int32_t *dev_sbt, int32_t layer0, int32_t slices);
+                        const int32_t *dev_sbt, const int32_t *dev_dbt, int32_t layer0,
+                        int32_t slices);

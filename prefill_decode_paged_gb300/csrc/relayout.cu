@@ -26,9 +26,10 @@
 
 struct kvr_plan {
     KvrHostPlan host;
-    void *dev_meta = nullptr;       // items, then prefill block ids
+    void *dev_meta = nullptr;       // items, then prefill and decode block ids
     const KvrItem *dev_items = nullptr;
     const int32_t *dev_sbt = nullptr;
+    const int32_t *dev_dbt = nullptr;
     int device = 0;
 };
 
@@ -50,6 +51,9 @@ __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
 
 __global__ void __launch_bounds__(KVR_THREADS)
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
+    // (prefill row address, decode row address) of the rows this CTA copies
+    __shared__ ulonglong2 rows[KVR_ROW_WINDOW];
+
     // Wait for the grid this launch follows in its stream (a no-op without
     // programmatic dependent launch), then let the next launch start early.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -59,25 +63,43 @@ __global__ void __launch_bounds__(KVR_THREADS)
     KvrItem it;
     uint32_t q0, q1;
     kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
+    if (q0 >= q1) return;
+    const uint32_t rc = (uint32_t)a.g.row_chunks;
+    const uint32_t r_end = a.g.div_rc.div(q1 - 1) + 1;
 
-    for (uint32_t base = q0 + threadIdx.x; base < q1; base += KVR_UNROLL * KVR_THREADS) {
-        uint4 v[KVR_UNROLL];
-        unsigned char *to[KVR_UNROLL];
-#pragma unroll
-        for (int k = 0; k < KVR_UNROLL; ++k) {
-            const uint32_t q = base + (uint32_t)k * KVR_THREADS;
-            to[k] = nullptr;
-            if (q < q1) {
-                uint32_t sp, dp;
-                int64_t soff, doff;
-                kvr_chunk(a.g, layer, it, a.sbt, q, &sp, &soff, &dp, &doff);
-                v[k] = load_stream(a.src[sp] + soff);
-                to[k] = a.dst[dp] + doff;
-            }
+    for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += KVR_ROW_WINDOW) {
+        const uint32_t w1 = min(w0 + (uint32_t)KVR_ROW_WINDOW, r_end);
+        // 1. one thread per row: the row's two addresses (block tables read here)
+        for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
+            uint32_t sp, dp;
+            int64_t soff, doff;
+            kvr_row(a.g, layer, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff);
+            rows[r - w0] = make_ulonglong2((unsigned long long)(a.src[sp] + soff),
+                                           (unsigned long long)(a.dst[dp] + doff));
         }
+        __syncthreads();
+        // 2. the 16-byte chunks of those rows: KVR_UNROLL loads in flight per thread
+        const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
+        for (uint32_t base = qa + threadIdx.x; base < qb; base += KVR_UNROLL * KVR_THREADS) {
+            uint4 v[KVR_UNROLL];
+            unsigned char *to[KVR_UNROLL];
 #pragma unroll
-        for (int k = 0; k < KVR_UNROLL; ++k)
-            if (to[k] != nullptr) store_stream(to[k], v[k]);
+            for (int k = 0; k < KVR_UNROLL; ++k) {
+                const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                to[k] = nullptr;
+                if (q < qb) {
+                    const uint32_t r = a.g.div_rc.div(q);
+                    const uint32_t off = (q - r * rc) * 16u;
+                    const ulonglong2 p = rows[r - w0];
+                    v[k] = load_stream((const unsigned char *)p.x + off);
+                    to[k] = (unsigned char *)p.y + off;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < KVR_UNROLL; ++k)
+                if (to[k] != nullptr) store_stream(to[k], v[k]);
+        }
+        __syncthreads();
     }
 }
 
@@ -86,7 +108,8 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
-    const KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, layer0, slices);
+    const KvrArgs a =
+        kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt, layer0, slices);
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
 
@@ -129,8 +152,9 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
     p->device = dev;
     const size_t items_bytes = p->host.items.size() * sizeof(KvrItem);
     const size_t sbt_bytes = p->host.sbt.size() * sizeof(int32_t);
-    if (items_bytes + sbt_bytes > 0) {
-        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes) != cudaSuccess) {
+    const size_t dbt_bytes = p->host.dbt.size() * sizeof(int32_t);
+    if (items_bytes > 0) {
+        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes + dbt_bytes) != cudaSuccess) {
             cudaGetLastError();
             delete p;
             return KVR_ERR_NOMEM;
@@ -139,6 +163,8 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
         if (cudaMemcpy(base, p->host.items.data(), items_bytes, cudaMemcpyHostToDevice) !=
                 cudaSuccess ||
             cudaMemcpy(base + items_bytes, p->host.sbt.data(), sbt_bytes,
+                       cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(base + items_bytes + sbt_bytes, p->host.dbt.data(), dbt_bytes,
                        cudaMemcpyHostToDevice) != cudaSuccess) {
             cudaFree(p->dev_meta);
             delete p;
@@ -146,6 +172,7 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
         }
         p->dev_items = (const KvrItem *)base;
         p->dev_sbt = (const int32_t *)(base + items_bytes);
+        p->dev_dbt = (const int32_t *)(base + items_bytes + sbt_bytes);
     }
     *out = p;
     return KVR_OK;
@@ -242,7 +269,9 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     if (st != KVR_OK) return st;
     const size_t items_bytes = hp.items.size() * sizeof(KvrItem);
     const size_t sbt_bytes = hp.sbt.size() * sizeof(int32_t);
-    if (items_bytes + sbt_bytes > KVR_PREALLOC_SCRATCH_BYTES) return KVR_ERR_SCRATCH_LIMIT;
+    const size_t dbt_bytes = hp.dbt.size() * sizeof(int32_t);
+    if (items_bytes + sbt_bytes + dbt_bytes > KVR_PREALLOC_SCRATCH_BYTES)
+        return KVR_ERR_SCRATCH_LIMIT;
     if (items_bytes == 0) return KVR_OK;
 
     // The whole array is overwritten up to what this call reads, so nothing
@@ -251,11 +280,15 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     if (cudaMemcpyAsync(sc.addr, hp.items.data(), items_bytes, cudaMemcpyHostToDevice, s) !=
             cudaSuccess ||
         cudaMemcpyAsync(sc.addr + items_bytes, hp.sbt.data(), sbt_bytes,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(sc.addr + items_bytes + sbt_bytes, hp.dbt.data(), dbt_bytes,
                         cudaMemcpyHostToDevice, s) != cudaSuccess)
         return KVR_ERR_CUDA;
 
     const KvrArgs a = kvr_launch_args(hp, (const KvrItem *)sc.addr,
-                                      (const int32_t *)(sc.addr + items_bytes), 0, hp.slices_all);
+                                      (const int32_t *)(sc.addr + items_bytes),
+                                      (const int32_t *)(sc.addr + items_bytes + sbt_bytes), 0,
+                                      hp.slices_all);
     const uint64_t grid = (uint64_t)hp.num_layers * a.tasks_per_layer;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);

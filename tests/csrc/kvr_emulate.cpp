@@ -28,18 +28,23 @@ Extents pool_extents(const kvr_desc *d) {
     return e;
 }
 
-// Walk one launch. copy != 0: move the bytes (host pools); otherwise only check.
-// Returns the number of out-of-bounds or misaligned chunk addresses (all skipped),
-// or a negative kvr_status. *chunks receives the number of chunks visited.
+// Walk one launch exactly as the kernel's loops do (CTA by CTA, row window by
+// row window, thread by thread). copy != 0: move the bytes (host pools);
+// otherwise only check. Returns the number of out-of-bounds or misaligned
+// chunk addresses (all skipped), or a negative kvr_status. *chunks receives
+// the number of chunks visited.
 int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chunks) {
     KvrHostPlan hp;
     kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
     if (st != KVR_OK) return st;
     const int all = layer < 0;
     const int32_t slices = all ? hp.slices_all : hp.slices_layer;
-    const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), all ? 0 : layer, slices);
+    const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
+                                      all ? 0 : layer, slices);
     const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
     const Extents ext = pool_extents(d);
+    const uint32_t rc = (uint32_t)a.g.row_chunks;
+    static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
     int64_t bad = 0, visited = 0;
     for (uint64_t task = 0; task < grid; ++task) {
         int32_t l;
@@ -50,25 +55,47 @@ int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chun
             ++bad;
             continue;
         }
-        for (uint32_t tid = 0; tid < KVR_THREADS; ++tid) {
-            for (uint32_t base = q0 + tid; base < q1; base += KVR_UNROLL * KVR_THREADS) {
-                for (int k = 0; k < KVR_UNROLL; ++k) {
-                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
-                    if (q >= q1) continue;
+        if (q0 == q1) continue;
+        const uint32_t r_end = a.g.div_rc.div(q1 - 1) + 1;
+        for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += KVR_ROW_WINDOW) {
+            const uint32_t w1 = w0 + KVR_ROW_WINDOW < r_end ? w0 + KVR_ROW_WINDOW : r_end;
+            for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
+                for (uint32_t r = w0 + tid; r < w1; r += KVR_THREADS) {
                     uint32_t sp, dp;
                     int64_t soff, doff;
-                    kvr_chunk(a.g, l, it, a.sbt, q, &sp, &soff, &dp, &doff);
-                    ++visited;
+                    kvr_row(a.g, l, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff);
                     if (sp >= (uint32_t)hp.src_tp || dp >= (uint32_t)hp.dst_tp || soff < 0 ||
-                        doff < 0 || soff + 16 > ext.src_bytes || doff + 16 > ext.dst_bytes ||
-                        ((uintptr_t)hp.src[sp] + soff) % 16 != 0 ||
-                        ((uintptr_t)hp.dst[dp] + doff) % 16 != 0) {
+                        doff < 0 || soff + a.g.row_bytes > ext.src_bytes ||
+                        doff + a.g.row_bytes > ext.dst_bytes) {
                         ++bad;
+                        rows_src[r - w0] = rows_dst[r - w0] = UINT64_MAX;
                         continue;
                     }
-                    if (copy)
-                        memcpy((unsigned char *)hp.dst[dp] + doff,
-                               (const unsigned char *)hp.src[sp] + soff, 16);
+                    rows_src[r - w0] = (uint64_t)((uintptr_t)hp.src[sp] + soff);
+                    rows_dst[r - w0] = (uint64_t)((uintptr_t)hp.dst[dp] + doff);
+                }
+            const uint32_t qa = q0 > w0 * rc ? q0 : w0 * rc;
+            const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
+            for (uint32_t tid = 0; tid < KVR_THREADS; ++tid) {
+                for (uint32_t base = qa + tid; base < qb; base += KVR_UNROLL * KVR_THREADS) {
+                    for (int k = 0; k < KVR_UNROLL; ++k) {
+                        const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                        if (q >= qb) continue;
+                        const uint32_t r = a.g.div_rc.div(q);
+                        const uint32_t off = (q - r * rc) * 16u;
+                        ++visited;
+                        if (r < w0 || r >= w1 || rows_src[r - w0] == UINT64_MAX) {
+                            ++bad;
+                            continue;
+                        }
+                        const uint64_t from = rows_src[r - w0] + off;
+                        const uint64_t to = rows_dst[r - w0] + off;
+                        if (from % 16 != 0 || to % 16 != 0 || off + 16 > (uint32_t)a.g.row_bytes) {
+                            ++bad;
+                            continue;
+                        }
+                        if (copy) memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from, 16);
+                    }
                 }
             }
         }
@@ -91,7 +118,7 @@ int64_t emu_check(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunk
     return walk(d, sm_count, layer, 0, chunks);
 }
 
-// Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer].
+// Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
     kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
@@ -102,6 +129,7 @@ int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     out[2] = hp.slices_layer;
     out[3] = n * hp.slices_all * hp.num_layers;
     out[4] = n * hp.slices_layer;
+    out[5] = hp.tile;
     return 0;
 }
 

@@ -281,7 +281,7 @@ def test_fast_division_matches_hardware_division(emu):
 
 def test_launch_shapes(emu):
     """Per-layer launches are sliced to fill the GPU; whole-prompt launches are not."""
-    info = (ctypes.c_int64 * 5)()
+    info = (ctypes.c_int64 * 6)()
     for name, n_items in (("llama70b", 128), ("qwen32k", 2048)):
         w = wl.get(name)
         s, d = fake_pools(w)
@@ -290,3 +290,11 @@ def test_launch_shapes(emu):
         assert info[0] == n_items
         assert info[4] >= SMS                      # a per-layer launch covers every SM
         assert info[3] == n_items * w.num_layers * info[1]
+        assert info[5] == w.dst_block                 # 128 KB+ decode blocks: one per tile
+    # small decode blocks are grouped: MLA's 16-token (18 KB) blocks, 3 per tile (54 KB)
+    w = wl.get("dsv3mla")
+    s, d = fake_pools(w)
+    desc = kr._Desc(s, d, **w.geometry())
+    assert emu.emu_plan_info(ctypes.byref(desc.desc), SMS, info) == 0
+    assert info[5] == 48
+    assert info[0] == sum(-(-int(n) // 48) for n in w.seq_lens)

@@ -55,9 +55,10 @@ def test_calls_in_a_row_match_the_allocating_entry_point():
 
 def test_work_list_beyond_the_scratch_is_rejected_before_any_work():
     import torch
-    n = PREALLOC_SCRATCH_BYTES // 16 + 1000          # one 16-byte work item per token
+    # one-token blocks on both sides: 4 + 4 bytes of block ids per token
+    n = PREALLOC_SCRATCH_BYTES // 8 + 1000
     w = wl.custom("prealloc_too_big", 34, num_layers=1, num_components=1, kv_heads=1,
-                  head_dim=8, elem_bytes=2, src_tp=1, dst_tp=1, src_block=16, dst_block=1,
+                  head_dim=8, elem_bytes=2, src_tp=1, dst_tp=1, src_block=1, dst_block=1,
                   seq_lens=[n], values="randn")
     src = w.src_pools_torch("cuda")
     dst = w.dst_pools_torch("cuda")
