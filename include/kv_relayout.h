@@ -18,7 +18,14 @@
  * device, collective or network. Elements are moved as raw bits (no dtype
  * conversion; NaN payloads and -0 are preserved).
  *
- * Pool layout. Each TP shard of each side is ONE contiguous device buffer of
+ * Pool memory. A pool may live in this GPU's HBM, in managed memory, or in
+ * pinned host memory mapped into the device address space (cudaHostAlloc,
+ * cudaHostRegister): on Grace-based GB300 systems the kernel then reads or
+ * writes host memory directly over NVLink-C2C, with no staging copy. Launch
+ * calls that build a plan check that the first and last byte of every pool is
+ * such memory (KVR_ERR_POOL_ADDRESS otherwise).
+ *
+ * Pool layout. Each TP shard of each side is ONE contiguous buffer of
  *   [num_layers][num_components][num_blocks][block_size][kv_heads / tp][head_dim]
  * elements of elem_bytes bytes. Components: 2 = K then V planes, 1 = a single
  * latent plane (MLA). Shard s holds the contiguous head range
@@ -68,7 +75,8 @@ typedef enum kvr_status {
     KVR_ERR_CUDA = -8,          /* a CUDA runtime call failed (no device, launch error, ...) */
     KVR_ERR_NOMEM = -9,         /* host or device allocation of the plan failed */
     KVR_ERR_POOL_OVERLAP = -10, /* a decode pool overlaps another decode pool or a prefill pool */
-    KVR_ERR_SCRATCH_LIMIT = -11 /* kv_relayout_all_prealloc: work list larger than its scratch */
+    KVR_ERR_SCRATCH_LIMIT = -11, /* kv_relayout_all_prealloc: work list larger than its scratch */
+    KVR_ERR_POOL_ADDRESS = -12  /* a pool's first or last byte is not memory this GPU can access */
 } kvr_status;
 
 typedef struct kvr_desc {
@@ -105,9 +113,10 @@ kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
                                   int64_t *bytes_written);
 
 /*
- * Validate *desc (as above), build the work list on the host and upload it
- * with the prefill block ids to the current device (one allocation, one
- * synchronous copy). *out is set to the new plan, or to NULL on failure.
+ * Validate *desc (as above), check that every pool is memory the current
+ * device can access, build the work list on the host and upload it with the
+ * used block ids to the current device (one allocation, synchronous copies).
+ * *out is set to the new plan, or to NULL on failure.
  */
 kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
 
@@ -151,7 +160,8 @@ const char *kv_relayout_strerror(kvr_status status);
  * a request) and the used prefill and decode block ids (4 bytes each) into a
  * fixed device array of KVR_PREALLOC_SCRATCH_BYTES (1 MiB) that the library
  * reserves on every GPU that loads it, until the process exits, and launches
- * the same kernel as kv_relayout_all() on `stream` (asynchronous).
+ * the same kernel as kv_relayout_all() on `stream` (asynchronous). The pool
+ * memory checks of kv_relayout_plan() apply.
  *
  *  - A work list larger than the array is rejected with
  *    KVR_ERR_SCRATCH_LIMIT before anything is copied or launched; use

@@ -54,8 +54,9 @@ kvr_status check_table(int32_t R, const int32_t *lens, const int64_t *off, const
     return KVR_OK;
 }
 
-int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count) {
-    const int64_t target = (int64_t)std::max(sm_count, 1) * KVR_TARGET_CTAS_PER_SM;
+int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count,
+                      int ctas_per_sm) {
+    const int64_t target = (int64_t)std::max(sm_count, 1) * ctas_per_sm;
     if (tasks_unsliced <= 0 || tasks_unsliced >= target) return 1;
     const int64_t want = ceil_div(target, tasks_unsliced);
     const int64_t most = std::max<int64_t>(1, avg_chunks / KVR_MIN_SLICE_CHUNKS);
@@ -211,8 +212,9 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     }
 
     const int64_t avg_chunks = n_items ? (bytes / L / 16) / n_items : 0;
-    hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count);
-    hp->slices_all = choose_slices((int64_t)L * n_items, avg_chunks, sm_count);
+    hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count, KVR_LAYER_CTAS_PER_SM);
+    hp->slices_all =
+        choose_slices((int64_t)L * n_items, avg_chunks, sm_count, KVR_TARGET_CTAS_PER_SM);
     while ((int64_t)L * n_items * hp->slices_all > INT32_MAX && hp->slices_all > 1)
         --hp->slices_all;
     return KVR_OK;
@@ -265,6 +267,7 @@ extern "C" const char *kv_relayout_strerror(kvr_status s) {
         case KVR_ERR_NOMEM: return "out of memory";
         case KVR_ERR_POOL_OVERLAP: return "decode pool overlaps another pool";
         case KVR_ERR_SCRATCH_LIMIT: return "work list larger than the preallocated scratch";
+        case KVR_ERR_POOL_ADDRESS: return "pool is not memory this GPU can access";
     }
     return "unknown status";
 }

@@ -15,13 +15,20 @@
 #ifndef KVR_UNROLL
 #define KVR_UNROLL 8             // 16-byte loads in flight per thread before its stores
 #endif
+#ifndef KVR_UNROLL_LAYER
+#define KVR_UNROLL_LAYER 4       // the same for per-layer launches (short, latency-bound)
+#endif
 #ifndef KVR_ROW_WINDOW
 #define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once
 #endif
-// A launch aims at this many CTAs per SM; items are sliced until it does,
-// but no slice gets fewer than KVR_MIN_SLICE_CHUNKS 16-byte chunks.
+// A launch aims at this many CTAs per SM (whole-prompt / per-layer); items
+// are sliced until it does, but no slice gets fewer than
+// KVR_MIN_SLICE_CHUNKS 16-byte chunks.
 #ifndef KVR_TARGET_CTAS_PER_SM
 #define KVR_TARGET_CTAS_PER_SM 8
+#endif
+#ifndef KVR_LAYER_CTAS_PER_SM
+#define KVR_LAYER_CTAS_PER_SM 8
 #endif
 #ifndef KVR_MIN_SLICE_CHUNKS
 #define KVR_MIN_SLICE_CHUNKS 512

@@ -49,6 +49,8 @@ __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
                  : "memory");
 }
 
+// U: 16-byte loads each thread keeps in flight before its stores.
+template <int U>
 __global__ void __launch_bounds__(KVR_THREADS)
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
     // (prefill row address, decode row address) of the rows this CTA copies
@@ -78,13 +80,13 @@ __global__ void __launch_bounds__(KVR_THREADS)
                                            (unsigned long long)(a.dst[dp] + doff));
         }
         __syncthreads();
-        // 2. the 16-byte chunks of those rows: KVR_UNROLL loads in flight per thread
+        // 2. the 16-byte chunks of those rows: U loads in flight per thread
         const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
-        for (uint32_t base = qa + threadIdx.x; base < qb; base += KVR_UNROLL * KVR_THREADS) {
-            uint4 v[KVR_UNROLL];
-            unsigned char *to[KVR_UNROLL];
+        for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
+            uint4 v[U];
+            unsigned char *to[U];
 #pragma unroll
-            for (int k = 0; k < KVR_UNROLL; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const uint32_t q = base + (uint32_t)k * KVR_THREADS;
                 to[k] = nullptr;
                 if (q < qb) {
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
                 }
             }
 #pragma unroll
-            for (int k = 0; k < KVR_UNROLL; ++k)
+            for (int k = 0; k < U; ++k)
                 if (to[k] != nullptr) store_stream(to[k], v[k]);
         }
         __syncthreads();
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
 }
 
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
-                  void *stream) {
+                  bool per_layer, void *stream) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
@@ -123,8 +125,52 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel, a) == cudaSuccess ? KVR_OK
-                                                                            : KVR_ERR_CUDA;
+    const cudaError_t e = per_layer
+                              ? cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL_LAYER>, a)
+                              : cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL>, a);
+    return e == cudaSuccess ? KVR_OK : KVR_ERR_CUDA;
+}
+
+// The first and last byte of a pool must be memory device `dev` can access:
+// its own HBM, managed memory, or pinned host memory mapped at the same
+// address (so a pageable host pointer, a freed or foreign pointer, or another
+// GPU's memory is refused instead of faulting inside the kernel).
+kvr_status check_pool(const void *pool, int64_t bytes, int dev) {
+    const unsigned char *ends[2] = {(const unsigned char *)pool,
+                                    (const unsigned char *)pool + (bytes > 0 ? bytes - 1 : 0)};
+    for (const unsigned char *q : ends) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+            cudaGetLastError();
+            return KVR_ERR_POOL_ADDRESS;
+        }
+        switch (at.type) {
+            case cudaMemoryTypeDevice:
+                if (at.device != dev) return KVR_ERR_POOL_ADDRESS;
+                break;
+            case cudaMemoryTypeManaged:
+                break;
+            case cudaMemoryTypeHost:
+                if (at.devicePointer != (const void *)q) return KVR_ERR_POOL_ADDRESS;
+                break;
+            default:
+                return KVR_ERR_POOL_ADDRESS;
+        }
+    }
+    return KVR_OK;
+}
+
+kvr_status check_pools(const KvrHostPlan &hp, int dev) {
+    const int64_t layers_comps = (int64_t)hp.num_layers * hp.g.C;
+    for (int32_t s = 0; s < hp.src_tp; ++s) {
+        const kvr_status st = check_pool(hp.src[s], hp.g.src_plane_bytes * layers_comps, dev);
+        if (st != KVR_OK) return st;
+    }
+    for (int32_t s = 0; s < hp.dst_tp; ++s) {
+        const kvr_status st = check_pool(hp.dst[s], hp.g.dst_plane_bytes * layers_comps, dev);
+        if (st != KVR_OK) return st;
+    }
+    return KVR_OK;
 }
 
 }  // namespace
@@ -145,6 +191,7 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
+    if (st == KVR_OK) st = check_pools(p->host, dev);
     if (st != KVR_OK) {
         delete p;
         return st;
@@ -181,12 +228,12 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
 extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
     if (layer < 0 || layer >= plan->host.num_layers) return KVR_ERR_LAYER_RANGE;
-    return launch(plan, layer, 1, plan->host.slices_layer, stream);
+    return launch(plan, layer, 1, plan->host.slices_layer, true, stream);
 }
 
 extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
-    return launch(plan, 0, plan->host.num_layers, plan->host.slices_all, stream);
+    return launch(plan, 0, plan->host.num_layers, plan->host.slices_all, false, stream);
 }
 
 extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
@@ -266,6 +313,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
+    if (st == KVR_OK) st = check_pools(hp, dev);
     if (st != KVR_OK) return st;
     const size_t items_bytes = hp.items.size() * sizeof(KvrItem);
     const size_t sbt_bytes = hp.sbt.size() * sizeof(int32_t);
@@ -300,6 +348,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel, a) == cudaSuccess ? KVR_OK
-                                                                            : KVR_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL>, a) == cudaSuccess
+               ? KVR_OK
+               : KVR_ERR_CUDA;
 }

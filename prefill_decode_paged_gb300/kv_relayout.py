@@ -21,6 +21,7 @@ STATUS = {
     -3: "KVR_ERR_ALIGNMENT", -4: "KVR_ERR_BLOCK_RANGE", -5: "KVR_ERR_TABLE_SHORT",
     -6: "KVR_ERR_DST_ALIAS", -7: "KVR_ERR_LAYER_RANGE", -8: "KVR_ERR_CUDA",
     -9: "KVR_ERR_NOMEM", -10: "KVR_ERR_POOL_OVERLAP", -11: "KVR_ERR_SCRATCH_LIMIT",
+    -12: "KVR_ERR_POOL_ADDRESS",
 }
 PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",

@@ -44,6 +44,7 @@ int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chun
     const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
     const Extents ext = pool_extents(d);
     const uint32_t rc = (uint32_t)a.g.row_chunks;
+    const uint32_t U = all ? KVR_UNROLL : KVR_UNROLL_LAYER;
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
     int64_t bad = 0, visited = 0;
     for (uint64_t task = 0; task < grid; ++task) {
@@ -77,9 +78,9 @@ int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chun
             const uint32_t qa = q0 > w0 * rc ? q0 : w0 * rc;
             const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
             for (uint32_t tid = 0; tid < KVR_THREADS; ++tid) {
-                for (uint32_t base = qa + tid; base < qb; base += KVR_UNROLL * KVR_THREADS) {
-                    for (int k = 0; k < KVR_UNROLL; ++k) {
-                        const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                for (uint32_t base = qa + tid; base < qb; base += U * KVR_THREADS) {
+                    for (uint32_t k = 0; k < U; ++k) {
+                        const uint32_t q = base + k * KVR_THREADS;
                         if (q >= qb) continue;
                         const uint32_t r = a.g.div_rc.div(q);
                         const uint32_t off = (q - r * rc) * 16u;

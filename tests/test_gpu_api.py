@@ -132,3 +132,56 @@ def test_empty_batch_and_repeated_launches():
         torch.cuda.synchronize()
     for a, b in zip(_ref(w, src_np), to_host(dst, w)):
         np.testing.assert_array_equal(b, a)
+
+
+def _pinned_like(tensors):
+    import torch
+    out = []
+    for t in tensors:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        out.append(h)
+    return out
+
+
+def test_pools_in_pinned_host_memory():
+    """Prefill and/or decode pools in pinned host memory: the kernel reaches them
+    directly (no staging copy) and the bytes are the oracle's."""
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    ref = _ref(w, src_np)
+    dev_src = to_device(src_np, 2)
+    host_src = _pinned_like(dev_src)
+    for src in (host_src, dev_src):
+        for host_dst in (True, False):
+            dst = to_device(w.dst_pools_numpy(), 2)
+            if host_dst:
+                dst = _pinned_like(dst)
+            if src is dev_src and not host_dst:
+                continue
+            with RelayoutPlan(src, dst, **w.geometry()) as plan:
+                plan.run_all()
+                torch.cuda.synchronize()
+            for a, t in zip(ref, dst):
+                np.testing.assert_array_equal(t.cpu().numpy().view(np.uint16), a)
+
+
+def test_pools_the_gpu_cannot_reach_are_refused():
+    import torch
+    from prefill_decode_paged_gb300 import relayout_all_prealloc
+    w = _small()
+    src = to_device(w.src_pools_numpy(), 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    pageable = [np.zeros(w.src_shape(), dtype=np.int16) for _ in range(w.src_tp)]
+    bad_src = [a.ctypes.data // 256 * 256 + 256 for a in pageable]   # 16-B aligned, pageable
+    with pytest.raises(KVRelayoutError) as e:
+        RelayoutPlan(bad_src, dst, **w.geometry())
+    assert e.value.name == "KVR_ERR_POOL_ADDRESS"
+    with pytest.raises(KVRelayoutError) as e:
+        relayout_all_prealloc(src, [a.ctypes.data // 256 * 256 + 256 for a in
+                                    [np.zeros(w.dst_shape(), np.int16) for _ in range(2)]],
+                              **w.geometry())
+    assert e.value.name == "KVR_ERR_POOL_ADDRESS"
+    torch.cuda.synchronize()
+    assert all(bool((t == -1).all()) for t in dst)
