@@ -41,7 +41,7 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, src],
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, src, "-lm"],
                    check=True)
     os.replace(tmp, out)
     return out
@@ -56,6 +56,13 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvo_relayout.restype = ctypes.c_int
     lib.kvo_relayout.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                  i64, i64, p, p, i32, p, p, p, p, p]
+    lib.kvo_relayout_convert.restype = ctypes.c_int
+    lib.kvo_relayout_convert.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, p, i32,
+                                         i32, i32, i32, i64, i64, p, p, i32, p, p, p, p, p]
+    for name, t in (("kvo_e4m3_encode_array", None), ("kvo_e4m3_decode_array", None),
+                    ("kvo_bf16_encode_array", None)):
+        getattr(lib, name).restype = None
+        getattr(lib, name).argtypes = [p, p, i64]
     return lib
 
 
@@ -85,6 +92,37 @@ def transfer_bytes(num_layers, num_components, kv_heads, head_dim, elem_bytes, s
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     return int(lib.kvo_transfer_bytes(num_layers, num_components, kv_heads, head_dim,
                                       elem_bytes, len(lens), lens.ctypes.data))
+
+
+# dtype codes of the converting relayout
+BF16 = 1
+E4M3 = 2
+
+
+def e4m3_encode(x, lib=None):
+    """fp32 values -> E4M3 codes (nearest, ties to even, saturating at +-448)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib.kvo_e4m3_encode_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def e4m3_decode(codes, lib=None):
+    lib = lib or load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float32)
+    lib.kvo_e4m3_decode_array(c.ctypes.data, out.ctypes.data, c.size)
+    return out
+
+
+def bf16_encode(x, lib=None):
+    """fp32 values -> bf16 bit patterns (nearest, ties to even)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib.kvo_bf16_encode_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
 
 
 def _ptr_array(arrays, writable: bool):
@@ -129,3 +167,31 @@ def relayout(src_pools, dst_pools, *, num_layers, num_components, kv_heads, head
                           db.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle rejected the geometry (status {rc})")
+
+
+def relayout_convert(src_pools, dst_pools, *, num_layers, num_components, kv_heads, head_dim,
+                     src_dtype, dst_dtype, per_head, scales, src_tp, dst_tp, src_block,
+                     dst_block, src_num_blocks, dst_num_blocks, seq_lens, src_off, src_bt,
+                     dst_off, dst_bt, layer_begin=0, layer_end=None, lib=None, **_ignored):
+    """The converting relayout (BF16 <-> E4M3) of the C oracle, in place on numpy pools."""
+    lib = lib or load()
+    if layer_end is None:
+        layer_end = num_layers
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    so = np.ascontiguousarray(src_off, dtype=np.int64)
+    sb = np.ascontiguousarray(src_bt, dtype=np.int32)
+    do = np.ascontiguousarray(dst_off, dtype=np.int64)
+    db = np.ascontiguousarray(dst_bt, dtype=np.int32)
+    sb = sb if sb.size else np.zeros(1, np.int32)
+    db = db if db.size else np.zeros(1, np.int32)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    sp = _ptr_array(src_pools, False)
+    dp = _ptr_array(dst_pools, True)
+    rc = lib.kvo_relayout_convert(layer_begin, layer_end, num_layers, num_components, kv_heads,
+                                  head_dim, src_dtype, dst_dtype, int(per_head), sc.ctypes.data,
+                                  src_tp, dst_tp, src_block, dst_block, src_num_blocks,
+                                  dst_num_blocks, sp, dp, len(lens), lens.ctypes.data,
+                                  so.ctypes.data, sb.ctypes.data, do.ctypes.data,
+                                  db.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the conversion (status {rc})")

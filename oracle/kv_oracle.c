@@ -127,3 +127,207 @@ int kvo_relayout(int32_t layer_begin, int32_t layer_end,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * dtype-converting relayout (page "PD 分离与 KV 传输", section "布局转换",
+ * item on data types: one side keeps BF16 KV, the other FP8 KV, and the
+ * conversion belongs around the transfer). The page fixes neither the FP8
+ * format nor the scale; the readings taken here:
+ *   - FP8 is E4M3 as in the OCP 8-bit floating point specification: 1 sign,
+ *     4 exponent bits (bias 7), 3 mantissa bits, subnormals, no infinities,
+ *     S.1111.111 is NaN, largest finite value 448;
+ *   - quantize:   q = E4M3(x * fl32(1 / s)), round to nearest, ties to even,
+ *     magnitudes above 448 (and infinities) saturate to +-448, NaN -> S.1111.111;
+ *   - dequantize: y = BF16(float(q) * s), round to nearest, ties to even,
+ *     NaN -> sign | 0x7FC0;
+ *   - s is one positive scale per (layer, component), or per (layer,
+ *     component, KV head).
+ * All products are single fp32 multiplications (as the C float type gives).
+ * ------------------------------------------------------------------------- */
+#include <math.h>
+#include <string.h>
+
+#define KVO_BF16 1
+#define KVO_E4M3 2
+
+/* Exact value of the non-negative E4M3 code c (0..126), from its fields. */
+static double e4m3_magnitude(int c)
+{
+    const int e = c >> 3, m = c & 7;
+    if (e == 0)
+        return ldexp((double)m, -9);         /* subnormal: m/8 * 2^(1-7) */
+    return ldexp((double)(8 + m), e - 10);   /* (1 + m/8) * 2^(e-7) */
+}
+
+float kvo_e4m3_decode(uint8_t code)
+{
+    if ((code & 0x7F) == 0x7F)
+        return NAN;
+    const double v = e4m3_magnitude(code & 0x7F);
+    return (float)((code & 0x80) ? -v : v);
+}
+
+uint8_t kvo_e4m3_encode(float v)
+{
+    uint32_t bits;
+    memcpy(&bits, &v, 4);
+    const uint8_t sign = (bits >> 31) ? 0x80 : 0x00;
+    if (v != v)
+        return sign | 0x7F;
+    const double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* largest code whose value does not exceed a (values grow with the code) */
+    int lo = 0, hi = 126;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (e4m3_magnitude(mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const double below = a - e4m3_magnitude(lo);
+    const double above = e4m3_magnitude(lo + 1) - a;
+    int code;
+    if (below < above)
+        code = lo;
+    else if (above < below)
+        code = lo + 1;
+    else
+        code = (lo & 1) ? lo + 1 : lo;      /* tie: the even code */
+    return (uint8_t)(sign | code);
+}
+
+/* fp32 -> bf16 bits, nearest with ties to even, by comparing the two
+ * neighbouring bf16 values (the upper neighbour of the largest finite bf16
+ * is taken as 2^128, which rounds to infinity). */
+uint16_t kvo_bf16_encode(float v)
+{
+    uint32_t bits;
+    memcpy(&bits, &v, 4);
+    const uint16_t sign = (uint16_t)((bits >> 16) & 0x8000);
+    if (v != v)
+        return sign | 0x7FC0;
+    const uint32_t mag = bits & 0x7FFFFFFFu;
+    const uint32_t lo = mag & 0xFFFF0000u;
+    if (lo == mag)
+        return (uint16_t)(sign | (lo >> 16));
+    float flo;
+    memcpy(&flo, &lo, 4);
+    const double vlo = (double)flo;
+    double vhi;
+    if (lo == 0x7F7F0000u) {
+        vhi = ldexp(1.0, 128);
+    } else {
+        const uint32_t hib = lo + 0x10000u;
+        float fhi;
+        memcpy(&fhi, &hib, 4);
+        vhi = (double)fhi;
+    }
+    const double a = fabs((double)v);
+    uint32_t pick;
+    if (a - vlo < vhi - a)
+        pick = lo;
+    else if (vhi - a < a - vlo)
+        pick = lo + 0x10000u;
+    else
+        pick = ((lo >> 16) & 1) ? lo + 0x10000u : lo;
+    return (uint16_t)(sign | (pick >> 16));
+}
+
+/* The relayout of kvo_relayout() with a dtype change on the way: src_dtype
+ * and dst_dtype are KVO_BF16 / KVO_E4M3 (one of each); elements are 2 bytes
+ * (little-endian) for BF16 and 1 byte for E4M3; scales[] has L*C entries, or
+ * L*C*H when per_head is 1. Returns 0, or -1 for an unsupported request. */
+int kvo_relayout_convert(int32_t layer_begin, int32_t layer_end,
+                         int32_t num_layers, int32_t num_components,
+                         int32_t kv_heads, int32_t head_dim,
+                         int32_t src_dtype, int32_t dst_dtype,
+                         int32_t per_head, const float *scales,
+                         int32_t src_tp, int32_t dst_tp,
+                         int32_t src_block, int32_t dst_block,
+                         int64_t src_num_blocks, int64_t dst_num_blocks,
+                         const uint8_t *const *src_pools, uint8_t *const *dst_pools,
+                         int32_t num_requests, const int32_t *seq_lens,
+                         const int64_t *src_off, const int32_t *src_bt,
+                         const int64_t *dst_off, const int32_t *dst_bt)
+{
+    if (kv_heads % src_tp != 0 || kv_heads % dst_tp != 0)
+        return -1;
+    if (!((src_dtype == KVO_BF16 && dst_dtype == KVO_E4M3) ||
+          (src_dtype == KVO_E4M3 && dst_dtype == KVO_BF16)))
+        return -1;
+    (void)num_layers;
+    const int64_t src_es = src_dtype == KVO_BF16 ? 2 : 1;
+    const int64_t dst_es = dst_dtype == KVO_BF16 ? 2 : 1;
+    const int64_t src_heads = kv_heads / src_tp;
+    const int64_t dst_heads = kv_heads / dst_tp;
+    const int64_t C = num_components;
+    const int64_t D = head_dim;
+
+    for (int32_t r = 0; r < num_requests; ++r) {
+        const int64_t n = seq_lens[r];
+        for (int64_t l = layer_begin; l < layer_end; ++l) {
+            for (int64_t c = 0; c < C; ++c) {
+                for (int64_t t = 0; t < n; ++t) {
+                    const int64_t sblk = src_bt[src_off[r] + t / src_block];
+                    const int64_t soff = t % src_block;
+                    const int64_t dblk = dst_bt[dst_off[r] + t / dst_block];
+                    const int64_t doff = t % dst_block;
+                    for (int64_t h = 0; h < kv_heads; ++h) {
+                        const int64_t sp = h / src_heads;
+                        const int64_t sh = h % src_heads;
+                        const int64_t dp = h / dst_heads;
+                        const int64_t dh = h % dst_heads;
+                        const float s = per_head ? scales[(l * C + c) * kv_heads + h]
+                                                 : scales[l * C + c];
+                        for (int64_t e = 0; e < D; ++e) {
+                            const int64_t s_elem =
+                                ((((l * C + c) * src_num_blocks + sblk) * src_block + soff)
+                                     * src_heads + sh) * D + e;
+                            const int64_t d_elem =
+                                ((((l * C + c) * dst_num_blocks + dblk) * dst_block + doff)
+                                     * dst_heads + dh) * D + e;
+                            const uint8_t *from = src_pools[sp] + s_elem * src_es;
+                            uint8_t *to = dst_pools[dp] + d_elem * dst_es;
+                            if (src_dtype == KVO_BF16) {
+                                const uint32_t xb = ((uint32_t)from[0] | ((uint32_t)from[1] << 8)) << 16;
+                                float x;
+                                memcpy(&x, &xb, 4);
+                                const float inv = 1.0f / s;
+                                const float y = x * inv;
+                                to[0] = kvo_e4m3_encode(y);
+                            } else {
+                                const float x = kvo_e4m3_decode(from[0]);
+                                const float y = x * s;
+                                const uint16_t b = kvo_bf16_encode(y);
+                                to[0] = (uint8_t)(b & 0xFF);
+                                to[1] = (uint8_t)(b >> 8);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Element-wise helpers over arrays (used by the tests' pins). */
+void kvo_e4m3_encode_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e4m3_encode(x[i]);
+}
+
+void kvo_e4m3_decode_array(const uint8_t *x, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_e4m3_decode(x[i]);
+}
+
+void kvo_bf16_encode_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvo_bf16_encode(x[i]);
+}

@@ -1,0 +1,38 @@
+"""bench.py on the GPU: the JSON line keeps its contract (small workload, few steps)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_line_keeps_the_contract():
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--config", "tiny",
+                          "--steps", "20", "--warmup", "3", "--e2e-steps", "3",
+                          "--cpu-budget-s", "0.2"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-3000:]
+    lines = [l for l in res.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, res.stdout
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "gpu_launches", "roofline", "e2e", "cpu_baseline", "clocks"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3
+    assert d["gpu_launches"] == 20
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["bytes_per_step"] == 204800
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    c = d["cpu_baseline"]
+    assert c["kind"] == "oracle" and c["cores"] == 1 and c["value"] > 0
+    assert d["per_layer"]["eager"]["launches_per_step"] == 2

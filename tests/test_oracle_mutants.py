@@ -41,6 +41,35 @@ MUTANTS = {
                            "for (int32_t r = 0; r < 1 && r < num_requests; ++r) {"),
 }
 
+CONVERT_MUTANTS = {
+    "e4m3_ties_to_lower": ("code = (lo & 1) ? lo + 1 : lo;", "code = lo;"),
+    "e4m3_no_saturation": ("if (a >= 448.0)", "if (a >= 1e30)"),
+    "e4m3_subnormal_exponent": ("return ldexp((double)m, -9);", "return ldexp((double)m, -10);"),
+    "scale_not_inverted": ("const float y = x * inv;", "const float y = x * s;"),
+    "per_head_scale_ignores_head": ("scales[(l * C + c) * kv_heads + h]",
+                                    "scales[(l * C + c) * kv_heads]"),
+    "bf16_ties_always_up": ("pick = ((lo >> 16) & 1) ? lo + 0x10000u : lo;",
+                            "pick = lo + 0x10000u;"),
+    "bf16_high_byte_dropped": ("to[1] = (uint8_t)(b >> 8);", "to[1] = 0;"),
+}
+
+CONVERT_BATTERY = textwrap.dedent("""
+    import sys
+    sys.path[:0] = [{root!r}, {tests!r}]
+    import oracle, test_oracle_convert_pins as P
+    lib = oracle.load({lib!r})
+    P.test_e4m3_decode_fixed_points(lib)
+    P.test_e4m3_decode_matches_torch(lib)
+    P.test_e4m3_round_trip(lib)
+    P.test_e4m3_encode_matches_torch_in_range(lib)
+    P.test_e4m3_encode_saturates_and_keeps_nan(lib)
+    P.test_bf16_encode_matches_torch(lib)
+    for per_head in (0, 1):
+        P.test_quantize_placement_reduces_to_a_copy_of_codes(lib, per_head)
+        P.test_dequantize_placement_reduces_to_a_copy_of_values(lib, per_head)
+    P.test_quantize_then_dequantize_stays_within_e4m3_precision(lib)
+""")
+
 BATTERY = textwrap.dedent("""
     import sys
     sys.path[:0] = [{root!r}, {tests!r}]
@@ -57,8 +86,9 @@ BATTERY = textwrap.dedent("""
 """)
 
 
-def _battery(lib_path):
-    code = BATTERY.format(root=ROOT, tests=os.path.join(ROOT, "tests"), lib=lib_path)
+def _battery(lib_path, battery=None):
+    code = (battery or BATTERY).format(root=ROOT, tests=os.path.join(ROOT, "tests"),
+                                       lib=lib_path)
     return subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                           timeout=300)
 
@@ -74,6 +104,8 @@ def test_unmutated_oracle_passes_the_battery(tmp_path):
         lib = _build(tmp_path, "control", f.read())
     res = _battery(lib)
     assert res.returncode == 0, res.stderr[-3000:]
+    res = _battery(lib, CONVERT_BATTERY)
+    assert res.returncode == 0, res.stderr[-3000:]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -81,7 +113,38 @@ def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     with open(SRC) as f:
         text = f.read()
-    assert text.count(old) == 1, f"mutation site for {name} not unique in the oracle"
+    assert text.count(old) >= 1, f"mutation site for {name} not in the oracle"
     lib = _build(tmp_path, name, text.replace(old, new))
     res = _battery(lib)
+    assert res.returncode != 0, f"mutant {name} survived the pins"
+
+
+INDEX_MUTANTS = ["src_shard_by_dst_heads", "dst_local_head_by_src_heads",
+                 "src_table_index_by_dst_block", "dst_offset_by_src_block",
+                 "src_row_stride_by_dst_block", "dropped_local_head",
+                 "layer_component_transposed", "last_token_dropped"]
+
+
+@pytest.mark.parametrize("name", INDEX_MUTANTS)
+def test_conversion_index_mutant_is_caught(tmp_path, name):
+    """The same indexing mistakes planted only in the converting loop nest (the
+    second occurrence of each site) must fail the conversion pins."""
+    old, new = MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) == 2, f"{name}: expected one site per loop nest"
+    first = text.index(old) + len(old)
+    lib = _build(tmp_path, name, text[:first] + text[first:].replace(old, new, 1))
+    res = _battery(lib, CONVERT_BATTERY)
+    assert res.returncode != 0, f"mutant {name} survived the conversion pins"
+
+
+@pytest.mark.parametrize("name", sorted(CONVERT_MUTANTS))
+def test_conversion_mutant_is_caught(tmp_path, name):
+    old, new = CONVERT_MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique in the oracle"
+    lib = _build(tmp_path, name, text.replace(old, new))
+    res = _battery(lib, CONVERT_BATTERY)
     assert res.returncode != 0, f"mutant {name} survived the pins"
