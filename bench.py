@@ -79,6 +79,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="CPU seconds for the oracle baseline sample")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--convert", default="none", choices=["none", "bf16_to_fp8", "fp8_to_bf16"],
+                   help="change the KV dtype on the way (FP8 = E4M3, per-head scales)")
     p.add_argument("--modes", default="all,layer,graph",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA graph)")
@@ -240,25 +242,61 @@ def _full_layers(config):
 
 # -- the CPU oracle -------------------------------------------------------------------
 
-def oracle_sample(w, src_layers, budget_s, reps_cap=1000):
+def oracle_sample(w, src_layers, budget_s, reps_cap=1000, conv=None):
     """Time the oracle, as it stands, on the given layers of the workload until the
-    budget is spent (at least once). Returns (bytes moved, seconds, layers per pass)."""
+    budget is spent (at least once). Returns (bytes moved, seconds, layers per pass).
+    With ``conv`` (the dict given to the plan) the converting oracle runs."""
     import dataclasses
+
+    import numpy as np
 
     import oracle
     n = len(src_layers[0])
     wk = dataclasses.replace(w, num_layers=n)
-    dst = wk.dst_pools_numpy()
-    per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim * \
-        w.elem_bytes
+    elems = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim
+    if conv is None:
+        dst = wk.dst_pools_numpy()
+        per_layer = 2 * elems * w.elem_bytes
+    else:
+        dst_es = 2 if conv["dst_dtype"] == BF16 else 1
+        dst = [np.zeros(wk.dst_shape(), {1: np.uint8, 2: np.uint16}[dst_es])
+               for _ in range(wk.dst_tp)]
+        per_layer = elems * (w.elem_bytes + dst_es)
+        per = len(conv["scales"]) // w.num_layers
+        geo = wk.geometry()
+        geo.pop("elem_bytes")
     moved, spent, reps = 0, 0.0, 0
     while reps < reps_cap and (reps == 0 or spent < budget_s):
         t = time.perf_counter()
-        oracle.relayout(src_layers, dst, **wk.geometry())
+        if conv is None:
+            oracle.relayout(src_layers, dst, **wk.geometry())
+        else:
+            oracle.relayout_convert(src_layers, dst, src_dtype=conv["src_dtype"],
+                                    dst_dtype=conv["dst_dtype"], per_head=conv["per_head"],
+                                    scales=conv["scales"][:per * n], **geo)
         spent += time.perf_counter() - t
-        moved += 2 * per_layer * n
+        moved += per_layer * n
         reps += 1
     return moved, spent, n, reps
+
+
+BF16, E4M3 = 1, 2
+
+
+def conversion(args, w):
+    """(prefill workload, decode workload, convert dict or None) for --convert."""
+    import dataclasses
+
+    import numpy as np
+    if args.convert == "none":
+        return w, w, None
+    rng = np.random.default_rng(w.seed + 100)
+    scales = rng.uniform(0.01, 0.05, w.num_layers * w.num_components * w.kv_heads)
+    scales = scales.astype(np.float32)
+    fp8 = dataclasses.replace(w, elem_bytes=1, values="bits")
+    if args.convert == "bf16_to_fp8":
+        return w, fp8, dict(src_dtype=BF16, dst_dtype=E4M3, per_head=True, scales=scales)
+    return fp8, w, dict(src_dtype=E4M3, dst_dtype=BF16, per_head=True, scales=scales)
 
 
 def cpu_threads_used():
@@ -284,9 +322,10 @@ def run_ours(args):
     w = wl.get(args.config)
     if args.layers:
         w = w.with_layers(args.layers)
+    w, w_dst, conv = conversion(args, w)
     src = w.src_pools_torch(dev)
-    dst = w.dst_pools_torch(dev)
-    plan = RelayoutPlan(src, dst, **w.geometry())
+    dst = w_dst.dst_pools_torch(dev)
+    plan = RelayoutPlan(src, dst, convert=conv, **w.geometry())
     bytes_step = plan.bytes_read + plan.bytes_written
     stream = torch.cuda.current_stream(dev)
 
@@ -353,7 +392,7 @@ def run_ours(args):
     e2e = e2e_staged = None
     pinned_budget = 16 << 30
     pool_bytes = sum(t.numel() * t.element_size() for t in src + dst)
-    if not args.no_e2e and pool_bytes <= pinned_budget:
+    if not args.no_e2e and pool_bytes <= pinned_budget and conv is None:
         from prefill_decode_paged_gb300 import relayout_all_prealloc
         h_src = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in src]
         h_dst = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dst]
@@ -427,7 +466,7 @@ def run_ours(args):
         n_layers = max(1, min(L, 8))
         src_layers = [np.ascontiguousarray(t[:n_layers].cpu().numpy().view(w.int_dtype()))
                       for t in src]
-        moved, sec, nl, reps = oracle_sample(w, src_layers, args.cpu_budget_s)
+        moved, sec, nl, reps = oracle_sample(w, src_layers, args.cpu_budget_s, conv=conv)
         cpu = {"value": round(moved / sec / 1e9, 4), "unit": "GB/s", "cores": cpu_threads_used(),
                "kind": "oracle",
                "sample": f"{reps} pass(es) of the oracle over the first {nl} of {L} layers of "
@@ -438,7 +477,8 @@ def run_ours(args):
     hbm_peak, peak_src = measured_hbm_peak()
     avg_launch_ms = ms_all / K
     achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
-    traffic, _ = profiled_traffic(args.config, w.num_layers)
+    traffic, _ = profiled_traffic(
+        args.config if conv is None else f"{args.config}_{args.convert}", w.num_layers)
     prompts = w.num_requests
     value = whole_job_gbs(bytes_step, K, world, ms_all * 1e-3)
     out = {
@@ -452,10 +492,13 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if w.values == "randn" else f"u{8 * w.elem_bytes}",
+        "dtype": ("bf16" if w.values == "randn" else f"u{8 * w.elem_bytes}") if conv is None
+        else args.convert.replace("_to_", "->"),
         "data": "synthetic (seeded randn bf16 pools, seeded random block tables)",
         "config": {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
                    "mode": "whole-prompt (all layers, one launch per step)",
+                   "convert": None if conv is None else
+                   f"{args.convert} (FP8 = E4M3, one scale per layer, component and head)",
                    "prompts_per_step": prompts, "tokens_per_step": int(w.seq_lens.sum()),
                    "bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2 (no flush)" if bytes_step > 2 * 129e6 else

@@ -104,6 +104,31 @@ typedef struct kvr_desc {
 typedef struct kvr_plan kvr_plan;
 
 /*
+ * Element types for a relayout that changes the KV dtype on the way (page
+ * "PD 分离与 KV 传输", section "布局转换": one side keeps BF16 KV, the other
+ * FP8 KV, and the conversion is best done on the GPU around the transfer).
+ * FP8 is E4M3 of the OCP 8-bit floating point format (bias 7, subnormals, no
+ * infinities, S.1111.111 = NaN, largest finite 448). With scale s:
+ *   BF16 -> E4M3:  q = E4M3(x * fl32(1 / s)), nearest with ties to even; values
+ *                  beyond +-448 and infinities saturate to +-448; a NaN x gives
+ *                  S.1111.111 with the sign of x;
+ *   E4M3 -> BF16:  y = BF16(float(q) * s), nearest with ties to even; a NaN
+ *                  code gives sign | 0x7FC0 with the sign of the code.
+ * Products are single fp32 multiplications; 1/s is rounded to fp32 once.
+ */
+typedef enum kvr_dtype {
+    KVR_DTYPE_BF16 = 1,
+    KVR_DTYPE_FP8_E4M3 = 2
+} kvr_dtype;
+
+typedef struct kvr_convert {
+    int32_t src_dtype;     /* kvr_dtype of the prefill pools; desc->elem_bytes is its size */
+    int32_t dst_dtype;     /* kvr_dtype of the decode pools: the other of the two */
+    int32_t per_head;      /* 0: one scale per (layer, component); 1: per (layer, component, head) */
+    const float *scales;   /* host [L][C] or [L][C][H]: positive, finite; copied by the plan */
+} kvr_convert;
+
+/*
  * Validate *desc on the host and compute the bytes one full relayout reads
  * and writes (each = sum_r n_r * L * C * H * D * es, the page's "KV per token
  * times prompt length", section "传输的代价"). Makes no CUDA call and
@@ -119,6 +144,23 @@ kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
  * *out is set to the new plan, or to NULL on failure.
  */
 kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
+
+/*
+ * As kv_relayout_desc_bytes() / kv_relayout_plan(), for a relayout that also
+ * converts the element type (kvr_convert above; cv == NULL is a plain bit
+ * copy). Decode pools then hold dst_dtype elements: their layout is the same
+ * with dst_dtype's element size, and head_dim times each side's element size
+ * must be a multiple of 16 bytes (KVR_ERR_ALIGNMENT). Bytes read and written
+ * differ (e.g. 2 and 1 per element for BF16 -> E4M3). The plan's launches are
+ * kv_relayout_layer() / kv_relayout_all() as for any plan.
+ * Errors: KVR_ERR_UNSUPPORTED for a dtype pair other than BF16 <-> E4M3;
+ * KVR_ERR_INVALID_ARG if desc->elem_bytes is not src_dtype's size, per_head
+ * is not 0/1, or a scale is missing, not finite or not positive.
+ */
+kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc, const kvr_convert *cv,
+                                          int64_t *bytes_read, int64_t *bytes_written);
+kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_convert *cv,
+                                    kvr_plan **out);
 
 /*
  * Move layer `layer` of every request: one kernel launch on `stream`

@@ -137,9 +137,10 @@ int kvo_relayout(int32_t layer_begin, int32_t layer_end,
  *     4 exponent bits (bias 7), 3 mantissa bits, subnormals, no infinities,
  *     S.1111.111 is NaN, largest finite value 448;
  *   - quantize:   q = E4M3(x * fl32(1 / s)), round to nearest, ties to even,
- *     magnitudes above 448 (and infinities) saturate to +-448, NaN -> S.1111.111;
- *   - dequantize: y = BF16(float(q) * s), round to nearest, ties to even,
- *     NaN -> sign | 0x7FC0;
+ *     magnitudes above 448 (and infinities) saturate to +-448, a NaN x gives
+ *     S.1111.111 with the sign of x;
+ *   - dequantize: y = BF16(float(q) * s), round to nearest, ties to even, a
+ *     NaN code gives sign | 0x7FC0 with the sign of the code;
  *   - s is one positive scale per (layer, component), or per (layer,
  *     component, KV head).
  * All products are single fp32 multiplications (as the C float type gives).
@@ -294,13 +295,24 @@ int kvo_relayout_convert(int32_t layer_begin, int32_t layer_end,
                                 const uint32_t xb = ((uint32_t)from[0] | ((uint32_t)from[1] << 8)) << 16;
                                 float x;
                                 memcpy(&x, &xb, 4);
-                                const float inv = 1.0f / s;
-                                const float y = x * inv;
-                                to[0] = kvo_e4m3_encode(y);
+                                if (x != x) {
+                                    /* NaN keeps the input's sign (the sign of a NaN
+                                     * product is not fixed by IEEE 754) */
+                                    to[0] = (uint8_t)(((xb >> 24) & 0x80) | 0x7F);
+                                } else {
+                                    const float inv = 1.0f / s;
+                                    const float y = x * inv;
+                                    to[0] = kvo_e4m3_encode(y);
+                                }
                             } else {
-                                const float x = kvo_e4m3_decode(from[0]);
-                                const float y = x * s;
-                                const uint16_t b = kvo_bf16_encode(y);
+                                uint16_t b;
+                                if ((from[0] & 0x7F) == 0x7F) {
+                                    b = (uint16_t)(((from[0] & 0x80) << 8) | 0x7FC0);
+                                } else {
+                                    const float x = kvo_e4m3_decode(from[0]);
+                                    const float y = x * s;
+                                    b = kvo_bf16_encode(y);
+                                }
                                 to[0] = (uint8_t)(b & 0xFF);
                                 to[1] = (uint8_t)(b >> 8);
                             }

@@ -12,10 +12,13 @@
 // CTA per task; a slice is a contiguous part of the item's 16-byte chunks, so
 // a per-layer launch with few items still fills the GPU.
 //
-// Inside an item, ROW r (one head row of D * es bytes) is ordered
+// Inside an item, ROW r (one head row: D elements) is ordered
 // [token o][component c][head h], and chunk q = r * row_chunks + k is the
-// k-th 16-byte piece of row r. Consecutive threads read and write consecutive
-// 16-byte pieces of one head row, and the rows of one token follow each other.
+// k-th UNIT of row r. A unit is 16 bytes of the row when elements are copied
+// as bits; when the element type changes on the way (BF16 <-> FP8 E4M3) it is
+// 16 elements: 32 bytes on the BF16 side, 16 on the FP8 side. Consecutive
+// threads read and write consecutive units of one head row, and the rows of
+// one token follow each other.
 #pragma once
 
 #include <stdint.h>
@@ -64,13 +67,25 @@ struct KvrItem {
     int32_t ntok;       // tokens in the tile, >= 1
 };
 
+// Element conversion done on the way.
+enum KvrConv : int32_t {
+    KVR_CONV_NONE = 0,          // bit copy of es-byte elements
+    KVR_CONV_BF16_TO_E4M3 = 1,  // quantize: q = E4M3(x * (1/s))
+    KVR_CONV_E4M3_TO_BF16 = 2,  // dequantize: y = BF16(q * s)
+};
+
 struct KvrGeom {
     int32_t C, H, Hp, Hd, Bp, Bd;
-    int32_t row_bytes;          // D * es, a multiple of 16
-    int32_t row_chunks;         // row_bytes / 16
+    int32_t src_row_bytes;      // D * source element bytes, a multiple of 16
+    int32_t dst_row_bytes;      // D * destination element bytes, a multiple of 16
+    int32_t row_chunks;         // units per row
+    int32_t src_unit_bytes;     // bytes one unit reads (16, or 32 from a BF16 side)
+    int32_t dst_unit_bytes;     // bytes one unit writes (16, or 32 to a BF16 side)
+    int32_t conv;               // KvrConv
+    int32_t per_head;           // conversion scales per (layer, component[, head])
     KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp, div_Bd;
-    int64_t src_blk_bytes;      // Bp * Hp * row_bytes
-    int64_t dst_blk_bytes;      // Bd * Hd * row_bytes
+    int64_t src_blk_bytes;      // Bp * Hp * src_row_bytes
+    int64_t dst_blk_bytes;      // Bd * Hd * dst_row_bytes
     int64_t src_plane_bytes;    // Np * src_blk_bytes: one (layer, component) plane
     int64_t dst_plane_bytes;    // Nd * dst_blk_bytes
 };
@@ -81,6 +96,7 @@ struct KvrArgs {
     const KvrItem *items;
     const int32_t *sbt;                 // flat prefill block ids
     const int32_t *dbt;                 // flat decode block ids
+    const float *factors;               // conversion: 1/s (quantize) or s (dequantize)
     const unsigned char *src[KVR_MAX_TP];
     unsigned char *dst[KVR_MAX_TP];
     int32_t layer0;                     // first layer of this launch
@@ -104,11 +120,11 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
 }
 
-// Row r of an item -> (prefill shard, byte offset of the row) and
-// (decode shard, byte offset of the row).
+// Row r of an item -> (prefill shard, byte offset of the row),
+// (decode shard, byte offset of the row) and the index of its conversion scale.
 KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
                     const int32_t *dbt, uint32_t r, uint32_t *sp, int64_t *soff, uint32_t *dp,
-                    int64_t *doff) {
+                    int64_t *doff, uint32_t *fidx) {
     const uint32_t oc = g.div_H.div(r);
     const uint32_t h = r - oc * (uint32_t)g.H;
     const uint32_t o = g.div_C.div(oc);
@@ -131,7 +147,8 @@ KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const in
     *sp = s_sh;
     *dp = d_sh;
     *soff = plane * g.src_plane_bytes + sb * g.src_blk_bytes +
-            ((int64_t)so * g.Hp + s_loc) * g.row_bytes;
+            ((int64_t)so * g.Hp + s_loc) * g.src_row_bytes;
     *doff = plane * g.dst_plane_bytes + db * g.dst_blk_bytes +
-            ((int64_t)dof * g.Hd + d_loc) * g.row_bytes;
+            ((int64_t)dof * g.Hd + d_loc) * g.dst_row_bytes;
+    *fidx = g.per_head ? (uint32_t)plane * (uint32_t)g.H + h : (uint32_t)plane;
 }

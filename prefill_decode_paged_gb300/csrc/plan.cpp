@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <new>
 #include <vector>
 
@@ -65,8 +66,9 @@ int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count,
 
 }  // namespace
 
-kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
-                               int64_t *bytes_out) {
+kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_count,
+                               KvrHostPlan *hp, int64_t *bytes_read_out,
+                               int64_t *bytes_written_out) {
     if (d == nullptr) return KVR_ERR_INVALID_ARG;
     const int32_t L = d->num_layers, C = d->num_components, H = d->kv_heads, D = d->head_dim;
     const int32_t es = d->elem_bytes, Tp = d->src_tp, Td = d->dst_tp;
@@ -79,21 +81,46 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     if (es != 1 && es != 2 && es != 4) return KVR_ERR_UNSUPPORTED;
     if (Tp > KVR_MAX_TP || Td > KVR_MAX_TP) return KVR_ERR_UNSUPPORTED;
     if (H % Tp != 0 || H % Td != 0) return KVR_ERR_UNSUPPORTED;
-    int64_t row_bytes = 0;
-    if (!mul_fits({D, es}, &row_bytes) || row_bytes > INT32_MAX) return KVR_ERR_UNSUPPORTED;
-    if (row_bytes % 16 != 0) return KVR_ERR_ALIGNMENT;
+
+    // element types: a bit copy, or BF16 <-> E4M3 with positive finite scales
+    int32_t conv = KVR_CONV_NONE;
+    int64_t es_dst = es;
+    if (cv != nullptr) {
+        const bool quant = cv->src_dtype == KVR_DTYPE_BF16 && cv->dst_dtype == KVR_DTYPE_FP8_E4M3;
+        const bool dequant =
+            cv->src_dtype == KVR_DTYPE_FP8_E4M3 && cv->dst_dtype == KVR_DTYPE_BF16;
+        if (!quant && !dequant) return KVR_ERR_UNSUPPORTED;
+        if (es != (quant ? 2 : 1)) return KVR_ERR_INVALID_ARG;
+        if (cv->per_head != 0 && cv->per_head != 1) return KVR_ERR_INVALID_ARG;
+        if (cv->scales == nullptr) return KVR_ERR_INVALID_ARG;
+        const int64_t n_scales = (int64_t)L * C * (cv->per_head ? H : 1);
+        for (int64_t i = 0; i < n_scales; ++i)
+            if (!(cv->scales[i] > 0.0f) || !std::isfinite(cv->scales[i]))
+                return KVR_ERR_INVALID_ARG;
+        conv = quant ? KVR_CONV_BF16_TO_E4M3 : KVR_CONV_E4M3_TO_BF16;
+        es_dst = quant ? 1 : 2;
+    }
+    int64_t src_row = 0, dst_row = 0;
+    if (!mul_fits({D, es}, &src_row) || src_row > INT32_MAX || !mul_fits({D, es_dst}, &dst_row) ||
+        dst_row > INT32_MAX)
+        return KVR_ERR_UNSUPPORTED;
+    if (src_row % 16 != 0 || dst_row % 16 != 0) return KVR_ERR_ALIGNMENT;
+    // a unit is 16 bytes of a copied row, or 16 elements of a converted one
+    const int64_t unit_src = conv == KVR_CONV_NONE ? 16 : 16 * (int64_t)es;
+    const int64_t unit_dst = conv == KVR_CONV_NONE ? 16 : 16 * es_dst;
+    const int64_t row_units = src_row / unit_src;
     const int32_t Hp = H / Tp, Hd = H / Td;
 
     // pool extents
     int64_t src_pool = 0, dst_pool = 0, src_blk = 0, dst_blk = 0;
-    if (!mul_fits({(int64_t)L, C, Np, Bp, Hp, row_bytes}, &src_pool) ||
-        !mul_fits({(int64_t)L, C, Nd, Bd, Hd, row_bytes}, &dst_pool))
+    if (!mul_fits({(int64_t)L, C, Np, Bp, Hp, src_row}, &src_pool) ||
+        !mul_fits({(int64_t)L, C, Nd, Bd, Hd, dst_row}, &dst_pool))
         return KVR_ERR_UNSUPPORTED;
-    mul_fits({(int64_t)Bp, Hp, row_bytes}, &src_blk);
-    mul_fits({(int64_t)Bd, Hd, row_bytes}, &dst_blk);
-    // one item's 16-byte chunks must stay below 2^31 (32-bit chunk indices)
+    mul_fits({(int64_t)Bp, Hp, src_row}, &src_blk);
+    mul_fits({(int64_t)Bd, Hd, dst_row}, &dst_blk);
+    // one item's units must stay below 2^31 (32-bit chunk indices)
     int64_t item_chunks = 0;
-    if (!mul_fits({(int64_t)Bd, C, H, row_bytes / 16}, &item_chunks) || item_chunks > INT32_MAX)
+    if (!mul_fits({(int64_t)Bd, C, H, row_units}, &item_chunks) || item_chunks > INT32_MAX)
         return KVR_ERR_UNSUPPORTED;
 
     if (d->src_pools == nullptr || d->dst_pools == nullptr) return KVR_ERR_INVALID_ARG;
@@ -138,15 +165,18 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
                 return KVR_ERR_POOL_OVERLAP;
     }
 
-    int64_t bytes = 0;
-    if (!mul_fits({tokens, (int64_t)L, C, H, row_bytes}, &bytes)) return KVR_ERR_UNSUPPORTED;
-    if (bytes_out) *bytes_out = bytes;
+    int64_t bytes_read = 0, bytes_written = 0;
+    if (!mul_fits({tokens, (int64_t)L, C, H, src_row}, &bytes_read) ||
+        !mul_fits({tokens, (int64_t)L, C, H, dst_row}, &bytes_written))
+        return KVR_ERR_UNSUPPORTED;
+    if (bytes_read_out) *bytes_read_out = bytes_read;
+    if (bytes_written_out) *bytes_written_out = bytes_written;
     if (hp == nullptr) return KVR_OK;
 
-    // token tiles: whole decode blocks, about KVR_TARGET_ITEM_BYTES per layer
-    const int64_t blk_bytes_all_heads = (int64_t)Bd * C * H * row_bytes;
+    // token tiles: whole decode blocks, about KVR_TARGET_ITEM_BYTES read per layer
+    const int64_t blk_bytes_all_heads = (int64_t)Bd * C * H * src_row;
     int64_t per_tile = std::max<int64_t>(1, KVR_TARGET_ITEM_BYTES / blk_bytes_all_heads);
-    per_tile = std::min<int64_t>(per_tile, INT32_MAX / ((int64_t)Bd * C * H * (row_bytes / 16)));
+    per_tile = std::min<int64_t>(per_tile, INT32_MAX / ((int64_t)Bd * C * H * row_units));
     const int64_t tile = std::max<int64_t>(1, per_tile) * Bd;
 
     // launch sizes: CTAs = layers x items x slices must fit a 32-bit grid
@@ -161,8 +191,13 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
 
     KvrGeom &g = hp->g;
     g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
-    g.row_bytes = (int32_t)row_bytes;
-    g.row_chunks = (int32_t)(row_bytes / 16);
+    g.src_row_bytes = (int32_t)src_row;
+    g.dst_row_bytes = (int32_t)dst_row;
+    g.row_chunks = (int32_t)row_units;
+    g.src_unit_bytes = (int32_t)unit_src;
+    g.dst_unit_bytes = (int32_t)unit_dst;
+    g.conv = conv;
+    g.per_head = cv != nullptr ? cv->per_head : 0;
     g.div_rc = kvr_make_div((uint32_t)g.row_chunks);
     g.div_H = kvr_make_div((uint32_t)H);
     g.div_C = kvr_make_div((uint32_t)C);
@@ -180,7 +215,8 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
     hp->tile = (int32_t)tile;
     for (int32_t s = 0; s < Tp; ++s) hp->src[s] = d->src_pools[s];
     for (int32_t s = 0; s < Td; ++s) hp->dst[s] = d->dst_pools[s];
-    hp->bytes = bytes;
+    hp->bytes_read = bytes_read;
+    hp->bytes_written = bytes_written;
 
     try {
         hp->items.clear();
@@ -211,7 +247,19 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
         return KVR_ERR_NOMEM;
     }
 
-    const int64_t avg_chunks = n_items ? (bytes / L / 16) / n_items : 0;
+    try {
+        hp->factors.clear();
+        if (cv != nullptr) {
+            const int64_t n_scales = (int64_t)L * C * (cv->per_head ? H : 1);
+            for (int64_t i = 0; i < n_scales; ++i)
+                hp->factors.push_back(conv == KVR_CONV_BF16_TO_E4M3 ? 1.0f / cv->scales[i]
+                                                                    : cv->scales[i]);
+        }
+    } catch (const std::bad_alloc &) {
+        return KVR_ERR_NOMEM;
+    }
+
+    const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
     hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count, KVR_LAYER_CTAS_PER_SM);
     hp->slices_all =
         choose_slices((int64_t)L * n_items, avg_chunks, sm_count, KVR_TARGET_CTAS_PER_SM);
@@ -221,13 +269,15 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
 }
 
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,
-                        const int32_t *dev_dbt, int32_t layer0, int32_t slices) {
+                        const int32_t *dev_dbt, const float *dev_factors, int32_t layer0,
+                        int32_t slices) {
     KvrArgs a;
     memset(&a, 0, sizeof(a));
     a.g = hp.g;
     a.items = dev_items;
     a.sbt = dev_sbt;
     a.dbt = dev_dbt;
+    a.factors = dev_factors;
     for (int32_t s = 0; s < hp.src_tp; ++s) a.src[s] = (const unsigned char *)hp.src[s];
     for (int32_t s = 0; s < hp.dst_tp; ++s) a.dst[s] = (unsigned char *)hp.dst[s];
     a.layer0 = layer0;
@@ -238,19 +288,26 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const i
     return a;
 }
 
-extern "C" kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
-                                             int64_t *bytes_written) {
-    int64_t b = 0;
+extern "C" kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc,
+                                                     const kvr_convert *cv,
+                                                     int64_t *bytes_read,
+                                                     int64_t *bytes_written) {
+    int64_t r = 0, w = 0;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, 0, nullptr, &b);
+        st = kvr_build_host_plan(desc, cv, 0, nullptr, &r, &w);
     } catch (...) {
         return KVR_ERR_NOMEM;
     }
     if (st != KVR_OK) return st;
-    if (bytes_read) *bytes_read = b;
-    if (bytes_written) *bytes_written = b;
+    if (bytes_read) *bytes_read = r;
+    if (bytes_written) *bytes_written = w;
     return KVR_OK;
+}
+
+extern "C" kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
+                                             int64_t *bytes_written) {
+    return kv_relayout_desc_convert_bytes(desc, nullptr, bytes_read, bytes_written);
 }
 
 extern "C" const char *kv_relayout_strerror(kvr_status s) {

@@ -49,17 +49,20 @@ struct KvrHostPlan {
     std::vector<KvrItem> items;        // (request, token tile) work items
     std::vector<int32_t> sbt;          // used prefill block ids, request after request
     std::vector<int32_t> dbt;          // used decode block ids, request after request
-    int64_t bytes = 0;                 // bytes read (= bytes written) by one full relayout
+    std::vector<float> factors;        // conversion: 1/s (quantize) or s (dequantize)
+    int64_t bytes_read = 0;            // bytes one full relayout reads
+    int64_t bytes_written = 0;         // bytes one full relayout writes
     int32_t slices_all = 1;            // slices per item, whole-prompt launch
     int32_t slices_layer = 1;          // slices per item, per-layer launch
 };
 
-// Validate `d`; when `hp` is non-NULL also build the host plan for a device
-// with `sm_count` SMs. Never touches device memory.
-kvr_status kvr_build_host_plan(const kvr_desc *d, int sm_count, KvrHostPlan *hp,
-                               int64_t *bytes);
+// Validate `d` (and the conversion `cv`, NULL for a bit copy); when `hp` is
+// non-NULL also build the host plan for a device with `sm_count` SMs. Never
+// touches device memory. Either byte output may be NULL.
+kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_count,
+                               KvrHostPlan *hp, int64_t *bytes_read, int64_t *bytes_written);
 
 // Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,
-                        const int32_t *dev_sbt, const int32_t *dev_dbt, int32_t layer0,
-                        int32_t slices);
+                        const int32_t *dev_sbt, const int32_t *dev_dbt,
+                        const float *dev_factors, int32_t layer0, int32_t slices);

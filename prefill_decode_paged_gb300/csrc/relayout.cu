@@ -26,10 +26,11 @@
 
 struct kvr_plan {
     KvrHostPlan host;
-    void *dev_meta = nullptr;       // items, then prefill and decode block ids
+    void *dev_meta = nullptr;       // items, prefill and decode block ids, factors
     const KvrItem *dev_items = nullptr;
     const int32_t *dev_sbt = nullptr;
     const int32_t *dev_dbt = nullptr;
+    const float *dev_factors = nullptr;
     int device = 0;
 };
 
@@ -49,12 +50,99 @@ __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
                  : "memory");
 }
 
-// U: 16-byte loads each thread keeps in flight before its stores.
-template <int U>
+// -- element conversion (BF16 <-> FP8 E4M3) ------------------------------------
+//
+// Definitions (kv_relayout.h): quantize q = E4M3(x * (1/s)), nearest-even,
+// saturating at +-448, NaN kept with its sign; dequantize y = BF16(q * s),
+// nearest-even, a NaN code -> sign | 0x7FC0. The hardware conversion to E4M3
+// is applied to |y| and the input's sign is put back explicitly, so signed
+// zeros and NaN signs are exact; NaN codes are patched explicitly after the
+// hardware conversions to BF16.
+
+// E4M3 codes of two non-negative fp32 values: `hi` in bits 15..8, `lo` in 7..0.
+__device__ __forceinline__ uint32_t e4m3x2_rn_satfinite(float hi, float lo) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two BF16 elements (element 0 in the low half of `w`) -> two E4M3 codes
+// (element 0 in bits 7..0). The signs come from the inputs: since 1/s > 0 they
+// are the products' signs, and they also give a NaN input's sign (a NaN
+// product's sign is not fixed by IEEE 754; the GPU returns a positive one).
+__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
+    const float y0 = __fmul_rn(__uint_as_float(w << 16), inv);
+    const float y1 = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv);
+    const uint32_t sign = ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+    return e4m3x2_rn_satfinite(fabsf(y1), fabsf(y0)) | sign;
+}
+
+// 16 BF16 (two 16-byte pieces) -> 16 E4M3 codes (one 16-byte piece).
+__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float inv) {
+    uint4 o;
+    o.x = quant2(a.x, inv) | (quant2(a.y, inv) << 16);
+    o.y = quant2(a.z, inv) | (quant2(a.w, inv) << 16);
+    o.z = quant2(b.x, inv) | (quant2(b.y, inv) << 16);
+    o.w = quant2(b.z, inv) | (quant2(b.w, inv) << 16);
+    return o;
+}
+
+__device__ __forceinline__ float f16_to_f32(unsigned short h) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+
+// Two non-NaN E4M3 codes (element 0 in bits 7..0) -> two BF16 (element 0 in
+// the low half): exact decode to f16x2, exact widening, fp32 products,
+// nearest-even rounding to BF16 (overflow to infinity) by the hardware.
+__device__ __forceinline__ uint32_t dequant2(uint32_t codes, float s) {
+    uint32_t h2, out;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)codes));
+    const float y0 = __fmul_rn(f16_to_f32((unsigned short)(h2 & 0xFFFFu)), s);
+    const float y1 = __fmul_rn(f16_to_f32((unsigned short)(h2 >> 16)), s);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(y1), "f"(y0));
+    return out;
+}
+
+// Four E4M3 codes (one word) -> four BF16 (two words). A NaN code (x.1111.111)
+// gives sign | 0x7FC0 with the code's sign; the packed test finds such codes
+// four at a time, so the patch-up runs only for words that hold one.
+__device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t *lo, uint32_t *hi) {
+    uint32_t a = dequant2(w & 0xFFFFu, s), b = dequant2(w >> 16, s);
+    const uint32_t nan = ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+    if (nan != 0u) {
+        const uint32_t n0 = ((w & 0x80u) << 8) | 0x7FC0u, n1 = ((w & 0x8000u)) | 0x7FC0u;
+        const uint32_t n2 = ((w >> 8) & 0x8000u) | 0x7FC0u, n3 = ((w >> 16) & 0x8000u) | 0x7FC0u;
+        if (nan & 0x80u) a = (a & 0xFFFF0000u) | n0;
+        if (nan & 0x8000u) a = (a & 0x0000FFFFu) | (n1 << 16);
+        if (nan & 0x800000u) b = (b & 0xFFFF0000u) | n2;
+        if (nan & 0x80000000u) b = (b & 0x0000FFFFu) | (n3 << 16);
+    }
+    *lo = a;
+    *hi = b;
+}
+
+// 16 E4M3 codes (one 16-byte piece) -> 16 BF16 (two 16-byte pieces).
+__device__ __forceinline__ void dequant16(const uint4 &c, float s, uint4 *lo, uint4 *hi) {
+    dequant4(c.x, s, &lo->x, &lo->y);
+    dequant4(c.y, s, &lo->z, &lo->w);
+    dequant4(c.z, s, &hi->x, &hi->y);
+    dequant4(c.w, s, &hi->z, &hi->w);
+}
+
+// U: units each thread keeps in flight before its stores. CONV: KvrConv.
+// A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
+template <int U, int CONV>
 __global__ void __launch_bounds__(KVR_THREADS)
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
-    // (prefill row address, decode row address) of the rows this CTA copies
+    constexpr int NL = CONV == KVR_CONV_BF16_TO_E4M3 ? 2 : 1;
+    constexpr int NS = CONV == KVR_CONV_E4M3_TO_BF16 ? 2 : 1;
+    constexpr uint32_t SU = 16u * NL, DU = 16u * NS;   // bytes read / written per unit
+    // (prefill row address, decode row address) of the rows this CTA copies,
+    // and the rows' conversion factors
     __shared__ ulonglong2 rows[KVR_ROW_WINDOW];
+    __shared__ float row_factor[CONV == KVR_CONV_NONE ? 1 : KVR_ROW_WINDOW];
 
     // Wait for the grid this launch follows in its stream (a no-op without
     // programmatic dependent launch), then let the next launch start early.
@@ -73,35 +161,70 @@ __global__ void __launch_bounds__(KVR_THREADS)
         const uint32_t w1 = min(w0 + (uint32_t)KVR_ROW_WINDOW, r_end);
         // 1. one thread per row: the row's two addresses (block tables read here)
         for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
-            uint32_t sp, dp;
+            uint32_t sp, dp, fidx;
             int64_t soff, doff;
-            kvr_row(a.g, layer, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff);
+            kvr_row(a.g, layer, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff, &fidx);
             rows[r - w0] = make_ulonglong2((unsigned long long)(a.src[sp] + soff),
                                            (unsigned long long)(a.dst[dp] + doff));
+            if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
         }
         __syncthreads();
-        // 2. the 16-byte chunks of those rows: U loads in flight per thread
+        // 2. the units of those rows: U in flight per thread
         const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
         for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
-            uint4 v[U];
+            uint4 v[U][NL];
             unsigned char *to[U];
+            float f[U];
 #pragma unroll
             for (int k = 0; k < U; ++k) {
                 const uint32_t q = base + (uint32_t)k * KVR_THREADS;
                 to[k] = nullptr;
+                f[k] = 0.0f;
                 if (q < qb) {
                     const uint32_t r = a.g.div_rc.div(q);
-                    const uint32_t off = (q - r * rc) * 16u;
+                    const uint32_t u = q - r * rc;
                     const ulonglong2 p = rows[r - w0];
-                    v[k] = load_stream((const unsigned char *)p.x + off);
-                    to[k] = (unsigned char *)p.y + off;
+#pragma unroll
+                    for (int j = 0; j < NL; ++j)
+                        v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                    to[k] = (unsigned char *)p.y + u * DU;
+                    if (CONV != KVR_CONV_NONE) f[k] = row_factor[r - w0];
                 }
             }
 #pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (to[k] != nullptr) store_stream(to[k], v[k]);
+            for (int k = 0; k < U; ++k) {
+                if (to[k] == nullptr) continue;
+                if (CONV == KVR_CONV_NONE) {
+                    store_stream(to[k], v[k][0]);
+                } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
+                    store_stream(to[k], quant16(v[k][0], v[k][NL - 1], f[k]));
+                } else {
+                    uint4 lo, hi;
+                    dequant16(v[k][0], f[k], &lo, &hi);
+                    store_stream(to[k], lo);
+                    store_stream(to[k] + 16, hi);
+                }
+            }
         }
         __syncthreads();
+    }
+}
+
+using KvrKernel = void (*)(KvrArgs);
+
+// Kernel instance for a conversion and launch mode: 8 loads in flight per
+// thread for whole-prompt launches, 4 for per-layer ones.
+KvrKernel pick_kernel(int32_t conv, bool per_layer) {
+    switch (conv) {
+        case KVR_CONV_BF16_TO_E4M3:
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER / 2, KVR_CONV_BF16_TO_E4M3>
+                             : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3>;
+        case KVR_CONV_E4M3_TO_BF16:
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_E4M3_TO_BF16>
+                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16>;
+        default:
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_NONE>
+                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE>;
     }
 }
 
@@ -110,8 +233,8 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
-    const KvrArgs a =
-        kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt, layer0, slices);
+    const KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt,
+                                      p->dev_factors, layer0, slices);
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
 
@@ -125,10 +248,9 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = per_layer
-                              ? cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL_LAYER>, a)
-                              : cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL>, a);
-    return e == cudaSuccess ? KVR_OK : KVR_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, pick_kernel(p->host.g.conv, per_layer), a) == cudaSuccess
+               ? KVR_OK
+               : KVR_ERR_CUDA;
 }
 
 // The first and last byte of a pool must be memory device `dev` can access:
@@ -175,7 +297,7 @@ kvr_status check_pools(const KvrHostPlan &hp, int dev) {
 
 }  // namespace
 
-extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
+static kvr_status make_plan(const kvr_desc *desc, const kvr_convert *cv, kvr_plan **out) {
     if (out == nullptr) return KVR_ERR_INVALID_ARG;
     *out = nullptr;
     int dev = 0, sms = 0;
@@ -187,7 +309,7 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
     if (p == nullptr) return KVR_ERR_NOMEM;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, sms, &p->host, nullptr);
+        st = kvr_build_host_plan(desc, cv, sms, &p->host, nullptr, nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
@@ -200,8 +322,10 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
     const size_t items_bytes = p->host.items.size() * sizeof(KvrItem);
     const size_t sbt_bytes = p->host.sbt.size() * sizeof(int32_t);
     const size_t dbt_bytes = p->host.dbt.size() * sizeof(int32_t);
+    const size_t fac_bytes = p->host.factors.size() * sizeof(float);
     if (items_bytes > 0) {
-        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes + dbt_bytes) != cudaSuccess) {
+        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes + dbt_bytes + fac_bytes) !=
+            cudaSuccess) {
             cudaGetLastError();
             delete p;
             return KVR_ERR_NOMEM;
@@ -212,7 +336,10 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
             cudaMemcpy(base + items_bytes, p->host.sbt.data(), sbt_bytes,
                        cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(base + items_bytes + sbt_bytes, p->host.dbt.data(), dbt_bytes,
-                       cudaMemcpyHostToDevice) != cudaSuccess) {
+                       cudaMemcpyHostToDevice) != cudaSuccess ||
+            (fac_bytes > 0 &&
+             cudaMemcpy(base + items_bytes + sbt_bytes + dbt_bytes, p->host.factors.data(),
+                        fac_bytes, cudaMemcpyHostToDevice) != cudaSuccess)) {
             cudaFree(p->dev_meta);
             delete p;
             return KVR_ERR_CUDA;
@@ -220,9 +347,24 @@ extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
         p->dev_items = (const KvrItem *)base;
         p->dev_sbt = (const int32_t *)(base + items_bytes);
         p->dev_dbt = (const int32_t *)(base + items_bytes + sbt_bytes);
+        if (fac_bytes > 0)
+            p->dev_factors = (const float *)(base + items_bytes + sbt_bytes + dbt_bytes);
     }
     *out = p;
     return KVR_OK;
+}
+
+extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
+    return make_plan(desc, nullptr, out);
+}
+
+extern "C" kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_convert *cv,
+                                               kvr_plan **out) {
+    if (cv == nullptr) {
+        if (out != nullptr) *out = nullptr;
+        return KVR_ERR_INVALID_ARG;
+    }
+    return make_plan(desc, cv, out);
 }
 
 extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
@@ -239,8 +381,8 @@ extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
 extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
                                              int64_t *bytes_written) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
-    if (bytes_read) *bytes_read = plan->host.bytes;
-    if (bytes_written) *bytes_written = plan->host.bytes;
+    if (bytes_read) *bytes_read = plan->host.bytes_read;
+    if (bytes_written) *bytes_written = plan->host.bytes_written;
     return KVR_OK;
 }
 
@@ -309,7 +451,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
 
     KvrHostPlan hp;
     try {
-        st = kvr_build_host_plan(desc, sc.sms, &hp, nullptr);
+        st = kvr_build_host_plan(desc, nullptr, sc.sms, &hp, nullptr, nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
@@ -335,8 +477,8 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
 
     const KvrArgs a = kvr_launch_args(hp, (const KvrItem *)sc.addr,
                                       (const int32_t *)(sc.addr + items_bytes),
-                                      (const int32_t *)(sc.addr + items_bytes + sbt_bytes), 0,
-                                      hp.slices_all);
+                                      (const int32_t *)(sc.addr + items_bytes + sbt_bytes),
+                                      nullptr, 0, hp.slices_all);
     const uint64_t grid = (uint64_t)hp.num_layers * a.tasks_per_layer;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -348,7 +490,8 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL>, a) == cudaSuccess
+    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE>, a) ==
+                   cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
 }

@@ -26,7 +26,10 @@ STATUS = {
 PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_all", "kv_relayout_plan_bytes", "kv_relayout_plan_destroy",
-           "kv_relayout_strerror", "kv_relayout_all_prealloc")
+           "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
+           "kv_relayout_plan_convert")
+DTYPE_BF16 = 1
+DTYPE_FP8_E4M3 = 2
 
 
 class KVRelayoutError(RuntimeError):
@@ -34,6 +37,11 @@ class KVRelayoutError(RuntimeError):
         self.status = status
         self.name = STATUS.get(status, str(status))
         super().__init__(f"{what}: {self.name} ({_strerror(status)})")
+
+
+class KvrConvert(ctypes.Structure):
+    _fields_ = [("src_dtype", ctypes.c_int32), ("dst_dtype", ctypes.c_int32),
+                ("per_head", ctypes.c_int32), ("scales", ctypes.c_void_p)]
 
 
 class KvrDesc(ctypes.Structure):
@@ -80,6 +88,10 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_strerror.argtypes = [i32]
         lib.kv_relayout_all_prealloc.restype = i32
         lib.kv_relayout_all_prealloc.argtypes = [p, p]
+        lib.kv_relayout_desc_convert_bytes.restype = i32
+        lib.kv_relayout_desc_convert_bytes.argtypes = [p, p, p, p]
+        lib.kv_relayout_plan_convert.restype = i32
+        lib.kv_relayout_plan_convert.argtypes = [p, p, p]
         _lib = lib
     return _lib
 
@@ -131,12 +143,29 @@ class _Desc:
         self.desc = d
 
 
-def desc_bytes(src_pools, dst_pools, **geometry):
+class _Convert:
+    """Keeps the C conversion descriptor and its scales alive."""
+
+    def __init__(self, src_dtype, dst_dtype, scales, per_head=False):
+        self.scales = np.ascontiguousarray(scales, dtype=np.float32)
+        c = KvrConvert()
+        c.src_dtype, c.dst_dtype, c.per_head = int(src_dtype), int(dst_dtype), int(per_head)
+        c.scales = self.scales.ctypes.data if self.scales.size else None
+        self.conv = c
+
+
+def desc_bytes(src_pools, dst_pools, convert=None, **geometry):
     """Validate a descriptor on the host; return (bytes_read, bytes_written)."""
     d = _Desc(src_pools, dst_pools, **geometry)
     r, w = ctypes.c_int64(), ctypes.c_int64()
-    st = library().kv_relayout_desc_bytes(ctypes.byref(d.desc), ctypes.byref(r),
-                                          ctypes.byref(w))
+    if convert is None:
+        st = library().kv_relayout_desc_bytes(ctypes.byref(d.desc), ctypes.byref(r),
+                                              ctypes.byref(w))
+    else:
+        cv = _Convert(**convert)
+        st = library().kv_relayout_desc_convert_bytes(ctypes.byref(d.desc),
+                                                      ctypes.byref(cv.conv), ctypes.byref(r),
+                                                      ctypes.byref(w))
     if st != 0:
         raise KVRelayoutError(st, "kv_relayout_desc_bytes")
     return r.value, w.value
@@ -175,13 +204,21 @@ class RelayoutPlan:
     ``src_pools``/``dst_pools``: one device buffer (torch tensor or address)
     per TP shard, layout [L][C][N][B][H / tp][D]. Block tables are CSR:
     ``src_off``/``dst_off`` (R + 1 offsets) into ``src_bt``/``dst_bt``.
+    ``convert``: None (bit copy) or dict(src_dtype=..., dst_dtype=..., scales=...,
+    per_head=False) for a BF16 <-> FP8 E4M3 relayout (``kv_relayout_plan_convert``).
     """
 
-    def __init__(self, src_pools, dst_pools, **geometry):
+    def __init__(self, src_pools, dst_pools, convert=None, **geometry):
+        self._h = None
         self._d = _Desc(src_pools, dst_pools, **geometry)
         self.num_layers = geometry["num_layers"]
         h = ctypes.c_void_p()
-        st = library().kv_relayout_plan(ctypes.byref(self._d.desc), ctypes.byref(h))
+        if convert is None:
+            st = library().kv_relayout_plan(ctypes.byref(self._d.desc), ctypes.byref(h))
+        else:
+            self._cv = _Convert(**convert)
+            st = library().kv_relayout_plan_convert(ctypes.byref(self._d.desc),
+                                                    ctypes.byref(self._cv.conv), ctypes.byref(h))
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_plan")
         self._h = h

@@ -18,13 +18,15 @@ struct Extents {
     int64_t src_bytes, dst_bytes;
 };
 
-Extents pool_extents(const kvr_desc *d) {
-    const int64_t row = (int64_t)d->head_dim * d->elem_bytes;
+Extents pool_extents(const kvr_desc *d, const kvr_convert *cv) {
+    const int64_t src_row = (int64_t)d->head_dim * d->elem_bytes;
+    int64_t dst_row = src_row;
+    if (cv != nullptr) dst_row = (int64_t)d->head_dim * (cv->dst_dtype == KVR_DTYPE_BF16 ? 2 : 1);
     Extents e;
     e.src_bytes = (int64_t)d->num_layers * d->num_components * d->src_num_blocks *
-                  d->src_block_size * (d->kv_heads / d->src_tp) * row;
+                  d->src_block_size * (d->kv_heads / d->src_tp) * src_row;
     e.dst_bytes = (int64_t)d->num_layers * d->num_components * d->dst_num_blocks *
-                  d->dst_block_size * (d->kv_heads / d->dst_tp) * row;
+                  d->dst_block_size * (d->kv_heads / d->dst_tp) * dst_row;
     return e;
 }
 
@@ -33,16 +35,20 @@ Extents pool_extents(const kvr_desc *d) {
 // otherwise only check. Returns the number of out-of-bounds or misaligned
 // chunk addresses (all skipped), or a negative kvr_status. *chunks receives
 // the number of chunks visited.
-int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chunks) {
+int64_t walk(const kvr_desc *d, const kvr_convert *cv, int sm_count, int layer, int copy,
+             int64_t *chunks) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
+    kvr_status st = kvr_build_host_plan(d, cv, sm_count, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
+    if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
     const int all = layer < 0;
     const int32_t slices = all ? hp.slices_all : hp.slices_layer;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
-                                      all ? 0 : layer, slices);
+                                      hp.factors.data(), all ? 0 : layer, slices);
     const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
-    const Extents ext = pool_extents(d);
+    const Extents ext = pool_extents(d, cv);
+    const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
+    const int64_t n_factors = (int64_t)hp.factors.size();
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     const uint32_t U = all ? KVR_UNROLL : KVR_UNROLL_LAYER;
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
@@ -62,12 +68,13 @@ int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chun
             const uint32_t w1 = w0 + KVR_ROW_WINDOW < r_end ? w0 + KVR_ROW_WINDOW : r_end;
             for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
                 for (uint32_t r = w0 + tid; r < w1; r += KVR_THREADS) {
-                    uint32_t sp, dp;
+                    uint32_t sp, dp, fidx;
                     int64_t soff, doff;
-                    kvr_row(a.g, l, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff);
+                    kvr_row(a.g, l, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff, &fidx);
                     if (sp >= (uint32_t)hp.src_tp || dp >= (uint32_t)hp.dst_tp || soff < 0 ||
-                        doff < 0 || soff + a.g.row_bytes > ext.src_bytes ||
-                        doff + a.g.row_bytes > ext.dst_bytes) {
+                        doff < 0 || soff + a.g.src_row_bytes > ext.src_bytes ||
+                        doff + a.g.dst_row_bytes > ext.dst_bytes ||
+                        (a.g.conv != KVR_CONV_NONE && (int64_t)fidx >= n_factors)) {
                         ++bad;
                         rows_src[r - w0] = rows_dst[r - w0] = UINT64_MAX;
                         continue;
@@ -83,15 +90,17 @@ int64_t walk(const kvr_desc *d, int sm_count, int layer, int copy, int64_t *chun
                         const uint32_t q = base + k * KVR_THREADS;
                         if (q >= qb) continue;
                         const uint32_t r = a.g.div_rc.div(q);
-                        const uint32_t off = (q - r * rc) * 16u;
+                        const uint32_t u = q - r * rc;
                         ++visited;
                         if (r < w0 || r >= w1 || rows_src[r - w0] == UINT64_MAX) {
                             ++bad;
                             continue;
                         }
-                        const uint64_t from = rows_src[r - w0] + off;
-                        const uint64_t to = rows_dst[r - w0] + off;
-                        if (from % 16 != 0 || to % 16 != 0 || off + 16 > (uint32_t)a.g.row_bytes) {
+                        const uint64_t from = rows_src[r - w0] + (uint64_t)u * su;
+                        const uint64_t to = rows_dst[r - w0] + (uint64_t)u * du;
+                        if (from % 16 != 0 || to % 16 != 0 ||
+                            (u + 1) * su > (uint32_t)a.g.src_row_bytes ||
+                            (u + 1) * du > (uint32_t)a.g.dst_row_bytes) {
                             ++bad;
                             continue;
                         }
@@ -111,18 +120,24 @@ extern "C" {
 
 // Relayout on host pools through the kernel's decomposition. layer < 0: all layers.
 int64_t emu_relayout(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
-    return walk(d, sm_count, layer, 1, chunks);
+    return walk(d, nullptr, sm_count, layer, 1, chunks);
 }
 
 // Bounds/alignment check of every address of a launch (pools are never touched).
 int64_t emu_check(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
-    return walk(d, sm_count, layer, 0, chunks);
+    return walk(d, nullptr, sm_count, layer, 0, chunks);
+}
+
+// The same check for a converting relayout (units of 16 elements).
+int64_t emu_check_convert(const kvr_desc *d, const kvr_convert *cv, int sm_count, int32_t layer,
+                          int64_t *chunks) {
+    return walk(d, cv, sm_count, layer, 0, chunks);
 }
 
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, sm_count, &hp, nullptr);
+    kvr_status st = kvr_build_host_plan(d, nullptr, sm_count, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     const int64_t n = (int64_t)hp.items.size();
     out[0] = n;

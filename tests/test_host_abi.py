@@ -298,3 +298,68 @@ def test_launch_shapes(emu):
     assert emu.emu_plan_info(ctypes.byref(desc.desc), SMS, info) == 0
     assert info[5] == 48
     assert info[0] == sum(-(-int(n) // 48) for n in w.seq_lens)
+
+
+# -- converting relayout (host side) -------------------------------------------------
+
+BF16, E4M3 = kr.DTYPE_BF16, kr.DTYPE_FP8_E4M3
+
+
+def _conv(w, src_dtype=BF16, dst_dtype=E4M3, per_head=False, value=0.05):
+    n = w.num_layers * w.num_components * (w.kv_heads if per_head else 1)
+    return dict(src_dtype=src_dtype, dst_dtype=dst_dtype, per_head=per_head,
+                scales=np.full(n, value, np.float32))
+
+
+def test_convert_bytes_and_errors(cuda_lib):
+    w = wl.llama70b()
+    s, d = fake_pools(w)
+    assert kr.desc_bytes(s, d, convert=_conv(w), **w.geometry()) == (1_342_177_280,
+                                                                      671_088_640)
+    w1 = dataclasses.replace(w, elem_bytes=1)
+    assert kr.desc_bytes(s, d, convert=_conv(w1, E4M3, BF16, True), **w1.geometry()) == (
+        671_088_640, 1_342_177_280)
+
+    def st(conv, geo=None):
+        return status_of(lambda: kr.desc_bytes(s, d, convert=conv, **(geo or w.geometry())))
+    assert st(_conv(w, BF16, BF16)) == "KVR_ERR_UNSUPPORTED"
+    assert st(_conv(w, E4M3, E4M3)) == "KVR_ERR_UNSUPPORTED"
+    assert st(_conv(w, 7, E4M3)) == "KVR_ERR_UNSUPPORTED"
+    assert st(_conv(w1, BF16, E4M3), w1.geometry()) == "KVR_ERR_INVALID_ARG"  # es must be 2
+    assert st(_conv(w, E4M3, BF16)) == "KVR_ERR_INVALID_ARG"                  # es must be 1
+    c = _conv(w); c["per_head"] = 2
+    assert st(c) == "KVR_ERR_INVALID_ARG"
+    for bad in (0.0, -1.0, np.inf, np.nan):
+        c = _conv(w); c["scales"] = c["scales"].copy(); c["scales"][7] = bad
+        assert st(c) == "KVR_ERR_INVALID_ARG", bad
+    c = _conv(w); c["scales"] = np.zeros(0, np.float32)
+    assert st(c) == "KVR_ERR_INVALID_ARG"
+    g = dict(w.geometry(), head_dim=8)               # 16-byte BF16 rows, 8-byte FP8 rows
+    assert st(_conv(w), g) == "KVR_ERR_ALIGNMENT"
+
+
+@pytest.mark.parametrize("name,direction", [("llama70b", "quant"), ("llama70b", "dequant"),
+                                            ("qwen32k", "quant"), ("dsv3mla", "quant"),
+                                            ("dsv3mla", "dequant"), ("llama8b", "dequant")])
+def test_convert_launches_stay_in_bounds(emu, name, direction):
+    """Every address of the converting launches (units of 16 elements: 32 bytes on the
+    BF16 side, 16 on the FP8 side) against the pools' full extents."""
+    emu.emu_check_convert.restype = ctypes.c_int64
+    emu.emu_check_convert.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.c_int32, ctypes.c_void_p]
+    w = wl.get(name)
+    if direction == "dequant":
+        w = dataclasses.replace(w, elem_bytes=1)
+        conv = _conv(w, E4M3, BF16, per_head=True)
+    else:
+        conv = _conv(w)
+    s, d = fake_pools(w, gap=1 << 33)                 # room for 2-byte decode elements
+    desc = kr._Desc(s, d, **w.geometry())
+    cv = kr._Convert(**conv)
+    n = ctypes.c_int64()
+    units_per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim // 16
+    layers = [-1] if name == "llama70b" else [0, w.num_layers - 1]
+    for l in layers:
+        assert emu.emu_check_convert(ctypes.byref(desc.desc), ctypes.byref(cv.conv), SMS, l,
+                                     ctypes.byref(n)) == 0
+        assert n.value == units_per_layer * (w.num_layers if l < 0 else 1)

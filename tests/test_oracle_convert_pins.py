@@ -225,3 +225,32 @@ def test_quantize_then_dequantize_stays_within_e4m3_precision(oracle_lib):
         rel = np.abs(xb[m] - xa[m]) / np.abs(xa[m])
         assert m.sum() > 1000 and rel.max() <= 2.0 ** -4 + 2.0 ** -7
         assert np.all(b[~cover] == 0)
+
+
+def test_nan_keeps_its_sign_through_both_conversions(oracle_lib):
+    """A NaN's sign comes from the input, not from the (platform-dependent) sign of
+    a NaN product."""
+    w = _conv_workload(40, num_layers=1, num_components=1, kv_heads=1, head_dim=16,
+                       src_tp=1, dst_tp=1, src_block=4, dst_block=4, seq_lens=[2])
+    src = [np.zeros(w.src_shape(), np.uint16)]
+    rows = src[0].reshape(-1, 16)
+    ids = w.src_bt[:1]
+    v = src[0].reshape(w.src_num_blocks, 4, 16)
+    v[ids[0], 0, :8] = 0x7FC1                        # +NaN
+    v[ids[0], 0, 8:] = 0xFFC1                        # -NaN
+    q = [np.zeros(w.dst_shape(), np.uint8)]
+    oracle.relayout_convert(src, q, src_dtype=oracle.BF16, dst_dtype=oracle.E4M3, per_head=0,
+                            scales=np.ones(1, np.float32), lib=oracle_lib, **_geometry(w))
+    got = q[0].reshape(w.dst_num_blocks, 4, 16)[w.dst_bt[0], 0]
+    assert list(got[:8]) == [0x7F] * 8 and list(got[8:]) == [0xFF] * 8
+    w8 = dataclasses.replace(w, elem_bytes=1)
+    codes = [np.zeros(w.src_shape(), np.uint8)]
+    c = codes[0].reshape(w.src_num_blocks, 4, 16)
+    c[ids[0], 0, :8] = 0x7F
+    c[ids[0], 0, 8:] = 0xFF
+    y = [np.zeros(w.dst_shape(), np.uint16)]
+    oracle.relayout_convert(codes, y, src_dtype=oracle.E4M3, dst_dtype=oracle.BF16, per_head=0,
+                            scales=np.ones(1, np.float32), lib=oracle_lib, **_geometry(w8))
+    got = y[0].reshape(w.dst_num_blocks, 4, 16)[w.dst_bt[0], 0]
+    assert list(got[:8]) == [0x7FC0] * 8 and list(got[8:]) == [0xFFC0] * 8
+    del rows

@@ -51,6 +51,10 @@ CONVERT_MUTANTS = {
     "bf16_ties_always_up": ("pick = ((lo >> 16) & 1) ? lo + 0x10000u : lo;",
                             "pick = lo + 0x10000u;"),
     "bf16_high_byte_dropped": ("to[1] = (uint8_t)(b >> 8);", "to[1] = 0;"),
+    "nan_sign_from_nowhere": ("to[0] = (uint8_t)(((xb >> 24) & 0x80) | 0x7F);",
+                              "to[0] = (uint8_t)0x7F;"),
+    "nan_code_sign_dropped": ("b = (uint16_t)(((from[0] & 0x80) << 8) | 0x7FC0);",
+                              "b = (uint16_t)0x7FC0;"),
 }
 
 CONVERT_BATTERY = textwrap.dedent("""
@@ -68,6 +72,7 @@ CONVERT_BATTERY = textwrap.dedent("""
         P.test_quantize_placement_reduces_to_a_copy_of_codes(lib, per_head)
         P.test_dequantize_placement_reduces_to_a_copy_of_values(lib, per_head)
     P.test_quantize_then_dequantize_stays_within_e4m3_precision(lib)
+    P.test_nan_keeps_its_sign_through_both_conversions(lib)
 """)
 
 BATTERY = textwrap.dedent("""
