@@ -56,6 +56,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kvo_relayout.restype = ctypes.c_int
     lib.kvo_relayout.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                  i64, i64, p, p, i32, p, p, p, p, p]
+    lib.kvo_relayout_general.restype = ctypes.c_int
+    lib.kvo_relayout_general.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, p,
+                                         i32, i32, i32, i32, p, i64, i64, i64, p, i64, i64,
+                                         i64, i32, p, p, p, p, p]
     lib.kvo_relayout_convert.restype = ctypes.c_int
     lib.kvo_relayout_convert.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, p, i32,
                                          i32, i32, i32, i64, i64, p, p, i32, p, p, p, p, p]
@@ -195,3 +199,62 @@ def relayout_convert(src_pools, dst_pools, *, num_layers, num_components, kv_hea
                                   db.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle rejected the conversion (status {rc})")
+
+
+def _views_table(views, tp, num_layers, num_components):
+    """Bases and shared (block, token, head) byte strides of [shard][layer][comp] views."""
+    bases = np.zeros(tp * num_layers * num_components, dtype=np.uint64)
+    strides = None
+    for sh in range(tp):
+        for l in range(num_layers):
+            for c in range(num_components):
+                v = views[sh][l][c]
+                if v.ndim != 4 or v.strides[3] != v.itemsize:
+                    raise ValueError("each view must be [block][token][head][dim], dim contiguous")
+                if strides is None:
+                    strides = v.strides[:3]
+                elif v.strides[:3] != strides:
+                    raise ValueError("all views of a side must share their strides")
+                bases[(sh * num_layers + l) * num_components + c] = v.ctypes.data
+    return bases, strides
+
+
+def relayout_general(src_views, dst_views, *, num_layers, num_components, kv_heads, head_dim,
+                     src_tp, dst_tp, src_block, dst_block, seq_lens, src_off, src_bt, dst_off,
+                     dst_bt, elem_bytes=None, src_dtype=0, dst_dtype=0, per_head=0,
+                     scales=None, layer_begin=0, layer_end=None, lib=None, **_ignored):
+    """The oracle on any layout. ``src_views[s][l][c]`` / ``dst_views[s][l][c]`` are numpy
+    views [block][token][head][dim] (dim contiguous) of the shard/layer/component's
+    pool; they are written in place on the destination side."""
+    lib = lib or load()
+    if layer_end is None:
+        layer_end = num_layers
+    sb_, ss = _views_table(src_views, src_tp, num_layers, num_components)
+    db_, ds = _views_table(dst_views, dst_tp, num_layers, num_components)
+    if elem_bytes is None:
+        elem_bytes = src_views[0][0][0].itemsize
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    so = np.ascontiguousarray(src_off, dtype=np.int64)
+    sbt = np.ascontiguousarray(src_bt, dtype=np.int32)
+    do = np.ascontiguousarray(dst_off, dtype=np.int64)
+    dbt = np.ascontiguousarray(dst_bt, dtype=np.int32)
+    sbt = sbt if sbt.size else np.zeros(1, np.int32)
+    dbt = dbt if dbt.size else np.zeros(1, np.int32)
+    sc = np.ascontiguousarray(scales if scales is not None else [1.0], dtype=np.float32)
+    rc = lib.kvo_relayout_general(layer_begin, layer_end, num_layers, num_components, kv_heads,
+                                  head_dim, src_dtype, dst_dtype, elem_bytes, int(per_head),
+                                  sc.ctypes.data, src_tp, dst_tp, src_block, dst_block,
+                                  sb_.ctypes.data, ss[0], ss[1], ss[2], db_.ctypes.data, ds[0],
+                                  ds[1], ds[2], len(lens), lens.ctypes.data, so.ctypes.data,
+                                  sbt.ctypes.data, do.ctypes.data, dbt.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the request (status {rc})")
+
+
+def standard_views(pools, num_layers, num_components, num_blocks, block, heads, head_dim):
+    """[shard][layer][comp] views of pools in the layout [L][C][N][B][H/T][D]."""
+    out = []
+    for p in pools:
+        v = p.reshape(num_layers, num_components, num_blocks, block, heads, head_dim)
+        out.append([[v[l, c] for c in range(num_components)] for l in range(num_layers)])
+    return out

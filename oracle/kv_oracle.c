@@ -343,3 +343,114 @@ void kvo_bf16_encode_array(const float *x, uint16_t *out, int64_t n)
     for (int64_t i = 0; i < n; ++i)
         out[i] = kvo_bf16_encode(x[i]);
 }
+
+/* ---------------------------------------------------------------------------
+ * Any physical layout (page "PD 分离与 KV 传输", section "布局转换": attention
+ * backends differ in physical layout -- whether K and V are stored together,
+ * and the order of the head and token dimensions). Reading taken: each side
+ * is, per (TP shard, layer, component), a strided view [block][token][head][dim]
+ * whose head rows (dim) are contiguous; base[(shard * L + layer) * C + comp]
+ * is the address of element [0][0][0][0] of that view, and the block, token
+ * and head strides (in bytes) are shared by all views of a side. The standard
+ * layout [L][C][N][B][H/T][D] is one such choice; per-layer buffers, K and V
+ * in separate buffers, K/V interleaved per block and head-major blocks are
+ * others, and so is a contiguous [tokens][heads][dim] staging buffer (pd.py's
+ * gathered shape) seen as blocks of one token.
+ *
+ * src_dtype / dst_dtype: 0 (elements copied as elem_bytes raw bytes; both
+ * must then be 0) or KVO_BF16 / KVO_E4M3 (converted as kvo_relayout_convert).
+ * ------------------------------------------------------------------------- */
+static void convert_element(int32_t src_dtype, const uint8_t *from, uint8_t *to, float s)
+{
+    if (src_dtype == KVO_BF16) {
+        const uint32_t xb = ((uint32_t)from[0] | ((uint32_t)from[1] << 8)) << 16;
+        float x;
+        memcpy(&x, &xb, 4);
+        if (x != x) {
+            to[0] = (uint8_t)(((xb >> 24) & 0x80) | 0x7F);
+        } else {
+            const float inv = 1.0f / s;
+            to[0] = kvo_e4m3_encode(x * inv);
+        }
+    } else {
+        uint16_t b;
+        if ((from[0] & 0x7F) == 0x7F) {
+            b = (uint16_t)(((from[0] & 0x80) << 8) | 0x7FC0);
+        } else {
+            b = kvo_bf16_encode(kvo_e4m3_decode(from[0]) * s);
+        }
+        to[0] = (uint8_t)(b & 0xFF);
+        to[1] = (uint8_t)(b >> 8);
+    }
+}
+
+int kvo_relayout_general(int32_t layer_begin, int32_t layer_end,
+                         int32_t num_layers, int32_t num_components,
+                         int32_t kv_heads, int32_t head_dim,
+                         int32_t src_dtype, int32_t dst_dtype, int32_t elem_bytes,
+                         int32_t per_head, const float *scales,
+                         int32_t src_tp, int32_t dst_tp,
+                         int32_t src_block, int32_t dst_block,
+                         const uint64_t *src_base, int64_t s_block_stride,
+                         int64_t s_token_stride, int64_t s_head_stride,
+                         const uint64_t *dst_base, int64_t d_block_stride,
+                         int64_t d_token_stride, int64_t d_head_stride,
+                         int32_t num_requests, const int32_t *seq_lens,
+                         const int64_t *src_off, const int32_t *src_bt,
+                         const int64_t *dst_off, const int32_t *dst_bt)
+{
+    if (kv_heads % src_tp != 0 || kv_heads % dst_tp != 0)
+        return -1;
+    const int converting = src_dtype != 0;
+    if (converting && !((src_dtype == KVO_BF16 && dst_dtype == KVO_E4M3) ||
+                        (src_dtype == KVO_E4M3 && dst_dtype == KVO_BF16)))
+        return -1;
+    if (!converting && dst_dtype != 0)
+        return -1;
+    const int64_t src_es = !converting ? elem_bytes : (src_dtype == KVO_BF16 ? 2 : 1);
+    const int64_t dst_es = !converting ? elem_bytes : (dst_dtype == KVO_BF16 ? 2 : 1);
+    const int64_t src_heads = kv_heads / src_tp;
+    const int64_t dst_heads = kv_heads / dst_tp;
+    const int64_t C = num_components;
+    const int64_t L = num_layers;
+
+    for (int32_t r = 0; r < num_requests; ++r) {
+        const int64_t n = seq_lens[r];
+        for (int64_t l = layer_begin; l < layer_end; ++l) {
+            for (int64_t c = 0; c < C; ++c) {
+                for (int64_t t = 0; t < n; ++t) {
+                    const int64_t sblk = src_bt[src_off[r] + t / src_block];
+                    const int64_t soff = t % src_block;
+                    const int64_t dblk = dst_bt[dst_off[r] + t / dst_block];
+                    const int64_t doff = t % dst_block;
+                    for (int64_t h = 0; h < kv_heads; ++h) {
+                        const int64_t sp = h / src_heads;
+                        const int64_t sh = h % src_heads;
+                        const int64_t dp = h / dst_heads;
+                        const int64_t dh = h % dst_heads;
+                        const uint8_t *src_row = (const uint8_t *)(uintptr_t)
+                            src_base[(sp * L + l) * C + c] + sblk * s_block_stride +
+                            soff * s_token_stride + sh * s_head_stride;
+                        uint8_t *dst_row = (uint8_t *)(uintptr_t)
+                            dst_base[(dp * L + l) * C + c] + dblk * d_block_stride +
+                            doff * d_token_stride + dh * d_head_stride;
+                        const float s = !converting ? 0.0f
+                                        : per_head ? scales[(l * C + c) * kv_heads + h]
+                                                   : scales[l * C + c];
+                        for (int64_t e = 0; e < head_dim; ++e) {
+                            const uint8_t *from = src_row + e * src_es;
+                            uint8_t *to = dst_row + e * dst_es;
+                            if (!converting) {
+                                for (int64_t b = 0; b < elem_bytes; ++b)
+                                    to[b] = from[b];
+                            } else {
+                                convert_element(src_dtype, from, to, s);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    return 0;
+}

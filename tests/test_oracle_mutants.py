@@ -75,6 +75,35 @@ CONVERT_BATTERY = textwrap.dedent("""
     P.test_nan_keeps_its_sign_through_both_conversions(lib)
 """)
 
+LAYOUT_MUTANTS = {
+    "token_and_head_strides_swapped": ("soff * s_token_stride + sh * s_head_stride;",
+                                       "soff * s_head_stride + sh * s_token_stride;"),
+    "base_ignores_shard": ("dst_base[(dp * L + l) * C + c]", "dst_base[(0 * L + l) * C + c]"),
+    "base_layer_component_swapped": ("src_base[(sp * L + l) * C + c]",
+                                     "src_base[(sp * L + c) * C + l]"),
+    "dst_block_stride_dropped": ("dblk * d_block_stride +", "dblk * d_token_stride +"),
+    "generic_quant_scale_not_inverted": ("to[0] = kvo_e4m3_encode(x * inv);",
+                                         "to[0] = kvo_e4m3_encode(x * s);"),
+    "generic_dequant_sign_dropped": ("b = kvo_bf16_encode(kvo_e4m3_decode(from[0]) * s);",
+                                     "b = kvo_bf16_encode(fabsf(kvo_e4m3_decode(from[0])) * s);"),
+}
+
+LAYOUT_BATTERY = textwrap.dedent("""
+    import sys
+    sys.path[:0] = [{root!r}, {tests!r}]
+    import oracle, test_oracle_layout_pins as P
+    lib = oracle.load({lib!r})
+    P.test_standard_views_reduce_to_the_standard_oracle(lib)
+    P.test_head_major_blocks_are_a_transpose(lib)
+    P.test_head_major_prefill_side_too(lib)
+    P.test_separate_buffers_per_layer_and_component(lib)
+    P.test_k_and_v_interleaved_per_block(lib)
+    P.test_staging_buffer_holds_pd_py_gather(lib)
+    P.test_pack_then_unpack_equals_the_direct_relayout(lib)
+    P.test_standard_views_reduce_to_the_converting_oracle(lib, "quant")
+    P.test_standard_views_reduce_to_the_converting_oracle(lib, "dequant")
+""")
+
 BATTERY = textwrap.dedent("""
     import sys
     sys.path[:0] = [{root!r}, {tests!r}]
@@ -111,6 +140,8 @@ def test_unmutated_oracle_passes_the_battery(tmp_path):
     assert res.returncode == 0, res.stderr[-3000:]
     res = _battery(lib, CONVERT_BATTERY)
     assert res.returncode == 0, res.stderr[-3000:]
+    res = _battery(lib, LAYOUT_BATTERY)
+    assert res.returncode == 0, res.stderr[-3000:]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -133,11 +164,12 @@ INDEX_MUTANTS = ["src_shard_by_dst_heads", "dst_local_head_by_src_heads",
 @pytest.mark.parametrize("name", INDEX_MUTANTS)
 def test_conversion_index_mutant_is_caught(tmp_path, name):
     """The same indexing mistakes planted only in the converting loop nest (the
-    second occurrence of each site) must fail the conversion pins."""
+    second occurrence of each site; the layout-generic nest is the third) must fail
+    the conversion pins."""
     old, new = MUTANTS[name]
     with open(SRC) as f:
         text = f.read()
-    assert text.count(old) == 2, f"{name}: expected one site per loop nest"
+    assert text.count(old) >= 2, f"{name}: expected a site in each loop nest"
     first = text.index(old) + len(old)
     lib = _build(tmp_path, name, text[:first] + text[first:].replace(old, new, 1))
     res = _battery(lib, CONVERT_BATTERY)
@@ -149,7 +181,18 @@ def test_conversion_mutant_is_caught(tmp_path, name):
     old, new = CONVERT_MUTANTS[name]
     with open(SRC) as f:
         text = f.read()
-    assert text.count(old) == 1, f"mutation site for {name} not unique in the oracle"
+    assert text.count(old) >= 1, f"mutation site for {name} not in the oracle"
     lib = _build(tmp_path, name, text.replace(old, new))
     res = _battery(lib, CONVERT_BATTERY)
     assert res.returncode != 0, f"mutant {name} survived the pins"
+
+
+@pytest.mark.parametrize("name", sorted(LAYOUT_MUTANTS))
+def test_layout_mutant_is_caught(tmp_path, name):
+    old, new = LAYOUT_MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique in the oracle"
+    lib = _build(tmp_path, name, text.replace(old, new))
+    res = _battery(lib, LAYOUT_BATTERY)
+    assert res.returncode != 0, f"mutant {name} survived the layout pins"
