@@ -146,6 +146,34 @@ kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
 kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
 
 /*
+ * A physical layout of one side (page "PD 分离与 KV 传输", section "布局转换":
+ * attention backends differ in whether K and V are stored together and in
+ * the order of the head and token dimensions). Per (TP shard s, layer l,
+ * component c) the side is a strided view [block][token][local head][dim]:
+ * element [b][t][h][e] of that view is at
+ *   bases[(s * L + l) * C + c] + b * block_stride + t * token_stride
+ *                              + h * head_stride + e * element size,
+ * i.e. head rows (dim) are contiguous and the three strides are shared by all
+ * views of the side. Examples: the standard layout [L][C][N][B][H/T][D];
+ * one K and one V tensor per layer; K and V interleaved per block
+ * ([N][C][B][H][D]); head-major blocks ([N][H][B][D]); a contiguous
+ * [tokens][heads][dim] staging buffer seen as blocks of one token.
+ * Requirements: every base 16-byte aligned and non-NULL; strides >= 0 and
+ * multiples of 16 (a stride whose dimension has extent 1 is ignored). On the
+ * decode side the views must not alias: sorted by stride, each dimension
+ * (of extent > 1) must step over the whole extent of the smaller ones, the
+ * smallest over one head row; no two decode views may share a byte (views
+ * may interleave, as K and V blocks do) and no decode view's span may meet a
+ * prefill view's span (else KVR_ERR_POOL_OVERLAP).
+ */
+typedef struct kvr_layout {
+    const void *const *bases;   /* host [tp * num_layers * num_components] device addresses */
+    int64_t block_stride;       /* bytes between consecutive blocks */
+    int64_t token_stride;       /* bytes between consecutive token slots of a block */
+    int64_t head_stride;        /* bytes between consecutive local heads of a token */
+} kvr_layout;
+
+/*
  * As kv_relayout_desc_bytes() / kv_relayout_plan(), for a relayout that also
  * converts the element type (kvr_convert above; cv == NULL is a plain bit
  * copy). Decode pools then hold dst_dtype elements: their layout is the same
@@ -161,6 +189,21 @@ kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc, const kvr_conver
                                           int64_t *bytes_read, int64_t *bytes_written);
 kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_convert *cv,
                                     kvr_plan **out);
+
+/*
+ * The general form: any layout on either side (kvr_layout above) and an
+ * optional conversion. src_layout / dst_layout NULL: that side is
+ * desc->src_pools / desc->dst_pools in the standard layout; non-NULL: the
+ * layout replaces the pools (desc->src_pools / dst_pools are then ignored and
+ * may be NULL; num_blocks still bounds the block ids). cv NULL: bit copy.
+ * kv_relayout_desc_bytes_ex() validates on the host only (no CUDA call).
+ */
+kvr_status kv_relayout_desc_bytes_ex(const kvr_desc *desc, const kvr_layout *src_layout,
+                                     const kvr_layout *dst_layout, const kvr_convert *cv,
+                                     int64_t *bytes_read, int64_t *bytes_written);
+kvr_status kv_relayout_plan_ex(const kvr_desc *desc, const kvr_layout *src_layout,
+                               const kvr_layout *dst_layout, const kvr_convert *cv,
+                               kvr_plan **out);
 
 /*
  * Move layer `layer` of every request: one kernel launch on `stream`
@@ -199,7 +242,8 @@ const char *kv_relayout_strerror(kvr_status status);
  * stall the other streams. kv_relayout_plan() allocates a small device buffer
  * for the work list; this call allocates nothing: it validates *desc exactly
  * like kv_relayout_plan(), copies the work list (16 bytes per token tile of
- * a request) and the used prefill and decode block ids (4 bytes each) into a
+ * a request, 8 bytes per (shard, layer, component) view of each side, 4 bytes
+ * per used prefill and decode block id) into a
  * fixed device array of KVR_PREALLOC_SCRATCH_BYTES (1 MiB) that the library
  * reserves on every GPU that loads it, until the process exits, and launches
  * the same kernel as kv_relayout_all() on `stream` (asynchronous). The pool

@@ -75,7 +75,7 @@ enum KvrConv : int32_t {
 };
 
 struct KvrGeom {
-    int32_t C, H, Hp, Hd, Bp, Bd;
+    int32_t L, C, H, Hp, Hd, Bp, Bd;
     int32_t src_row_bytes;      // D * source element bytes, a multiple of 16
     int32_t dst_row_bytes;      // D * destination element bytes, a multiple of 16
     int32_t row_chunks;         // units per row
@@ -84,10 +84,9 @@ struct KvrGeom {
     int32_t conv;               // KvrConv
     int32_t per_head;           // conversion scales per (layer, component[, head])
     KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp, div_Bd;
-    int64_t src_blk_bytes;      // Bp * Hp * src_row_bytes
-    int64_t dst_blk_bytes;      // Bd * Hd * dst_row_bytes
-    int64_t src_plane_bytes;    // Np * src_blk_bytes: one (layer, component) plane
-    int64_t dst_plane_bytes;    // Nd * dst_blk_bytes
+    // byte strides of each side's [block][token][head] view (rows are contiguous)
+    int64_t s_block_stride, s_token_stride, s_head_stride;
+    int64_t d_block_stride, d_token_stride, d_head_stride;
 };
 
 // Kernel parameter block (passed by value as a __grid_constant__).
@@ -97,8 +96,8 @@ struct KvrArgs {
     const int32_t *sbt;                 // flat prefill block ids
     const int32_t *dbt;                 // flat decode block ids
     const float *factors;               // conversion: 1/s (quantize) or s (dequantize)
-    const unsigned char *src[KVR_MAX_TP];
-    unsigned char *dst[KVR_MAX_TP];
+    const uint64_t *src_base;           // [Tp][L][C] addresses of the prefill views
+    const uint64_t *dst_base;           // [Td][L][C] addresses of the decode views
     int32_t layer0;                     // first layer of this launch
     int32_t slices;                     // tasks per item
     uint32_t tasks_per_layer;           // n_items * slices
@@ -120,11 +119,11 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
 }
 
-// Row r of an item -> (prefill shard, byte offset of the row),
-// (decode shard, byte offset of the row) and the index of its conversion scale.
+// Row r of an item -> address of its prefill row, address of its decode row,
+// and the index of its conversion scale.
 KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
-                    const int32_t *dbt, uint32_t r, uint32_t *sp, int64_t *soff, uint32_t *dp,
-                    int64_t *doff, uint32_t *fidx) {
+                    const int32_t *dbt, const uint64_t *src_base, const uint64_t *dst_base,
+                    uint32_t r, uint64_t *saddr, uint64_t *daddr, uint32_t *fidx) {
     const uint32_t oc = g.div_H.div(r);
     const uint32_t h = r - oc * (uint32_t)g.H;
     const uint32_t o = g.div_C.div(oc);
@@ -143,12 +142,12 @@ KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const in
     const uint32_t s_loc = h - s_sh * (uint32_t)g.Hp;
     const uint32_t d_sh = g.div_Hd.div(h);
     const uint32_t d_loc = h - d_sh * (uint32_t)g.Hd;
-    const int64_t plane = (int64_t)layer * g.C + c;
-    *sp = s_sh;
-    *dp = d_sh;
-    *soff = plane * g.src_plane_bytes + sb * g.src_blk_bytes +
-            ((int64_t)so * g.Hp + s_loc) * g.src_row_bytes;
-    *doff = plane * g.dst_plane_bytes + db * g.dst_blk_bytes +
-            ((int64_t)dof * g.Hd + d_loc) * g.dst_row_bytes;
-    *fidx = g.per_head ? (uint32_t)plane * (uint32_t)g.H + h : (uint32_t)plane;
+    const uint32_t plane = (uint32_t)layer * (uint32_t)g.C + c;
+    const uint64_t sv = src_base[s_sh * (uint32_t)g.L * (uint32_t)g.C + plane];
+    const uint64_t dv = dst_base[d_sh * (uint32_t)g.L * (uint32_t)g.C + plane];
+    *saddr = sv + (uint64_t)(sb * g.s_block_stride + (int64_t)so * g.s_token_stride +
+                             (int64_t)s_loc * g.s_head_stride);
+    *daddr = dv + (uint64_t)(db * g.d_block_stride + (int64_t)dof * g.d_token_stride +
+                             (int64_t)d_loc * g.d_head_stride);
+    *fidx = g.per_head ? plane * (uint32_t)g.H + h : plane;
 }

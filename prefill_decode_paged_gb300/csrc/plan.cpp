@@ -31,10 +31,6 @@ bool mul_fits(std::initializer_list<int64_t> xs, int64_t *out) {
     return true;
 }
 
-bool overlaps(uintptr_t a, int64_t na, uintptr_t b, int64_t nb) {
-    return a < b + (uint64_t)nb && b < a + (uint64_t)na;
-}
-
 kvr_status check_table(int32_t R, const int32_t *lens, const int64_t *off, const int32_t *bt,
                        int32_t block, int64_t num_blocks) {
     if (R > 0 && (off == nullptr || lens == nullptr)) return KVR_ERR_INVALID_ARG;
@@ -64,10 +60,156 @@ int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count,
     return (int32_t)std::min(want, most);
 }
 
+// One side's views: base address per (shard, layer, component), shared
+// strides, and the bytes one view spans.
+struct Side {
+    std::vector<uint64_t> base;
+    int64_t bs = 0, ts = 0, hs = 0;
+    int64_t span = 0;
+    // a view seen as n_outer intervals of inner bytes, outer_stride apart (the
+    // outer dimension is the one with the largest stride among those of extent > 1)
+    int64_t outer_stride = 0, n_outer = 1, inner = 0;
+};
+
+kvr_status make_side(const kvr_layout *lay, const void *const *pools, int32_t T, int32_t L,
+                     int32_t C, int64_t N, int32_t B, int32_t Hl, int64_t row, Side *out) {
+    const int64_t views = (int64_t)T * L * C;
+    if (views > (int64_t)1 << 26) return KVR_ERR_UNSUPPORTED;
+    out->base.assign((size_t)views, 0);
+    int64_t plane = 0;
+    if (lay == nullptr) {
+        if (pools == nullptr) return KVR_ERR_INVALID_ARG;
+        for (int32_t s = 0; s < T; ++s)
+            if (pools[s] == nullptr) return KVR_ERR_INVALID_ARG;
+        for (int32_t s = 0; s < T; ++s)
+            if ((uintptr_t)pools[s] % 16 != 0) return KVR_ERR_ALIGNMENT;
+        int64_t bs = 0, total = 0;
+        if (!mul_fits({(int64_t)B, Hl, row}, &bs) || !mul_fits({N, bs}, &plane) ||
+            !mul_fits({plane, (int64_t)L, C}, &total))
+            return KVR_ERR_UNSUPPORTED;
+        out->bs = bs;
+        out->ts = (int64_t)Hl * row;
+        out->hs = row;
+        for (int32_t s = 0; s < T; ++s)
+            for (int64_t v = 0; v < (int64_t)L * C; ++v)
+                out->base[s * (int64_t)L * C + v] = (uint64_t)(uintptr_t)pools[s] + v * plane;
+    } else {
+        if (lay->bases == nullptr) return KVR_ERR_INVALID_ARG;
+        if (lay->block_stride < 0 || lay->token_stride < 0 || lay->head_stride < 0)
+            return KVR_ERR_INVALID_ARG;
+        for (int64_t v = 0; v < views; ++v)
+            if (lay->bases[v] == nullptr) return KVR_ERR_INVALID_ARG;
+        for (int64_t v = 0; v < views; ++v)
+            if ((uintptr_t)lay->bases[v] % 16 != 0) return KVR_ERR_ALIGNMENT;
+        out->bs = lay->block_stride;
+        out->ts = lay->token_stride;
+        out->hs = lay->head_stride;
+        for (int64_t v = 0; v < views; ++v) out->base[v] = (uint64_t)(uintptr_t)lay->bases[v];
+    }
+    // a stride counts only where its dimension has more than one position
+    const int64_t bs = N > 1 ? out->bs : 0, ts = B > 1 ? out->ts : 0, hs = Hl > 1 ? out->hs : 0;
+    if (bs % 16 != 0 || ts % 16 != 0 || hs % 16 != 0) return KVR_ERR_ALIGNMENT;
+    int64_t a = 0, b = 0, c = 0;
+    if (!mul_fits({N - 1, bs}, &a) || !mul_fits({(int64_t)B - 1, ts}, &b) ||
+        !mul_fits({(int64_t)Hl - 1, hs}, &c))
+        return KVR_ERR_UNSUPPORTED;
+    const __int128 span = (__int128)a + b + c + row;
+    if (span > (__int128)INT64_MAX) return KVR_ERR_UNSUPPORTED;
+    out->span = lay == nullptr ? plane : (int64_t)span;
+    std::vector<std::pair<int64_t, int64_t>> dims;   // (stride, extent) of extent > 1
+    if (N > 1) dims.push_back({bs, N});
+    if (B > 1) dims.push_back({ts, B});
+    if (Hl > 1) dims.push_back({hs, Hl});
+    std::sort(dims.begin(), dims.end());
+    out->inner = row;
+    for (size_t k = 0; k + 1 < dims.size(); ++k) out->inner += (dims[k].second - 1) * dims[k].first;
+    if (!dims.empty()) {
+        out->outer_stride = dims.back().first;
+        out->n_outer = dims.back().second;
+    }
+    for (uint64_t v : out->base)
+        if (v > UINT64_MAX - (uint64_t)out->span) return KVR_ERR_UNSUPPORTED;
+    return KVR_OK;
+}
+
+// Decode views must not alias: with the dimensions (of extent > 1) sorted by
+// stride, each must step over everything the smaller ones span.
+bool views_are_injective(int64_t N, int64_t bs, int64_t B, int64_t ts, int64_t Hl, int64_t hs,
+                         int64_t row) {
+    std::vector<std::pair<int64_t, int64_t>> dims;   // (stride, extent)
+    if (N > 1) dims.push_back({bs, N});
+    if (B > 1) dims.push_back({ts, B});
+    if (Hl > 1) dims.push_back({hs, Hl});
+    std::sort(dims.begin(), dims.end());
+    __int128 inner = row;
+    for (const auto &dm : dims) {
+        if ((__int128)dm.first < inner) return false;
+        inner += (__int128)(dm.second - 1) * dm.first;
+    }
+    return true;
+}
+
+// Do two views of one side (same strides, bases a and b) share a byte? Each
+// is n_outer intervals of `inner` bytes, outer_stride apart; they meet iff a
+// shift delta + k * outer_stride (|k| < n_outer) comes within `inner` of 0.
+bool views_meet(uint64_t a, uint64_t b, const Side &sd) {
+    const uint64_t delta = a > b ? a - b : b - a;
+    const uint64_t inner = (uint64_t)sd.inner;
+    if (sd.n_outer <= 1 || sd.outer_stride == 0) return delta < inner;
+    const uint64_t so = (uint64_t)sd.outer_stride;
+    const uint64_t q = delta / so, r = delta % so;
+    if (q + 1 <= (uint64_t)sd.n_outer && r < inner) return true;
+    if (q + 2 <= (uint64_t)sd.n_outer && so - r < inner) return true;
+    return false;
+}
+
+// A decode view may share no byte with another decode view (exact test for
+// views of equal strides) nor come near any prefill view (their spans may not
+// intersect). Also returns each side's spans merged (for the device-access
+// checks).
+kvr_status check_regions(const Side &src, const Side &dst, std::vector<uint64_t> *src_merged,
+                         std::vector<uint64_t> *dst_merged) {
+    std::vector<uint64_t> db(dst.base);
+    std::sort(db.begin(), db.end());
+    for (size_t i = 0; i < db.size(); ++i)
+        for (size_t j = i + 1; j < db.size() && db[j] < db[i] + (uint64_t)dst.span; ++j)
+            if (views_meet(db[i], db[j], dst)) return KVR_ERR_POOL_OVERLAP;
+
+    struct Reg {
+        uint64_t lo, hi;
+        bool dst;
+    };
+    std::vector<Reg> regs;
+    regs.reserve(src.base.size() + dst.base.size());
+    for (uint64_t b : src.base) regs.push_back({b, b + (uint64_t)src.span, false});
+    for (uint64_t b : dst.base) regs.push_back({b, b + (uint64_t)dst.span, true});
+    std::sort(regs.begin(), regs.end(), [](const Reg &x, const Reg &y) { return x.lo < y.lo; });
+    uint64_t end_src = 0, end_dst = 0;
+    for (const Reg &r : regs) {
+        if (r.dst ? r.lo < end_src : r.lo < end_dst) return KVR_ERR_POOL_OVERLAP;
+        (r.dst ? end_dst : end_src) = std::max(r.dst ? end_dst : end_src, r.hi);
+    }
+    for (int side = 0; side < 2; ++side) {
+        std::vector<uint64_t> &m = side ? *dst_merged : *src_merged;
+        m.clear();
+        for (const Reg &r : regs) {
+            if (r.dst != (side == 1)) continue;
+            if (!m.empty() && r.lo <= m.back()) {
+                m.back() = std::max(m.back(), r.hi);
+            } else {
+                m.push_back(r.lo);
+                m.push_back(r.hi);
+            }
+        }
+    }
+    return KVR_OK;
+}
+
 }  // namespace
 
-kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_count,
-                               KvrHostPlan *hp, int64_t *bytes_read_out,
+kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
+                               const kvr_layout *dst_layout, const kvr_convert *cv,
+                               int sm_count, KvrHostPlan *hp, int64_t *bytes_read_out,
                                int64_t *bytes_written_out) {
     if (d == nullptr) return KVR_ERR_INVALID_ARG;
     const int32_t L = d->num_layers, C = d->num_components, H = d->kv_heads, D = d->head_dim;
@@ -111,29 +253,26 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_
     const int64_t row_units = src_row / unit_src;
     const int32_t Hp = H / Tp, Hd = H / Td;
 
-    // pool extents
-    int64_t src_pool = 0, dst_pool = 0, src_blk = 0, dst_blk = 0;
-    if (!mul_fits({(int64_t)L, C, Np, Bp, Hp, src_row}, &src_pool) ||
-        !mul_fits({(int64_t)L, C, Nd, Bd, Hd, dst_row}, &dst_pool))
-        return KVR_ERR_UNSUPPORTED;
-    mul_fits({(int64_t)Bp, Hp, src_row}, &src_blk);
-    mul_fits({(int64_t)Bd, Hd, dst_row}, &dst_blk);
     // one item's units must stay below 2^31 (32-bit chunk indices)
     int64_t item_chunks = 0;
     if (!mul_fits({(int64_t)Bd, C, H, row_units}, &item_chunks) || item_chunks > INT32_MAX)
         return KVR_ERR_UNSUPPORTED;
 
-    if (d->src_pools == nullptr || d->dst_pools == nullptr) return KVR_ERR_INVALID_ARG;
-    for (int32_t s = 0; s < Tp; ++s)
-        if (d->src_pools[s] == nullptr) return KVR_ERR_INVALID_ARG;
-    for (int32_t s = 0; s < Td; ++s)
-        if (d->dst_pools[s] == nullptr) return KVR_ERR_INVALID_ARG;
-    for (int32_t s = 0; s < Tp; ++s)
-        if ((uintptr_t)d->src_pools[s] % 16 != 0) return KVR_ERR_ALIGNMENT;
-    for (int32_t s = 0; s < Td; ++s)
-        if ((uintptr_t)d->dst_pools[s] % 16 != 0) return KVR_ERR_ALIGNMENT;
+    // the views of both sides
+    Side src, dst;
+    kvr_status st;
+    try {
+        st = make_side(src_layout, d->src_pools, Tp, L, C, Np, Bp, Hp, src_row, &src);
+        if (st != KVR_OK) return st;
+        st = make_side(dst_layout, d->dst_pools, Td, L, C, Nd, Bd, Hd, dst_row, &dst);
+        if (st != KVR_OK) return st;
+    } catch (const std::bad_alloc &) {
+        return KVR_ERR_NOMEM;
+    }
+    if (!views_are_injective(Nd, dst.bs, Bd, dst.ts, Hd, dst.hs, dst_row))
+        return KVR_ERR_POOL_OVERLAP;
 
-    kvr_status st = check_table(R, d->seq_lens, d->src_bt_offsets, d->src_bt, Bp, Np);
+    st = check_table(R, d->seq_lens, d->src_bt_offsets, d->src_bt, Bp, Np);
     if (st != KVR_OK) return st;
     st = check_table(R, d->seq_lens, d->dst_bt_offsets, d->dst_bt, Bd, Nd);
     if (st != KVR_OK) return st;
@@ -154,16 +293,14 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_
     }
     if (std::adjacent_find(used.begin(), used.end()) != used.end()) return KVR_ERR_DST_ALIAS;
 
-    // decode pools must not overlap each other or any prefill pool
-    for (int32_t a = 0; a < Td; ++a) {
-        const uintptr_t pa = (uintptr_t)d->dst_pools[a];
-        for (int32_t b = a + 1; b < Td; ++b)
-            if (overlaps(pa, dst_pool, (uintptr_t)d->dst_pools[b], dst_pool))
-                return KVR_ERR_POOL_OVERLAP;
-        for (int32_t b = 0; b < Tp; ++b)
-            if (overlaps(pa, dst_pool, (uintptr_t)d->src_pools[b], src_pool))
-                return KVR_ERR_POOL_OVERLAP;
+    // decode views must not overlap each other or any prefill view
+    std::vector<uint64_t> src_regions, dst_regions;
+    try {
+        st = check_regions(src, dst, &src_regions, &dst_regions);
+    } catch (const std::bad_alloc &) {
+        return KVR_ERR_NOMEM;
     }
+    if (st != KVR_OK) return st;
 
     int64_t bytes_read = 0, bytes_written = 0;
     if (!mul_fits({tokens, (int64_t)L, C, H, src_row}, &bytes_read) ||
@@ -190,7 +327,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_
         return KVR_ERR_UNSUPPORTED;
 
     KvrGeom &g = hp->g;
-    g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
+    g.L = L; g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
     g.src_row_bytes = (int32_t)src_row;
     g.dst_row_bytes = (int32_t)dst_row;
     g.row_chunks = (int32_t)row_units;
@@ -205,16 +342,20 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_
     g.div_Hd = kvr_make_div((uint32_t)Hd);
     g.div_Bp = kvr_make_div((uint32_t)Bp);
     g.div_Bd = kvr_make_div((uint32_t)Bd);
-    g.src_blk_bytes = src_blk;
-    g.dst_blk_bytes = dst_blk;
-    g.src_plane_bytes = src_pool / ((int64_t)L * C);
-    g.dst_plane_bytes = dst_pool / ((int64_t)L * C);
+    g.s_block_stride = src.bs;
+    g.s_token_stride = src.ts;
+    g.s_head_stride = src.hs;
+    g.d_block_stride = dst.bs;
+    g.d_token_stride = dst.ts;
+    g.d_head_stride = dst.hs;
     hp->num_layers = L;
     hp->src_tp = Tp;
     hp->dst_tp = Td;
     hp->tile = (int32_t)tile;
-    for (int32_t s = 0; s < Tp; ++s) hp->src[s] = d->src_pools[s];
-    for (int32_t s = 0; s < Td; ++s) hp->dst[s] = d->dst_pools[s];
+    hp->src_base.swap(src.base);
+    hp->dst_base.swap(dst.base);
+    hp->src_regions.swap(src_regions);
+    hp->dst_regions.swap(dst_regions);
     hp->bytes_read = bytes_read;
     hp->bytes_written = bytes_written;
 
@@ -269,8 +410,9 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_
 }
 
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,
-                        const int32_t *dev_dbt, const float *dev_factors, int32_t layer0,
-                        int32_t slices) {
+                        const int32_t *dev_dbt, const float *dev_factors,
+                        const uint64_t *dev_src_base, const uint64_t *dev_dst_base,
+                        int32_t layer0, int32_t slices) {
     KvrArgs a;
     memset(&a, 0, sizeof(a));
     a.g = hp.g;
@@ -278,8 +420,8 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const i
     a.sbt = dev_sbt;
     a.dbt = dev_dbt;
     a.factors = dev_factors;
-    for (int32_t s = 0; s < hp.src_tp; ++s) a.src[s] = (const unsigned char *)hp.src[s];
-    for (int32_t s = 0; s < hp.dst_tp; ++s) a.dst[s] = (unsigned char *)hp.dst[s];
+    a.src_base = dev_src_base;
+    a.dst_base = dev_dst_base;
     a.layer0 = layer0;
     a.slices = slices;
     a.tasks_per_layer = (uint32_t)(hp.items.size() * (size_t)slices);
@@ -288,14 +430,15 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const i
     return a;
 }
 
-extern "C" kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc,
-                                                     const kvr_convert *cv,
-                                                     int64_t *bytes_read,
-                                                     int64_t *bytes_written) {
+extern "C" kvr_status kv_relayout_desc_bytes_ex(const kvr_desc *desc,
+                                                const kvr_layout *src_layout,
+                                                const kvr_layout *dst_layout,
+                                                const kvr_convert *cv, int64_t *bytes_read,
+                                                int64_t *bytes_written) {
     int64_t r = 0, w = 0;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, cv, 0, nullptr, &r, &w);
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, 0, nullptr, &r, &w);
     } catch (...) {
         return KVR_ERR_NOMEM;
     }
@@ -305,9 +448,17 @@ extern "C" kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc,
     return KVR_OK;
 }
 
+extern "C" kvr_status kv_relayout_desc_convert_bytes(const kvr_desc *desc,
+                                                     const kvr_convert *cv,
+                                                     int64_t *bytes_read,
+                                                     int64_t *bytes_written) {
+    return kv_relayout_desc_bytes_ex(desc, nullptr, nullptr, cv, bytes_read, bytes_written);
+}
+
 extern "C" kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
                                              int64_t *bytes_written) {
-    return kv_relayout_desc_convert_bytes(desc, nullptr, bytes_read, bytes_written);
+    return kv_relayout_desc_bytes_ex(desc, nullptr, nullptr, nullptr, bytes_read,
+                                     bytes_written);
 }
 
 extern "C" const char *kv_relayout_strerror(kvr_status s) {

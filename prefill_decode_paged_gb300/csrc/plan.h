@@ -44,8 +44,10 @@ struct KvrHostPlan {
     int32_t num_layers = 0;
     int32_t src_tp = 0, dst_tp = 0;
     int32_t tile = 0;                  // tokens per work item (a multiple of Bd)
-    const void *src[KVR_MAX_TP] = {};
-    void *dst[KVR_MAX_TP] = {};
+    std::vector<uint64_t> src_base;    // [Tp][L][C] addresses of the prefill views
+    std::vector<uint64_t> dst_base;    // [Td][L][C] addresses of the decode views
+    std::vector<uint64_t> src_regions; // merged [start, end) byte ranges the prefill views span
+    std::vector<uint64_t> dst_regions; // the same for the decode side
     std::vector<KvrItem> items;        // (request, token tile) work items
     std::vector<int32_t> sbt;          // used prefill block ids, request after request
     std::vector<int32_t> dbt;          // used decode block ids, request after request
@@ -56,13 +58,17 @@ struct KvrHostPlan {
     int32_t slices_layer = 1;          // slices per item, per-layer launch
 };
 
-// Validate `d` (and the conversion `cv`, NULL for a bit copy); when `hp` is
-// non-NULL also build the host plan for a device with `sm_count` SMs. Never
-// touches device memory. Either byte output may be NULL.
-kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_convert *cv, int sm_count,
-                               KvrHostPlan *hp, int64_t *bytes_read, int64_t *bytes_written);
+// Validate `d` with its layouts (NULL: the standard layout of d's pools) and
+// the conversion `cv` (NULL: bit copy); when `hp` is non-NULL also build the
+// host plan for a device with `sm_count` SMs. Never touches device memory.
+// Either byte output may be NULL.
+kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
+                               const kvr_layout *dst_layout, const kvr_convert *cv,
+                               int sm_count, KvrHostPlan *hp, int64_t *bytes_read,
+                               int64_t *bytes_written);
 
 // Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,
                         const int32_t *dev_sbt, const int32_t *dev_dbt,
-                        const float *dev_factors, int32_t layer0, int32_t slices);
+                        const float *dev_factors, const uint64_t *dev_src_base,
+                        const uint64_t *dev_dst_base, int32_t layer0, int32_t slices);

@@ -26,8 +26,10 @@
 
 struct kvr_plan {
     KvrHostPlan host;
-    void *dev_meta = nullptr;       // items, prefill and decode block ids, factors
+    void *dev_meta = nullptr;       // items, view bases, block ids, factors
     const KvrItem *dev_items = nullptr;
+    const uint64_t *dev_src_base = nullptr;
+    const uint64_t *dev_dst_base = nullptr;
     const int32_t *dev_sbt = nullptr;
     const int32_t *dev_dbt = nullptr;
     const float *dev_factors = nullptr;
@@ -161,11 +163,10 @@ __global__ void __launch_bounds__(KVR_THREADS)
         const uint32_t w1 = min(w0 + (uint32_t)KVR_ROW_WINDOW, r_end);
         // 1. one thread per row: the row's two addresses (block tables read here)
         for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
-            uint32_t sp, dp, fidx;
-            int64_t soff, doff;
-            kvr_row(a.g, layer, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff, &fidx);
-            rows[r - w0] = make_ulonglong2((unsigned long long)(a.src[sp] + soff),
-                                           (unsigned long long)(a.dst[dp] + doff));
+            uint32_t fidx;
+            uint64_t sa, da;
+            kvr_row(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da, &fidx);
+            rows[r - w0] = make_ulonglong2(sa, da);
             if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
         }
         __syncthreads();
@@ -234,7 +235,8 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
     const KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt,
-                                      p->dev_factors, layer0, slices);
+                                      p->dev_factors, p->dev_src_base, p->dev_dst_base,
+                                      layer0, slices);
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
 
@@ -283,21 +285,60 @@ kvr_status check_pool(const void *pool, int64_t bytes, int dev) {
 }
 
 kvr_status check_pools(const KvrHostPlan &hp, int dev) {
-    const int64_t layers_comps = (int64_t)hp.num_layers * hp.g.C;
-    for (int32_t s = 0; s < hp.src_tp; ++s) {
-        const kvr_status st = check_pool(hp.src[s], hp.g.src_plane_bytes * layers_comps, dev);
-        if (st != KVR_OK) return st;
-    }
-    for (int32_t s = 0; s < hp.dst_tp; ++s) {
-        const kvr_status st = check_pool(hp.dst[s], hp.g.dst_plane_bytes * layers_comps, dev);
-        if (st != KVR_OK) return st;
+    for (const std::vector<uint64_t> *regs : {&hp.src_regions, &hp.dst_regions}) {
+        for (size_t k = 0; k + 1 < regs->size(); k += 2) {
+            const kvr_status st = check_pool((const void *)(uintptr_t)(*regs)[k],
+                                             (int64_t)((*regs)[k + 1] - (*regs)[k]), dev);
+            if (st != KVR_OK) return st;
+        }
     }
     return KVR_OK;
 }
 
+// Where a host plan's tables go in one device buffer: items (16-byte aligned
+// start), view bases, block ids, factors, back to back.
+struct DevTables {
+    const KvrItem *items;
+    const uint64_t *src_base, *dst_base;
+    const int32_t *sbt, *dbt;
+    const float *factors;
+};
+
+struct Piece {
+    const void *host;
+    size_t bytes;
+};
+
+size_t tables_bytes(const KvrHostPlan &hp) {
+    return hp.items.size() * sizeof(KvrItem) +
+           (hp.src_base.size() + hp.dst_base.size()) * sizeof(uint64_t) +
+           (hp.sbt.size() + hp.dbt.size()) * sizeof(int32_t) + hp.factors.size() * sizeof(float);
+}
+
+DevTables place_tables(const KvrHostPlan &hp, unsigned char *base, Piece pieces[6]) {
+    size_t off = 0;
+    auto put = [&](int k, const void *h, size_t bytes) {
+        pieces[k] = {h, bytes};
+        unsigned char *p = base + off;
+        off += bytes;
+        return p;
+    };
+    DevTables t;
+    t.items = (const KvrItem *)put(0, hp.items.data(), hp.items.size() * sizeof(KvrItem));
+    t.src_base = (const uint64_t *)put(1, hp.src_base.data(), hp.src_base.size() * 8);
+    t.dst_base = (const uint64_t *)put(2, hp.dst_base.data(), hp.dst_base.size() * 8);
+    t.sbt = (const int32_t *)put(3, hp.sbt.data(), hp.sbt.size() * 4);
+    t.dbt = (const int32_t *)put(4, hp.dbt.data(), hp.dbt.size() * 4);
+    const float *f = (const float *)put(5, hp.factors.data(), hp.factors.size() * 4);
+    t.factors = hp.factors.empty() ? nullptr : f;
+    return t;
+}
+
 }  // namespace
 
-static kvr_status make_plan(const kvr_desc *desc, const kvr_convert *cv, kvr_plan **out) {
+static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
+                            const kvr_layout *dst_layout, const kvr_convert *cv,
+                            kvr_plan **out) {
     if (out == nullptr) return KVR_ERR_INVALID_ARG;
     *out = nullptr;
     int dev = 0, sms = 0;
@@ -309,7 +350,8 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_convert *cv, kvr_pla
     if (p == nullptr) return KVR_ERR_NOMEM;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, cv, sms, &p->host, nullptr, nullptr);
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, &p->host, nullptr,
+                                 nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
@@ -319,43 +361,43 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_convert *cv, kvr_pla
         return st;
     }
     p->device = dev;
-    const size_t items_bytes = p->host.items.size() * sizeof(KvrItem);
-    const size_t sbt_bytes = p->host.sbt.size() * sizeof(int32_t);
-    const size_t dbt_bytes = p->host.dbt.size() * sizeof(int32_t);
-    const size_t fac_bytes = p->host.factors.size() * sizeof(float);
-    if (items_bytes > 0) {
-        if (cudaMalloc(&p->dev_meta, items_bytes + sbt_bytes + dbt_bytes + fac_bytes) !=
-            cudaSuccess) {
+    if (!p->host.items.empty()) {
+        if (cudaMalloc(&p->dev_meta, tables_bytes(p->host)) != cudaSuccess) {
             cudaGetLastError();
             delete p;
             return KVR_ERR_NOMEM;
         }
-        unsigned char *base = (unsigned char *)p->dev_meta;
-        if (cudaMemcpy(base, p->host.items.data(), items_bytes, cudaMemcpyHostToDevice) !=
-                cudaSuccess ||
-            cudaMemcpy(base + items_bytes, p->host.sbt.data(), sbt_bytes,
-                       cudaMemcpyHostToDevice) != cudaSuccess ||
-            cudaMemcpy(base + items_bytes + sbt_bytes, p->host.dbt.data(), dbt_bytes,
-                       cudaMemcpyHostToDevice) != cudaSuccess ||
-            (fac_bytes > 0 &&
-             cudaMemcpy(base + items_bytes + sbt_bytes + dbt_bytes, p->host.factors.data(),
-                        fac_bytes, cudaMemcpyHostToDevice) != cudaSuccess)) {
-            cudaFree(p->dev_meta);
-            delete p;
-            return KVR_ERR_CUDA;
+        Piece pieces[6];
+        const DevTables t = place_tables(p->host, (unsigned char *)p->dev_meta, pieces);
+        unsigned char *to = (unsigned char *)p->dev_meta;
+        for (const Piece &pc : pieces) {
+            if (pc.bytes > 0 &&
+                cudaMemcpy(to, pc.host, pc.bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+                cudaFree(p->dev_meta);
+                delete p;
+                return KVR_ERR_CUDA;
+            }
+            to += pc.bytes;
         }
-        p->dev_items = (const KvrItem *)base;
-        p->dev_sbt = (const int32_t *)(base + items_bytes);
-        p->dev_dbt = (const int32_t *)(base + items_bytes + sbt_bytes);
-        if (fac_bytes > 0)
-            p->dev_factors = (const float *)(base + items_bytes + sbt_bytes + dbt_bytes);
+        p->dev_items = t.items;
+        p->dev_src_base = t.src_base;
+        p->dev_dst_base = t.dst_base;
+        p->dev_sbt = t.sbt;
+        p->dev_dbt = t.dbt;
+        p->dev_factors = t.factors;
     }
     *out = p;
     return KVR_OK;
 }
 
 extern "C" kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out) {
-    return make_plan(desc, nullptr, out);
+    return make_plan(desc, nullptr, nullptr, nullptr, out);
+}
+
+extern "C" kvr_status kv_relayout_plan_ex(const kvr_desc *desc, const kvr_layout *src_layout,
+                                          const kvr_layout *dst_layout, const kvr_convert *cv,
+                                          kvr_plan **out) {
+    return make_plan(desc, src_layout, dst_layout, cv, out);
 }
 
 extern "C" kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_convert *cv,
@@ -364,7 +406,7 @@ extern "C" kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_c
         if (out != nullptr) *out = nullptr;
         return KVR_ERR_INVALID_ARG;
     }
-    return make_plan(desc, cv, out);
+    return make_plan(desc, nullptr, nullptr, cv, out);
 }
 
 extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
@@ -451,34 +493,31 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
 
     KvrHostPlan hp;
     try {
-        st = kvr_build_host_plan(desc, nullptr, sc.sms, &hp, nullptr, nullptr);
+        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, &hp, nullptr,
+                                 nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
     if (st == KVR_OK) st = check_pools(hp, dev);
     if (st != KVR_OK) return st;
-    const size_t items_bytes = hp.items.size() * sizeof(KvrItem);
-    const size_t sbt_bytes = hp.sbt.size() * sizeof(int32_t);
-    const size_t dbt_bytes = hp.dbt.size() * sizeof(int32_t);
-    if (items_bytes + sbt_bytes + dbt_bytes > KVR_PREALLOC_SCRATCH_BYTES)
-        return KVR_ERR_SCRATCH_LIMIT;
-    if (items_bytes == 0) return KVR_OK;
+    if (tables_bytes(hp) > KVR_PREALLOC_SCRATCH_BYTES) return KVR_ERR_SCRATCH_LIMIT;
+    if (hp.items.empty()) return KVR_OK;
 
-    // The whole array is overwritten up to what this call reads, so nothing
-    // needs clearing; the copies are ordered before the launch on `stream`.
+    // The array is overwritten up to what this call reads, so nothing needs
+    // clearing; the copies are ordered before the launch on `stream`.
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(sc.addr, hp.items.data(), items_bytes, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(sc.addr + items_bytes, hp.sbt.data(), sbt_bytes,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(sc.addr + items_bytes + sbt_bytes, hp.dbt.data(), dbt_bytes,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return KVR_ERR_CUDA;
+    Piece pieces[6];
+    const DevTables t = place_tables(hp, sc.addr, pieces);
+    unsigned char *to = sc.addr;
+    for (const Piece &pc : pieces) {
+        if (pc.bytes > 0 &&
+            cudaMemcpyAsync(to, pc.host, pc.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return KVR_ERR_CUDA;
+        to += pc.bytes;
+    }
 
-    const KvrArgs a = kvr_launch_args(hp, (const KvrItem *)sc.addr,
-                                      (const int32_t *)(sc.addr + items_bytes),
-                                      (const int32_t *)(sc.addr + items_bytes + sbt_bytes),
-                                      nullptr, 0, hp.slices_all);
+    const KvrArgs a = kvr_launch_args(hp, t.items, t.sbt, t.dbt, nullptr, t.src_base,
+                                      t.dst_base, 0, hp.slices_all);
     const uint64_t grid = (uint64_t)hp.num_layers * a.tasks_per_layer;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);

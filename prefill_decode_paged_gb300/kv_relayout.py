@@ -27,7 +27,7 @@ PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_all", "kv_relayout_plan_bytes", "kv_relayout_plan_destroy",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
-           "kv_relayout_plan_convert")
+           "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 
@@ -42,6 +42,11 @@ class KVRelayoutError(RuntimeError):
 class KvrConvert(ctypes.Structure):
     _fields_ = [("src_dtype", ctypes.c_int32), ("dst_dtype", ctypes.c_int32),
                 ("per_head", ctypes.c_int32), ("scales", ctypes.c_void_p)]
+
+
+class KvrLayout(ctypes.Structure):
+    _fields_ = [("bases", ctypes.c_void_p), ("block_stride", ctypes.c_int64),
+                ("token_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64)]
 
 
 class KvrDesc(ctypes.Structure):
@@ -92,6 +97,10 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_desc_convert_bytes.argtypes = [p, p, p, p]
         lib.kv_relayout_plan_convert.restype = i32
         lib.kv_relayout_plan_convert.argtypes = [p, p, p]
+        lib.kv_relayout_desc_bytes_ex.restype = i32
+        lib.kv_relayout_desc_bytes_ex.argtypes = [p, p, p, p, p, p]
+        lib.kv_relayout_plan_ex.restype = i32
+        lib.kv_relayout_plan_ex.argtypes = [p, p, p, p, p]
         _lib = lib
     return _lib
 
@@ -154,11 +163,62 @@ class _Convert:
         self.conv = c
 
 
-def desc_bytes(src_pools, dst_pools, convert=None, **geometry):
+class _Layout:
+    """Keeps a C layout descriptor and its base-address array alive."""
+
+    def __init__(self, bases, block_stride, token_stride, head_stride):
+        self.bases = (ctypes.c_void_p * max(1, len(bases)))(*[_ptr(x) for x in bases])
+        lay = KvrLayout()
+        lay.bases = ctypes.cast(self.bases, ctypes.c_void_p)
+        lay.block_stride, lay.token_stride, lay.head_stride = (int(block_stride),
+                                                              int(token_stride),
+                                                              int(head_stride))
+        self.layout = lay
+
+
+def layout_of_views(views):
+    """A side's layout from its views: ``views[shard][layer][component]`` are tensors
+    (torch or numpy) shaped [block][token][head][dim] with a contiguous last
+    dimension and the same strides. Returns the dict RelayoutPlan takes."""
+    bases, strides = [], None
+    for per_shard in views:
+        for per_layer in per_shard:
+            for v in per_layer:
+                if hasattr(v, "data_ptr"):                       # torch
+                    es = v.element_size()
+                    st = tuple(x * es for x in v.stride())
+                    bases.append(int(v.data_ptr()))
+                else:                                            # numpy
+                    es = v.itemsize
+                    st = tuple(v.strides)
+                    bases.append(int(v.ctypes.data))
+                if len(st) != 4 or st[3] != es:
+                    raise ValueError("views must be [block][token][head][dim], dim contiguous")
+                if strides is None:
+                    strides = st[:3]
+                elif st[:3] != strides:
+                    raise ValueError("all views of a side must share their strides")
+    return dict(bases=bases, block_stride=strides[0], token_stride=strides[1],
+                head_stride=strides[2])
+
+
+def _layout_arg(layout):
+    return None if layout is None else _Layout(**layout)
+
+
+def desc_bytes(src_pools, dst_pools, convert=None, src_layout=None, dst_layout=None,
+               **geometry):
     """Validate a descriptor on the host; return (bytes_read, bytes_written)."""
     d = _Desc(src_pools, dst_pools, **geometry)
     r, w = ctypes.c_int64(), ctypes.c_int64()
-    if convert is None:
+    if src_layout is not None or dst_layout is not None:
+        sl, dl = _layout_arg(src_layout), _layout_arg(dst_layout)
+        cv = _Convert(**convert) if convert is not None else None
+        st = library().kv_relayout_desc_bytes_ex(
+            ctypes.byref(d.desc), ctypes.byref(sl.layout) if sl else None,
+            ctypes.byref(dl.layout) if dl else None, ctypes.byref(cv.conv) if cv else None,
+            ctypes.byref(r), ctypes.byref(w))
+    elif convert is None:
         st = library().kv_relayout_desc_bytes(ctypes.byref(d.desc), ctypes.byref(r),
                                               ctypes.byref(w))
     else:
@@ -206,14 +266,27 @@ class RelayoutPlan:
     ``src_off``/``dst_off`` (R + 1 offsets) into ``src_bt``/``dst_bt``.
     ``convert``: None (bit copy) or dict(src_dtype=..., dst_dtype=..., scales=...,
     per_head=False) for a BF16 <-> FP8 E4M3 relayout (``kv_relayout_plan_convert``).
+    ``src_layout`` / ``dst_layout``: None (the pools in the standard layout) or a
+    dict(bases=..., block_stride=..., token_stride=..., head_stride=...) as
+    :func:`layout_of_views` builds (``kv_relayout_plan_ex``); the side's pools are
+    then not used and may be None.
     """
 
-    def __init__(self, src_pools, dst_pools, convert=None, **geometry):
+    def __init__(self, src_pools, dst_pools, convert=None, src_layout=None, dst_layout=None,
+                 **geometry):
         self._h = None
         self._d = _Desc(src_pools, dst_pools, **geometry)
         self.num_layers = geometry["num_layers"]
         h = ctypes.c_void_p()
-        if convert is None:
+        if src_layout is not None or dst_layout is not None:
+            self._sl, self._dl = _layout_arg(src_layout), _layout_arg(dst_layout)
+            self._cv = _Convert(**convert) if convert is not None else None
+            st = library().kv_relayout_plan_ex(
+                ctypes.byref(self._d.desc),
+                ctypes.byref(self._sl.layout) if self._sl else None,
+                ctypes.byref(self._dl.layout) if self._dl else None,
+                ctypes.byref(self._cv.conv) if self._cv else None, ctypes.byref(h))
+        elif convert is None:
             st = library().kv_relayout_plan(ctypes.byref(self._d.desc), ctypes.byref(h))
         else:
             self._cv = _Convert(**convert)
@@ -261,3 +334,45 @@ class RelayoutPlan:
             self.close()
         except Exception:
             pass
+
+
+# -- staging buffer: pd.py's gathered [seq, kv_heads, head_dim] per layer ---------------
+
+def staging_geometry(geometry, side):
+    """Geometry with one side replaced by a staging buffer [L][C][sum n][H][D]: a single
+    shard of one-token blocks, request r's tokens at offset sum(n[:r])."""
+    lens = np.asarray(geometry["seq_lens"], dtype=np.int64)
+    total = int(lens.sum())
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ids = np.arange(total, dtype=np.int32)
+    g = dict(geometry)
+    g.update({f"{side}_tp": 1, f"{side}_block": 1, f"{side}_num_blocks": max(total, 1),
+              f"{side}_off": off, f"{side}_bt": ids})
+    return g
+
+
+def staging_layout(buf, num_layers, num_components):
+    """Layout of a staging tensor shaped [L][C][tokens][H][D] (one shard)."""
+    L, C, T, H, D = buf.shape
+    assert (L, C) == (num_layers, num_components)
+    return layout_of_views([[[buf[l, c].reshape(T, 1, H, D) for c in range(C)]
+                             for l in range(L)]])
+
+
+def pack_plan(src_pools, staging, convert=None, **geometry):
+    """Plan that gathers every request's KV out of the prefill pools into ``staging``
+    ([L][C][sum n][H][D]: pd.py's per-layer [seq, kv_heads, head_dim], requests one
+    after another), merging the prefill TP shards' heads."""
+    g = staging_geometry(geometry, "dst")
+    return RelayoutPlan(src_pools, None, convert=convert,
+                        dst_layout=staging_layout(staging, g["num_layers"], g["num_components"]),
+                        **g)
+
+
+def unpack_plan(staging, dst_pools, convert=None, **geometry):
+    """Plan that writes a staging buffer filled by :func:`pack_plan` into the decode
+    pools through the decode block table, splitting heads over the decode TP shards."""
+    g = staging_geometry(geometry, "src")
+    return RelayoutPlan(None, dst_pools, convert=convert,
+                        src_layout=staging_layout(staging, g["num_layers"], g["num_components"]),
+                        **g)

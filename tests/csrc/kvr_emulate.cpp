@@ -8,49 +8,68 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <vector>
+
 #include "kv_relayout.h"
 #include "kvr_index.h"
 #include "plan.h"
 
 namespace {
 
-struct Extents {
-    int64_t src_bytes, dst_bytes;
+// [start, end) byte ranges of the buffers one side may touch.
+struct Ranges {
+    std::vector<uint64_t> lo, hi;
+    bool holds(uint64_t a, uint64_t n) const {
+        for (size_t k = 0; k < lo.size(); ++k)
+            if (a >= lo[k] && a + n <= hi[k]) return true;
+        return false;
+    }
 };
 
-Extents pool_extents(const kvr_desc *d, const kvr_convert *cv) {
-    const int64_t src_row = (int64_t)d->head_dim * d->elem_bytes;
-    int64_t dst_row = src_row;
-    if (cv != nullptr) dst_row = (int64_t)d->head_dim * (cv->dst_dtype == KVR_DTYPE_BF16 ? 2 : 1);
-    Extents e;
-    e.src_bytes = (int64_t)d->num_layers * d->num_components * d->src_num_blocks *
-                  d->src_block_size * (d->kv_heads / d->src_tp) * src_row;
-    e.dst_bytes = (int64_t)d->num_layers * d->num_components * d->dst_num_blocks *
-                  d->dst_block_size * (d->kv_heads / d->dst_tp) * dst_row;
-    return e;
+// The standard layout: one pool per shard, [L][C][N][B][H/T][D].
+Ranges pool_ranges(const void *const *pools, int32_t T, const kvr_desc *d, int64_t N, int32_t B,
+                   int64_t es) {
+    Ranges r;
+    const int64_t bytes = (int64_t)d->num_layers * d->num_components * N * B *
+                          (d->kv_heads / T) * d->head_dim * es;
+    for (int32_t s = 0; s < T; ++s) {
+        r.lo.push_back((uint64_t)(uintptr_t)pools[s]);
+        r.hi.push_back((uint64_t)(uintptr_t)pools[s] + (uint64_t)bytes);
+    }
+    return r;
+}
+
+Ranges given_ranges(const uint64_t *pairs, int64_t n) {
+    Ranges r;
+    for (int64_t k = 0; k < n; ++k) {
+        r.lo.push_back(pairs[2 * k]);
+        r.hi.push_back(pairs[2 * k + 1]);
+    }
+    return r;
 }
 
 // Walk one launch exactly as the kernel's loops do (CTA by CTA, row window by
-// row window, thread by thread). copy != 0: move the bytes (host pools);
-// otherwise only check. Returns the number of out-of-bounds or misaligned
-// chunk addresses (all skipped), or a negative kvr_status. *chunks receives
-// the number of chunks visited.
-int64_t walk(const kvr_desc *d, const kvr_convert *cv, int sm_count, int layer, int copy,
+// row window, thread by thread). Every row must lie inside one of its side's
+// ranges and every unit address be 16-byte aligned. copy != 0 (bit copies
+// only): move the bytes. Returns the number of bad rows or units (all
+// skipped), or a negative kvr_status; *chunks receives the units visited.
+int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, const kvr_convert *cv,
+             const Ranges &sr, const Ranges &dr, int sm_count, int layer, int copy,
              int64_t *chunks) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, cv, sm_count, &hp, nullptr, nullptr);
+    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
     const int all = layer < 0;
     const int32_t slices = all ? hp.slices_all : hp.slices_layer;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
-                                      hp.factors.data(), all ? 0 : layer, slices);
+                                      hp.factors.data(), hp.src_base.data(), hp.dst_base.data(),
+                                      all ? 0 : layer, slices);
     const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
-    const Extents ext = pool_extents(d, cv);
-    const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
-    const int64_t n_factors = (int64_t)hp.factors.size();
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     const uint32_t U = all ? KVR_UNROLL : KVR_UNROLL_LAYER;
+    const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
+    const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
     int64_t bad = 0, visited = 0;
     for (uint64_t task = 0; task < grid; ++task) {
@@ -68,19 +87,19 @@ int64_t walk(const kvr_desc *d, const kvr_convert *cv, int sm_count, int layer, 
             const uint32_t w1 = w0 + KVR_ROW_WINDOW < r_end ? w0 + KVR_ROW_WINDOW : r_end;
             for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
                 for (uint32_t r = w0 + tid; r < w1; r += KVR_THREADS) {
-                    uint32_t sp, dp, fidx;
-                    int64_t soff, doff;
-                    kvr_row(a.g, l, it, a.sbt, a.dbt, r, &sp, &soff, &dp, &doff, &fidx);
-                    if (sp >= (uint32_t)hp.src_tp || dp >= (uint32_t)hp.dst_tp || soff < 0 ||
-                        doff < 0 || soff + a.g.src_row_bytes > ext.src_bytes ||
-                        doff + a.g.dst_row_bytes > ext.dst_bytes ||
+                    uint32_t fidx;
+                    uint64_t sa, da;
+                    kvr_row(a.g, l, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da,
+                            &fidx);
+                    if (!sr.holds(sa, (uint64_t)a.g.src_row_bytes) ||
+                        !dr.holds(da, (uint64_t)a.g.dst_row_bytes) ||
                         (a.g.conv != KVR_CONV_NONE && (int64_t)fidx >= n_factors)) {
                         ++bad;
                         rows_src[r - w0] = rows_dst[r - w0] = UINT64_MAX;
                         continue;
                     }
-                    rows_src[r - w0] = (uint64_t)((uintptr_t)hp.src[sp] + soff);
-                    rows_dst[r - w0] = (uint64_t)((uintptr_t)hp.dst[dp] + doff);
+                    rows_src[r - w0] = sa;
+                    rows_dst[r - w0] = da;
                 }
             const uint32_t qa = q0 > w0 * rc ? q0 : w0 * rc;
             const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
@@ -114,30 +133,60 @@ int64_t walk(const kvr_desc *d, const kvr_convert *cv, int sm_count, int layer, 
     return bad;
 }
 
+int64_t dst_es(const kvr_desc *d, const kvr_convert *cv) {
+    if (cv == nullptr) return d->elem_bytes;
+    return cv->dst_dtype == KVR_DTYPE_BF16 ? 2 : 1;
+}
+
 }  // namespace
 
 extern "C" {
 
 // Relayout on host pools through the kernel's decomposition. layer < 0: all layers.
 int64_t emu_relayout(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
-    return walk(d, nullptr, sm_count, layer, 1, chunks);
+    return walk(d, nullptr, nullptr, nullptr,
+                pool_ranges(d->src_pools, d->src_tp, d, d->src_num_blocks, d->src_block_size,
+                            d->elem_bytes),
+                pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
+                            d->dst_block_size, d->elem_bytes),
+                sm_count, layer, 1, chunks);
 }
 
 // Bounds/alignment check of every address of a launch (pools are never touched).
 int64_t emu_check(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunks) {
-    return walk(d, nullptr, sm_count, layer, 0, chunks);
+    return walk(d, nullptr, nullptr, nullptr,
+                pool_ranges(d->src_pools, d->src_tp, d, d->src_num_blocks, d->src_block_size,
+                            d->elem_bytes),
+                pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
+                            d->dst_block_size, d->elem_bytes),
+                sm_count, layer, 0, chunks);
 }
 
 // The same check for a converting relayout (units of 16 elements).
 int64_t emu_check_convert(const kvr_desc *d, const kvr_convert *cv, int sm_count, int32_t layer,
                           int64_t *chunks) {
-    return walk(d, cv, sm_count, layer, 0, chunks);
+    return walk(d, nullptr, nullptr, cv,
+                pool_ranges(d->src_pools, d->src_tp, d, d->src_num_blocks, d->src_block_size,
+                            d->elem_bytes),
+                pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
+                            d->dst_block_size, dst_es(d, cv)),
+                sm_count, layer, 0, chunks);
+}
+
+// Any layouts: every row must fall inside the [lo, hi) pairs given per side.
+int64_t emu_walk_ex(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl,
+                    const kvr_convert *cv, const uint64_t *src_ranges, int64_t n_src,
+                    const uint64_t *dst_ranges, int64_t n_dst, int sm_count, int32_t layer,
+                    int32_t copy, int64_t *chunks) {
+    return walk(d, sl, dl, cv, given_ranges(src_ranges, n_src), given_ranges(dst_ranges, n_dst),
+                sm_count, layer, copy, chunks);
 }
 
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, nullptr, sm_count, &hp, nullptr, nullptr);
+    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, &hp, nullptr,
+                                        nullptr);
     if (st != KVR_OK) return st;
     const int64_t n = (int64_t)hp.items.size();
     out[0] = n;

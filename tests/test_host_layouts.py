@@ -1,0 +1,220 @@
+"""Layouts on the host: validation of kvr_layout and the kernel's decomposition walked
+on the CPU over every layout family, against the layout-generic oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from prefill_decode_paged_gb300 import kv_relayout as kr
+from test_host_abi import SMS, _aligned, emu, fake_pools, status_of  # noqa: F401
+
+L_, C_ = 3, 2
+
+
+def _w(seed, **kw):
+    base = dict(num_layers=L_, num_components=C_, kv_heads=8, head_dim=16, elem_bytes=2,
+                src_tp=4, dst_tp=2, src_block=16, dst_block=64, seq_lens=[300, 1, 77, 0])
+    base.update(kw)
+    return wl.custom("lay", seed, **base)
+
+
+def _std(w, pools, side):
+    if side == "src":
+        return oracle.standard_views(pools, w.num_layers, w.num_components, w.src_num_blocks,
+                                     w.src_block, w.kv_heads // w.src_tp, w.head_dim)
+    return oracle.standard_views(pools, w.num_layers, w.num_components, w.dst_num_blocks,
+                                 w.dst_block, w.kv_heads // w.dst_tp, w.head_dim)
+
+
+def _alloc(shape, fill):
+    a = _aligned(shape, np.uint16)
+    a[...] = fill
+    return a
+
+
+def dst_family(w, kind):
+    """(buffers, views[shard][layer][comp]) of a decode side in layout `kind`."""
+    L, C, N, B, Hl, D = w.dst_shape()
+    if kind == "standard":
+        bufs = [_alloc(w.dst_shape(), 0xFFFF) for _ in range(w.dst_tp)]
+        return bufs, _std(w, bufs, "dst")
+    if kind == "hnd":
+        bufs = [_alloc((L, C, N, Hl, B, D), 0xFFFF) for _ in range(w.dst_tp)]
+        return bufs, [[[b[l, c].transpose(0, 2, 1, 3) for c in range(C)] for l in range(L)]
+                      for b in bufs]
+    if kind == "kv_interleaved":
+        bufs = [_alloc((L, N, C, B, Hl, D), 0xFFFF) for _ in range(w.dst_tp)]
+        return bufs, [[[b[l, :, c] for c in range(C)] for l in range(L)] for b in bufs]
+    if kind == "separate":
+        views = [[[_alloc((N, B, Hl, D), 0xFFFF) for _ in range(C)] for _ in range(L)]
+                 for _ in range(w.dst_tp)]
+        return [v for s in views for l in s for v in l], views
+    raise ValueError(kind)
+
+
+def _ranges(bufs):
+    out = []
+    for b in bufs:
+        out += [b.ctypes.data, b.ctypes.data + b.nbytes]
+    return np.array(out, dtype=np.uint64)
+
+
+def _walk(emu, w, src_views, src_bufs, dst_views, dst_bufs, layer=-1, geometry=None,
+          copy=1):
+    emu.emu_walk_ex.restype = ctypes.c_int64
+    emu.emu_walk_ex.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64, ctypes.c_void_p,
+                                                        ctypes.c_int64, ctypes.c_int,
+                                                        ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_void_p]
+    g = geometry or w.geometry()
+    d = kr._Desc(None, None, **g)
+    sl = kr._Layout(**kr.layout_of_views(src_views))
+    dl = kr._Layout(**kr.layout_of_views(dst_views))
+    sr, dr = _ranges(src_bufs), _ranges(dst_bufs)
+    n = ctypes.c_int64()
+    bad = emu.emu_walk_ex(ctypes.byref(d.desc), ctypes.byref(sl.layout), ctypes.byref(dl.layout),
+                          None, sr.ctypes.data, len(src_bufs), dr.ctypes.data, len(dst_bufs),
+                          SMS, layer, copy, ctypes.byref(n))
+    assert bad == 0, f"{bad} rows or units outside their buffers / misaligned"
+    return n.value
+
+
+def _tables(g):
+    keys = ("num_layers", "num_components", "kv_heads", "head_dim", "src_tp", "dst_tp",
+            "src_block", "dst_block", "seq_lens", "src_off", "src_bt", "dst_off", "dst_bt")
+    return {k: g[k] for k in keys}
+
+
+@pytest.mark.parametrize("kind", ["standard", "hnd", "kv_interleaved", "separate"])
+@pytest.mark.parametrize("mode", ["all", "layer"])
+def test_emulated_kernel_on_decode_layouts(emu, kind, mode):
+    w = _w(1)
+    src_bufs = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
+    for a, b in zip(src_bufs, w.src_pools_numpy()):
+        a[...] = b
+    sv = _std(w, src_bufs, "src")
+    ref_bufs, ref_views = dst_family(w, kind)
+    oracle.relayout_general(sv, ref_views, **_tables(w.geometry()))
+    got_bufs, got_views = dst_family(w, kind)
+    layers = [-1] if mode == "all" else range(w.num_layers)
+    for l in layers:
+        _walk(emu, w, sv, src_bufs, got_views, got_bufs, layer=l)
+    for a, b in zip(ref_bufs, got_bufs):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_emulated_kernel_head_major_prefill(emu):
+    w = _w(2)
+    std_src = w.src_pools_numpy()
+    L, C, N, B, Hl, D = w.src_shape()
+    hnd = []
+    for s in std_src:
+        a = _aligned((L, C, N, Hl, B, D), np.uint16)
+        a[...] = s.transpose(0, 1, 2, 4, 3, 5)
+        hnd.append(a)
+    sv = [[[b[l, c].transpose(0, 2, 1, 3) for c in range(C)] for l in range(L)] for b in hnd]
+    ref = w.dst_pools_numpy()
+    oracle.relayout(std_src, ref, **w.geometry())
+    got_bufs, got_views = dst_family(w, "standard")
+    _walk(emu, w, sv, hnd, got_views, got_bufs)
+    for a, b in zip(ref, got_bufs):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_emulated_pack_and_unpack_through_a_staging_buffer(emu):
+    w = _w(3)
+    src_bufs = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
+    for a, b in zip(src_bufs, w.src_pools_numpy()):
+        a[...] = b
+    total = int(w.seq_lens.sum())
+    stage = _aligned((L_, C_, total, w.kv_heads, w.head_dim), np.uint16)
+    stage[...] = 0
+    sviews = [[[stage[l, c].reshape(total, 1, w.kv_heads, w.head_dim) for c in range(C_)]
+               for l in range(L_)]]
+    g_pack = kr.staging_geometry(w.geometry(), "dst")
+    _walk(emu, w, _std(w, src_bufs, "src"), src_bufs, sviews, [stage], geometry=g_pack)
+    want = np.zeros_like(stage)
+    oracle.relayout_general(_std(w, src_bufs, "src"),
+                            [[[want[l, c].reshape(total, 1, w.kv_heads, w.head_dim)
+                               for c in range(C_)] for l in range(L_)]],
+                            **_tables(g_pack))
+    np.testing.assert_array_equal(stage, want)
+    got_bufs, got_views = dst_family(w, "standard")
+    g_unpack = kr.staging_geometry(w.geometry(), "src")
+    _walk(emu, w, sviews, [stage], got_views, got_bufs, geometry=g_unpack)
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src_bufs, ref, **w.geometry())
+    for a, b in zip(ref, got_bufs):
+        np.testing.assert_array_equal(a, b)
+
+
+# -- validation -----------------------------------------------------------------------
+
+def _fake_layout(base, tp, L, C, view_bytes, bs, ts, hs):
+    return dict(bases=[base + i * view_bytes for i in range(tp * L * C)], block_stride=bs,
+                token_stride=ts, head_stride=hs)
+
+
+def test_layout_errors_are_statuses(emu):
+    w = _w(4)
+    s, d = fake_pools(w)
+    L, C, N, B, Hl, D = w.dst_shape()
+    row = D * 2
+    view = N * B * Hl * row
+    good = _fake_layout(1 << 44, w.dst_tp, L, C, view, B * Hl * row, Hl * row, row)
+    g = w.geometry()
+
+    def st(dst_layout, src_pools=s):
+        return status_of(lambda: kr.desc_bytes(src_pools, None, dst_layout=dst_layout, **g))
+    assert st(good) == "KVR_OK"
+    assert kr.desc_bytes(s, None, dst_layout=good, **g) == kr.desc_bytes(s, d, **g)
+    hnd = _fake_layout(1 << 44, w.dst_tp, L, C, view, B * Hl * row, row, B * row)
+    assert st(hnd) == "KVR_OK"
+    bad = dict(good, bases=[good["bases"][0] + 8] + good["bases"][1:])
+    assert st(bad) == "KVR_ERR_ALIGNMENT"
+    assert st(dict(good, token_stride=Hl * row + 8)) == "KVR_ERR_ALIGNMENT"
+    assert st(dict(good, block_stride=-16)) == "KVR_ERR_INVALID_ARG"
+    assert st(dict(good, bases=[0] + good["bases"][1:])) == "KVR_ERR_INVALID_ARG"
+    # rows of one view landing on each other
+    assert st(dict(good, head_stride=16)) == "KVR_ERR_POOL_OVERLAP"
+    assert st(dict(good, block_stride=Hl * row)) == "KVR_ERR_POOL_OVERLAP"
+    # two decode views on top of each other, and a decode view on a prefill pool
+    overl = dict(good, bases=[good["bases"][0]] * len(good["bases"]))
+    assert st(overl) == "KVR_ERR_POOL_OVERLAP"
+    onsrc = dict(good, bases=[s[0]] + good["bases"][1:])
+    assert st(onsrc) == "KVR_ERR_POOL_OVERLAP"
+    # prefill views may overlap (read only), and the standard pools need not be given
+    src_same = _fake_layout(1 << 43, w.src_tp, L, C, 0, *[x * 1 for x in
+                                                          (16 * 2 * row, 2 * row, row)])
+    assert status_of(lambda: kr.desc_bytes(None, None, src_layout=src_same, dst_layout=good,
+                                           **g)) == "KVR_OK"
+    # standard pools missing and no layout
+    assert status_of(lambda: kr.desc_bytes(None, d, **g)) == "KVR_ERR_INVALID_ARG"
+
+
+def test_interleaved_views_are_accepted_exactly(emu):
+    """K and V interleaved per block ([N][C][B][H][D]) share no byte and pass; the same
+    views shifted onto each other by one row are refused."""
+    w = _w(5)
+    s, _ = fake_pools(w)
+    L, C, N, B, Hl, D = w.dst_shape()
+    row = D * 2
+    blk = B * Hl * row
+    base = 1 << 44
+    bases = []
+    for sh in range(w.dst_tp):
+        for l in range(L):
+            for c in range(C):
+                bases.append(base + (sh * L + l) * N * C * blk + c * blk)
+    lay = dict(bases=bases, block_stride=C * blk, token_stride=Hl * row, head_stride=row)
+    g = w.geometry()
+    assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=lay, **g)) == "KVR_OK"
+    shifted = dict(lay, bases=[b - (row if i % 2 else 0) for i, b in enumerate(bases)])
+    assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=shifted, **g)) == \
+        "KVR_ERR_POOL_OVERLAP"
+    last_block = dict(lay, bases=[b + (N - 1) * C * blk if i % 2 else b
+                                  for i, b in enumerate(bases)])
+    assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=last_block, **g)) == \
+        "KVR_ERR_POOL_OVERLAP"
