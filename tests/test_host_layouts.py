@@ -214,7 +214,11 @@ def test_interleaved_views_are_accepted_exactly(emu):
     shifted = dict(lay, bases=[b - (row if i % 2 else 0) for i, b in enumerate(bases)])
     assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=shifted, **g)) == \
         "KVR_ERR_POOL_OVERLAP"
-    last_block = dict(lay, bases=[b + (N - 1) * C * blk if i % 2 else b
+    # V moved by whole block strides stays in K's gaps (still disjoint) ...
+    gaps = dict(lay, bases=[b + 3 * C * blk if i % 2 else b for i, b in enumerate(bases)])
+    assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=gaps, **g)) == "KVR_OK"
+    # ... but V's first block on K's last block is refused
+    last_block = dict(lay, bases=[b + (N - 1) * C * blk - blk if i % 2 else b
                                   for i, b in enumerate(bases)])
     assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=last_block, **g)) == \
         "KVR_ERR_POOL_OVERLAP"
