@@ -1,0 +1,173 @@
+"""GPU parity of the layout-generic relayout against the CPU oracle (bit-exact)."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import pd_pages
+import workloads as wl
+from prefill_decode_paged_gb300 import (RelayoutPlan, layout_of_views, pack_plan,
+                                        unpack_plan)
+from prefill_decode_paged_gb300.kv_relayout import DTYPE_BF16, DTYPE_FP8_E4M3
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _w(seed, **kw):
+    base = dict(num_layers=3, num_components=2, kv_heads=8, head_dim=64, elem_bytes=2,
+                src_tp=4, dst_tp=2, src_block=16, dst_block=64, seq_lens=[300, 1, 77, 0, 129])
+    base.update(kw)
+    return wl.custom("glay", seed, **base)
+
+
+def _tables(w):
+    g = w.geometry()
+    keys = ("num_layers", "num_components", "kv_heads", "head_dim", "src_tp", "dst_tp",
+            "src_block", "dst_block", "seq_lens", "src_off", "src_bt", "dst_off", "dst_bt")
+    return {k: g[k] for k in keys}
+
+
+def _np_t(a):
+    import torch
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+
+def decode_family(w, kind, dtype=np.uint16, fill=0xFFFF):
+    """numpy buffers, numpy views and the matching torch buffers/views of a decode side."""
+    L, C, N, B, Hl, D = w.dst_shape()
+    if kind == "standard":
+        shapes, view = (L, C, N, B, Hl, D), lambda b, l, c: b[l, c]
+    elif kind == "hnd":
+        shapes, view = (L, C, N, Hl, B, D), lambda b, l, c: b[l, c].transpose(0, 2, 1, 3)
+    elif kind == "kv_interleaved":
+        shapes, view = (L, N, C, B, Hl, D), lambda b, l, c: b[l, :, c]
+    else:
+        raise ValueError(kind)
+    bufs = [np.full(shapes, fill, dtype) for _ in range(w.dst_tp)]
+    tbufs = [_np_t(b) for b in bufs]
+    tview = {"standard": lambda b, l, c: b[l, c],
+             "hnd": lambda b, l, c: b[l, c].permute(0, 2, 1, 3),
+             "kv_interleaved": lambda b, l, c: b[l, :, c]}[kind]
+    nv = [[[view(b, l, c) for c in range(C)] for l in range(L)] for b in bufs]
+    tv = [[[tview(b, l, c) for c in range(C)] for l in range(L)] for b in tbufs]
+    return bufs, nv, tbufs, tv
+
+
+@pytest.mark.parametrize("kind", ["standard", "hnd", "kv_interleaved"])
+@pytest.mark.parametrize("mode", ["all", "layer"])
+def test_decode_layouts_match_the_oracle(kind, mode):
+    import torch
+    w = _w(1)
+    src_np = w.src_pools_numpy()
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block, 2,
+                               w.head_dim)
+    ref_bufs, ref_views, _, _ = decode_family(w, kind)
+    oracle.relayout_general(sv, ref_views, **_tables(w))
+    src = [_np_t(a) for a in src_np]
+    _, _, tbufs, tviews = decode_family(w, kind)
+    with RelayoutPlan(src, None, dst_layout=layout_of_views(tviews), **w.geometry()) as plan:
+        if mode == "all":
+            plan.run_all()
+        else:
+            for layer in range(w.num_layers):
+                plan.run_layer(layer)
+        torch.cuda.synchronize()
+    for a, t in zip(ref_bufs, tbufs):
+        assert np.array_equal(t.cpu().numpy().view(np.uint16), a)
+
+
+def test_head_major_prefill_and_per_layer_decode_tensors():
+    """Prefill pools head-major in each block; decode side one K and one V tensor per
+    layer and shard (as engines that allocate per-layer caches do)."""
+    import torch
+    w = _w(2)
+    L, C, N, B, Hl, D = w.src_shape()
+    std = w.src_pools_numpy()
+    hnd = [np.ascontiguousarray(a.transpose(0, 1, 2, 4, 3, 5)) for a in std]
+    ths = [_np_t(a) for a in hnd]
+    sv_t = [[[t[l, c].permute(0, 2, 1, 3) for c in range(C)] for l in range(L)] for t in ths]
+    Ld, Cd, Nd, Bd, Hd, Dd = w.dst_shape()
+    per = [[[torch.full((Nd, Bd, Hd, Dd), -1, dtype=torch.int16, device="cuda")
+             for _ in range(Cd)] for _ in range(Ld)] for _ in range(w.dst_tp)]
+    with RelayoutPlan(None, None, src_layout=layout_of_views(sv_t),
+                      dst_layout=layout_of_views(per), **w.geometry()) as plan:
+        plan.run_all()
+        torch.cuda.synchronize()
+    ref = w.dst_pools_numpy()
+    oracle.relayout(std, ref, **w.geometry())
+    for s in range(w.dst_tp):
+        for l in range(Ld):
+            for c in range(Cd):
+                assert np.array_equal(per[s][l][c].cpu().numpy().view(np.uint16), ref[s][l, c])
+
+
+@pytest.mark.parametrize("direction", ["quant", "dequant"])
+def test_layouts_with_conversion(direction):
+    import torch
+    rng = np.random.default_rng(3)
+    w = _w(4, elem_bytes=2 if direction == "quant" else 1)
+    if direction == "quant":
+        src_np = [rng.integers(0, 1 << 16, w.src_shape(), dtype=np.uint16) for _ in range(4)]
+        kw = dict(src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3)
+        dt, fill = np.uint8, 0xFF
+    else:
+        src_np = [rng.integers(0, 256, w.src_shape(), dtype=np.uint8) for _ in range(4)]
+        kw = dict(src_dtype=DTYPE_FP8_E4M3, dst_dtype=DTYPE_BF16)
+        dt, fill = np.uint16, 0xFFFF
+    scales = rng.uniform(0.01, 2.0, w.num_layers * 2 * 8).astype(np.float32)
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block, 2,
+                               w.head_dim)
+    ref_bufs, ref_views, _, _ = decode_family(w, "hnd", dt, fill)
+    oracle.relayout_general(sv, ref_views, per_head=1, scales=scales, **kw, **_tables(w))
+    _, _, tbufs, tviews = decode_family(w, "hnd", dt, fill)
+    src = [_np_t(a) for a in src_np]
+    with RelayoutPlan(src, None, convert=dict(per_head=True, scales=scales, **kw),
+                      dst_layout=layout_of_views(tviews), **w.geometry()) as plan:
+        plan.run_all()
+        torch.cuda.synchronize()
+    for a, t in zip(ref_bufs, tbufs):
+        assert np.array_equal(t.cpu().numpy().view(dt), a)
+
+
+def test_pack_gives_pd_py_gather_and_unpack_gives_the_direct_relayout():
+    import torch
+    w = _w(5)
+    src_np = w.src_pools_numpy()
+    src = [_np_t(a) for a in src_np]
+    total = int(w.seq_lens.sum())
+    stage = torch.zeros((w.num_layers, 2, total, w.kv_heads, w.head_dim), dtype=torch.int16,
+                        device="cuda")
+    with pack_plan(src, stage, **w.geometry()) as plan:
+        plan.run_all()
+        torch.cuda.synchronize()
+    got = stage.cpu().numpy().view(np.uint16)
+    off = np.concatenate([[0], np.cumsum(w.seq_lens)])
+    for r, n in enumerate(w.seq_lens.tolist()):
+        if n == 0:
+            continue
+        blocks = w.src_bt[w.src_off[r]:w.src_off[r + 1]][: -(-n // w.src_block)]
+        for l in range(w.num_layers):
+            for c in range(2):
+                want = pd_pages.gather_prefill(src_np, l, c, blocks, n, num_layers=w.num_layers,
+                                               num_components=2, kv_heads=w.kv_heads,
+                                               head_dim=w.head_dim, src_tp=w.src_tp,
+                                               src_block=w.src_block,
+                                               src_num_blocks=w.src_num_blocks)
+                assert np.array_equal(got[l, c, off[r]:off[r] + n], want)
+    dst = [_np_t(a) for a in w.dst_pools_numpy()]
+    with unpack_plan(stage, dst, **w.geometry()) as plan:
+        for layer in range(w.num_layers):
+            plan.run_layer(layer)
+        torch.cuda.synchronize()
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src_np, ref, **w.geometry())
+    for a, t in zip(ref, dst):
+        assert np.array_equal(t.cpu().numpy().view(np.uint16), a)
