@@ -221,9 +221,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: str, layers: int):
+def profiled_traffic(config: str, layers: int, suffix: str = ""):
     """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"relayout_{config}.md")
+    path = os.path.join(ROOT, "profiles", f"relayout_{config}{suffix}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -477,8 +477,8 @@ def run_ours(args):
     hbm_peak, peak_src = measured_hbm_peak()
     avg_launch_ms = ms_all / K
     achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
-    traffic, _ = profiled_traffic(
-        args.config if conv is None else f"{args.config}_{args.convert}", w.num_layers)
+    traffic, _ = profiled_traffic(args.config, w.num_layers,
+                                  "" if conv is None else f"_{args.convert}")
     prompts = w.num_requests
     value = whole_job_gbs(bytes_step, K, world, ms_all * 1e-3)
     out = {
