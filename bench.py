@@ -81,6 +81,9 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--convert", default="none", choices=["none", "bf16_to_fp8", "fp8_to_bf16"],
                    help="change the KV dtype on the way (FP8 = E4M3, per-head scales)")
+    p.add_argument("--sm-sweep", default="",
+                   help="comma-separated SM counts: also time the whole-prompt relayout on "
+                        "streams limited to that many SMs (green contexts)")
     p.add_argument("--modes", default="all,layer,graph",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA graph)")
@@ -383,6 +386,31 @@ def run_ours(args):
         stream.wait_stream(cap)
         ms_graph = timed(g.replay, K)
 
+    # the whole-prompt relayout on streams limited to a number of SMs
+    sm_sweep = None
+    if args.sm_sweep:
+        from prefill_decode_paged_gb300 import SmStream
+        sm_sweep = {}
+        for want in [int(x) for x in args.sm_sweep.split(",") if x]:
+            with SmStream(want) as sms:
+                ext = torch.cuda.ExternalStream(sms.handle, device=dev)
+                steps = max(1, K // 4)
+                for _ in range(3):
+                    plan.run_all(sms.handle)
+                ext.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                th = time.time()
+                e0.record(ext)
+                for _ in range(steps):
+                    plan.run_all(sms.handle)
+                e1.record(ext)
+                ext.synchronize()
+                windows.append((th, time.time()))
+                ms = e0.elapsed_time(e1) / steps
+                sm_sweep[str(sms.sms)] = {"gbs": round(bytes_step / (ms * 1e-3) / 1e9, 1),
+                                          "ms_per_step": round(ms, 4)}
+
     # e2e: the pools live in pinned host memory; every step hands the batch over
     # through the public no-allocation call, whose kernel reads the prefill rows
     # from host memory and writes the decode rows to host memory over
@@ -527,6 +555,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": bytes_step},
         "e2e": e2e,
         "e2e_staged": e2e_staged,
+        "sm_sweep": sm_sweep,
         "cpu_baseline": cpu,
         "clocks": clock,
     }

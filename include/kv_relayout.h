@@ -228,6 +228,26 @@ void kv_relayout_plan_destroy(kvr_plan *plan);
 /* Static, human-readable name of a status. */
 const char *kv_relayout_strerror(kvr_status status);
 
+/*
+ * A stream whose kernels run on at most about `sm_count` SMs of the current
+ * device (a CUDA green context). Page "PD multiplexing: splitting prefill and
+ * decode by SM on one GPU", section "Green contexts: carving out SMs for a
+ * stream": memory-bound work reaches the bandwidth limit on a share of the
+ * SMs, leaving the rest to compute; launching the relayout on such a stream
+ * hands the KV over beside the model's kernels. The count is rounded up to
+ * the device's split granularity (8 SMs on this GPU generation);
+ * *sms_granted receives the SMs the stream got. The stream is a cudaStream_t
+ * for kv_relayout_layer() / kv_relayout_all() and any other launch; it shares
+ * memory with the rest of the process. Errors: KVR_ERR_INVALID_ARG for a
+ * count outside [1, SMs], KVR_ERR_UNSUPPORTED when the driver has no green
+ * contexts or cannot split, KVR_ERR_CUDA for other driver failures.
+ * Destroy it (after its work is done) with kv_relayout_sm_stream_destroy().
+ */
+typedef struct kvr_sm_stream kvr_sm_stream;
+kvr_status kv_relayout_sm_stream_create(int32_t sm_count, kvr_sm_stream **out, void **stream,
+                                        int32_t *sms_granted);
+void kv_relayout_sm_stream_destroy(kvr_sm_stream *s);
+
 /* Size of the device scratch array kv_relayout_all_prealloc() works in. */
 #define KVR_PREALLOC_SCRATCH_BYTES (1u << 20)
 

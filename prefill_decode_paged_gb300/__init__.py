@@ -9,9 +9,11 @@ Public API (see ``include/kv_relayout.h`` for the C ABI it binds):
   interleaved, head-major blocks ...) for ``RelayoutPlan(src_layout=..., dst_layout=...)``.
 * :func:`pack_plan` / :func:`unpack_plan` -- through a contiguous staging buffer
   ([L][C][tokens][H][D], pd.py's gathered shape).
+* :class:`SmStream` -- a stream limited to a number of SMs (green context), to run
+  the relayout beside other kernels.
 * :func:`relayout_all_prealloc` -- ``run_all`` without any device allocation, for
   callers that cannot allocate (work lists up to 1 MiB).
 """
 from .kv_relayout import (KVRelayoutError, RelayoutPlan, desc_bytes, library,  # noqa: F401
                           LIB_PATH, STATUS, EXPORTS, relayout_all_prealloc, layout_of_views,
-                          pack_plan, unpack_plan)
+                          pack_plan, unpack_plan, SmStream)

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkv_relayout.so")
-SOURCES = ["plan.cpp", "relayout.cu"]
+SOURCES = ["plan.cpp", "relayout.cu", "sm_stream.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

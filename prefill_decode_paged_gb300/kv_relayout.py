@@ -27,7 +27,8 @@ PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_all", "kv_relayout_plan_bytes", "kv_relayout_plan_destroy",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
-           "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex")
+           "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
+           "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 
@@ -101,6 +102,10 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_desc_bytes_ex.argtypes = [p, p, p, p, p, p]
         lib.kv_relayout_plan_ex.restype = i32
         lib.kv_relayout_plan_ex.argtypes = [p, p, p, p, p]
+        lib.kv_relayout_sm_stream_create.restype = i32
+        lib.kv_relayout_sm_stream_create.argtypes = [i32, p, p, p]
+        lib.kv_relayout_sm_stream_destroy.restype = None
+        lib.kv_relayout_sm_stream_destroy.argtypes = [p]
         _lib = lib
     return _lib
 
@@ -321,6 +326,43 @@ class RelayoutPlan:
     def close(self):
         if getattr(self, "_h", None) is not None:
             library().kv_relayout_plan_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class SmStream:
+    """A stream whose kernels run on at most ~``sm_count`` SMs (a green context).
+
+    ``handle`` is the cudaStream_t (an int) to pass as ``stream=`` to
+    :meth:`RelayoutPlan.run_all` / :meth:`RelayoutPlan.run_layer`; wrap it with
+    ``torch.cuda.ExternalStream(handle)`` to order it with torch work.
+    ``sms`` is the number of SMs granted (rounded up to the split granularity).
+    """
+
+    def __init__(self, sm_count: int):
+        self._h = ctypes.c_void_p()
+        s, g = ctypes.c_void_p(), ctypes.c_int32()
+        st = library().kv_relayout_sm_stream_create(int(sm_count), ctypes.byref(self._h),
+                                                    ctypes.byref(s), ctypes.byref(g))
+        if st != 0:
+            self._h = None
+            raise KVRelayoutError(st, "kv_relayout_sm_stream_create")
+        self.handle, self.sms = s.value, g.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            library().kv_relayout_sm_stream_destroy(self._h)
             self._h = None
 
     def __enter__(self):

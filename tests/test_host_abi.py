@@ -363,3 +363,14 @@ def test_convert_launches_stay_in_bounds(emu, name, direction):
         assert emu.emu_check_convert(ctypes.byref(desc.desc), ctypes.byref(cv.conv), SMS, l,
                                      ctypes.byref(n)) == 0
         assert n.value == units_per_layer * (w.num_layers if l < 0 else 1)
+
+
+def test_sm_stream_rejects_bad_counts_and_needs_a_gpu(cuda_lib):
+    import torch
+    with pytest.raises(kr.KVRelayoutError) as e:
+        kr.SmStream(0)
+    assert e.value.name == "KVR_ERR_INVALID_ARG"
+    if not torch.cuda.is_available():
+        with pytest.raises(kr.KVRelayoutError) as e:
+            kr.SmStream(8)
+        assert e.value.name == "KVR_ERR_CUDA"
