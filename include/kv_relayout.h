@@ -220,6 +220,17 @@ kvr_status kv_relayout_all(const kvr_plan *plan, void *stream);
 kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
                                   int64_t *bytes_written);
 
+/*
+ * The launch shape the plan chose: CTAs of one kv_relayout_all() launch
+ * (`grid_all`), of one kv_relayout_layer() launch (`grid_layer`), and the
+ * decode-side tokens one work item covers (`tile_tokens`). Any output pointer
+ * may be NULL. Per-layer grids are sized from the kernel's occupancy on the
+ * plan's device: a layer whose tiles fit in one wave of resident CTAs is
+ * split to fill that wave, a larger one to about three waves.
+ */
+kvr_status kv_relayout_plan_launch_shape(const kvr_plan *plan, int64_t *grid_all,
+                                         int64_t *grid_layer, int32_t *tile_tokens);
+
 /* Free the plan and its device buffer (NULL is a no-op). Synchronizes the
  * device buffer's release like cudaFree: call it after the launches that use
  * the plan have been ordered before any reuse of that memory. */

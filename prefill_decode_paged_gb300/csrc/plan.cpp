@@ -60,6 +60,19 @@ int32_t choose_slices(int64_t tasks_unsliced, int64_t avg_chunks, int sm_count,
     return (int32_t)std::min(want, most);
 }
 
+// Per-layer launches are short: a partial extra wave costs a large share of
+// the launch. With `slots` CTAs resident at once, a layer whose items fit in
+// one wave is sliced to fill that wave without spilling over; a layer with
+// more items is sliced to about three waves, so the last one is a small part.
+int32_t choose_layer_slices(int64_t items, int64_t avg_chunks, int sm_count, int resident) {
+    if (items <= 0) return 1;
+    const int64_t slots =
+        (int64_t)std::max(sm_count, 1) * (resident > 0 ? resident : KVR_LAYER_CTAS_PER_SM);
+    const int64_t want = items < slots ? slots / items : ceil_div(3 * slots, items);
+    const int64_t most = std::max<int64_t>(1, avg_chunks / KVR_MIN_SLICE_CHUNKS);
+    return (int32_t)std::max<int64_t>(1, std::min(want, most));
+}
+
 // One side's views: base address per (shard, layer, component), shared
 // strides, and the bytes one view spans.
 struct Side {
@@ -209,8 +222,8 @@ kvr_status check_regions(const Side &src, const Side &dst, std::vector<uint64_t>
 
 kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
                                const kvr_layout *dst_layout, const kvr_convert *cv,
-                               int sm_count, KvrHostPlan *hp, int64_t *bytes_read_out,
-                               int64_t *bytes_written_out) {
+                               int sm_count, int layer_resident, KvrHostPlan *hp,
+                               int64_t *bytes_read_out, int64_t *bytes_written_out) {
     if (d == nullptr) return KVR_ERR_INVALID_ARG;
     const int32_t L = d->num_layers, C = d->num_components, H = d->kv_heads, D = d->head_dim;
     const int32_t es = d->elem_bytes, Tp = d->src_tp, Td = d->dst_tp;
@@ -401,7 +414,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     }
 
     const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
-    hp->slices_layer = choose_slices(n_items, avg_chunks, sm_count, KVR_LAYER_CTAS_PER_SM);
+    hp->slices_layer = choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident);
     hp->slices_all =
         choose_slices((int64_t)L * n_items, avg_chunks, sm_count, KVR_TARGET_CTAS_PER_SM);
     while ((int64_t)L * n_items * hp->slices_all > INT32_MAX && hp->slices_all > 1)
@@ -438,7 +451,7 @@ extern "C" kvr_status kv_relayout_desc_bytes_ex(const kvr_desc *desc,
     int64_t r = 0, w = 0;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, 0, nullptr, &r, &w);
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, 0, 0, nullptr, &r, &w);
     } catch (...) {
         return KVR_ERR_NOMEM;
     }

@@ -21,9 +21,10 @@
 #ifndef KVR_ROW_WINDOW
 #define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once
 #endif
-// A launch aims at this many CTAs per SM (whole-prompt / per-layer); items
-// are sliced until it does, but no slice gets fewer than
-// KVR_MIN_SLICE_CHUNKS 16-byte chunks.
+// A whole-prompt launch aims at this many CTAs per SM; items are sliced until
+// it does, but no slice gets fewer than KVR_MIN_SLICE_CHUNKS units. Per-layer
+// launches are shaped by the kernel's occupancy (see choose_layer_slices);
+// KVR_LAYER_CTAS_PER_SM stands in for it when it is unknown.
 #ifndef KVR_TARGET_CTAS_PER_SM
 #define KVR_TARGET_CTAS_PER_SM 8
 #endif
@@ -62,10 +63,12 @@ struct KvrHostPlan {
 // the conversion `cv` (NULL: bit copy); when `hp` is non-NULL also build the
 // host plan for a device with `sm_count` SMs. Never touches device memory.
 // Either byte output may be NULL.
+// `layer_resident`: CTAs of the per-layer kernel one SM holds at once (0 when
+// unknown), used to shape per-layer grids.
 kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
                                const kvr_layout *dst_layout, const kvr_convert *cv,
-                               int sm_count, KvrHostPlan *hp, int64_t *bytes_read,
-                               int64_t *bytes_written);
+                               int sm_count, int layer_resident, KvrHostPlan *hp,
+                               int64_t *bytes_read, int64_t *bytes_written);
 
 // Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,

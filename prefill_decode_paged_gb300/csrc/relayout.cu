@@ -368,8 +368,17 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
     if (p == nullptr) return KVR_ERR_NOMEM;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, &p->host, nullptr,
-                                 nullptr);
+        const int32_t conv = cv == nullptr ? KVR_CONV_NONE
+                             : cv->src_dtype == KVR_DTYPE_BF16 ? KVR_CONV_BF16_TO_E4M3
+                                                                : KVR_CONV_E4M3_TO_BF16;
+        int resident = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, pick_kernel(conv, true),
+                                                          KVR_THREADS, 0) != cudaSuccess) {
+            cudaGetLastError();
+            resident = 0;
+        }
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, resident, &p->host,
+                                 nullptr, nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
@@ -446,6 +455,16 @@ extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *byte
     return KVR_OK;
 }
 
+extern "C" kvr_status kv_relayout_plan_launch_shape(const kvr_plan *plan, int64_t *grid_all,
+                                                    int64_t *grid_layer, int32_t *tile_tokens) {
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)plan->host.items.size();
+    if (grid_all) *grid_all = n * plan->host.num_layers * plan->host.slices_all;
+    if (grid_layer) *grid_layer = n * plan->host.slices_layer;
+    if (tile_tokens) *tile_tokens = plan->host.tile;
+    return KVR_OK;
+}
+
 extern "C" void kv_relayout_plan_destroy(kvr_plan *plan) {
     if (plan == nullptr) return;
     if (plan->dev_meta != nullptr) cudaFree(plan->dev_meta);
@@ -511,7 +530,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
 
     KvrHostPlan hp;
     try {
-        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, &hp, nullptr,
+        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, 0, &hp, nullptr,
                                  nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;

@@ -28,7 +28,8 @@ EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_all", "kv_relayout_plan_bytes", "kv_relayout_plan_destroy",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
            "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
-           "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy")
+           "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy",
+           "kv_relayout_plan_launch_shape")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 
@@ -106,6 +107,8 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_sm_stream_create.argtypes = [i32, p, p, p]
         lib.kv_relayout_sm_stream_destroy.restype = None
         lib.kv_relayout_sm_stream_destroy.argtypes = [p]
+        lib.kv_relayout_plan_launch_shape.restype = i32
+        lib.kv_relayout_plan_launch_shape.argtypes = [p, p, p, p]
         _lib = lib
     return _lib
 
@@ -305,6 +308,16 @@ class RelayoutPlan:
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_plan_bytes")
         self.bytes_read, self.bytes_written = r.value, w.value
+
+    @property
+    def launch_shape(self):
+        """(CTAs of one run_all launch, CTAs of one run_layer launch, tokens per tile)."""
+        ga, gl, t = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+        st = library().kv_relayout_plan_launch_shape(self._handle(), ctypes.byref(ga),
+                                                     ctypes.byref(gl), ctypes.byref(t))
+        if st != 0:
+            raise KVRelayoutError(st, "kv_relayout_plan_launch_shape")
+        return ga.value, gl.value, t.value
 
     def run_all(self, stream=None):
         """All layers, one launch on ``stream`` (default: torch's current stream)."""

@@ -57,7 +57,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
              const Ranges &sr, const Ranges &dr, int sm_count, int layer, int copy,
              int64_t *chunks) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, &hp, nullptr, nullptr);
+    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 5, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
     const int all = layer < 0;
@@ -185,8 +185,8 @@ int64_t emu_walk_ex(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *d
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, &hp, nullptr,
-                                        nullptr);
+    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, 5, &hp,
+                                        nullptr, nullptr);
     if (st != KVR_OK) return st;
     const int64_t n = (int64_t)hp.items.size();
     out[0] = n;

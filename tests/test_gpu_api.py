@@ -185,3 +185,23 @@ def test_pools_the_gpu_cannot_reach_are_refused():
     assert e.value.name == "KVR_ERR_POOL_ADDRESS"
     torch.cuda.synchronize()
     assert all(bool((t == -1).all()) for t in dst)
+
+
+def test_launch_shape_fills_the_gpu_per_layer():
+    """128 tiles of 64 decode tokens per layer: a per-layer launch splits them to cover
+    every SM; a whole-prompt launch holds every (layer, tile) task."""
+    import torch
+    w = wl.custom("shape", 9, num_layers=4, num_components=2, kv_heads=8, head_dim=128,
+                  elem_bytes=2, src_tp=2, dst_tp=1, src_block=16, dst_block=64,
+                  seq_lens=[2048] * 4)
+    src = [torch.zeros(w.src_shape(), dtype=torch.int16, device="cuda")
+           for _ in range(w.src_tp)]
+    dst = [torch.zeros(w.dst_shape(), dtype=torch.int16, device="cuda")
+           for _ in range(w.dst_tp)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        grid_all, grid_layer, tile = plan.launch_shape
+    assert tile == 64
+    items = 4 * 2048 // 64
+    assert grid_layer % items == 0 and grid_layer >= sms
+    assert grid_all % (items * w.num_layers) == 0
