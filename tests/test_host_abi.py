@@ -374,3 +374,21 @@ def test_sm_stream_rejects_bad_counts_and_needs_a_gpu(cuda_lib):
         with pytest.raises(kr.KVRelayoutError) as e:
             kr.SmStream(8)
         assert e.value.name == "KVR_ERR_CUDA"
+
+
+def test_geometry_past_the_kernels_32_bit_indices_is_unsupported(cuda_lib):
+    """Row sizes, tile sizes and work-list lengths the kernel indexes in 32 bits are
+    refused at plan time with a status, not truncated."""
+    def st(**geo):
+        w = wl.custom("big", 11, **geo)
+        s, d = fake_pools(w)
+        return status_of(lambda: kr.desc_bytes(s, d, **w.geometry()))
+    base = dict(num_layers=2, num_components=2, kv_heads=8, head_dim=128, elem_bytes=2,
+                src_tp=1, dst_tp=1, src_block=16, dst_block=32, seq_lens=[40])
+    assert st(**base) == "KVR_OK"
+    # one row of 2^31 bytes
+    assert st(**dict(base, head_dim=1 << 30)) == "KVR_ERR_UNSUPPORTED"
+    # one decode block of Bd * C * H rows of 16 units each: 2^24 * 2 * 8 * 16 = 2^32 units
+    assert st(**dict(base, dst_block=1 << 24)) == "KVR_ERR_UNSUPPORTED"
+    # the largest decode block whose units still fit: 2^22 * 256 = 2^30 units
+    assert st(**dict(base, dst_block=1 << 22)) == "KVR_OK"
