@@ -302,6 +302,37 @@ def conversion(args, w):
     return fp8, w, dict(src_dtype=E4M3, dst_dtype=BF16, per_head=True, scales=scales)
 
 
+def host_link_ceiling(torch, dev, read_bytes, write_bytes, steps):
+    """What the host link itself gives for one step's traffic: pinned host -> HBM
+    copy of the bytes the step reads, concurrently with an HBM -> pinned host copy
+    of the bytes it writes (cudaMemcpyAsync on two streams; wall clock)."""
+    h_in = torch.empty(read_bytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(write_bytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(read_bytes, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(write_bytes, dtype=torch.uint8, device=dev)
+    h_in.fill_(1)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def once():
+        with torch.cuda.stream(up):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(down):
+            h_out.copy_(d_out, non_blocking=True)
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        once()
+    torch.cuda.synchronize(dev)
+    sec = (time.perf_counter() - t0) / steps
+    return {"gbs": round((read_bytes + write_bytes) / sec / 1e9, 2),
+            "ms_per_step": round(sec * 1e3, 4),
+            "what": "pinned host -> HBM copy of the bytes a step reads, concurrent with an "
+                    "HBM -> pinned host copy of the bytes it writes (cudaMemcpyAsync, two "
+                    "streams)"}
+
+
 def cpu_threads_used():
     return 1  # the oracle is a single-threaded loop nest
 
@@ -463,6 +494,9 @@ def run_ours(args):
         for h, t in zip(h_dst, dst):
             if not torch.equal(h.to(dev), t):
                 raise SystemExit("bench.py: host-pool relayout differs from the HBM one")
+        e2e["link_ceiling"] = host_link_ceiling(torch, dev, plan.bytes_read,
+                                                plan.bytes_written, args.e2e_steps)
+        e2e["frac_of_link"] = round(e2e["value"] / e2e["link_ceiling"]["gbs"], 4)
 
         def staged_step():
             for h, t in zip(h_src, src):

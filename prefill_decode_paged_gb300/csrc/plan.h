@@ -16,7 +16,10 @@
 #define KVR_UNROLL 8             // 16-byte loads in flight per thread before its stores
 #endif
 #ifndef KVR_UNROLL_LAYER
-#define KVR_UNROLL_LAYER 4       // the same for per-layer launches (short, latency-bound)
+#define KVR_UNROLL_LAYER 8       // the same for per-layer bit-copy launches
+#endif
+#ifndef KVR_UNROLL_LAYER_CONVERT
+#define KVR_UNROLL_LAYER_CONVERT 4  // per-layer converting launches (more registers per unit)
 #endif
 #ifndef KVR_ROW_WINDOW
 #define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once

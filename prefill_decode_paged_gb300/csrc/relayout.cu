@@ -235,12 +235,13 @@ using KvrKernel = void (*)(KvrArgs);
 KvrKernel pick_kernel(int32_t conv, bool per_layer) {
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
-            return per_layer
-                       ? kvr_relayout_kernel<KVR_UNROLL_LAYER / 2, KVR_CONV_BF16_TO_E4M3, true>
-                       : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3, false>;
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT / 2,
+                                                   KVR_CONV_BF16_TO_E4M3, true>
+                             : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3, false>;
         case KVR_CONV_E4M3_TO_BF16:
-            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_E4M3_TO_BF16, true>
-                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16, false>;
+            return per_layer
+                       ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT, KVR_CONV_E4M3_TO_BF16, true>
+                       : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16, false>;
         default:
             return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_NONE, true>
                              : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE, false>;

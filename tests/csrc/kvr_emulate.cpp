@@ -57,7 +57,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
              const Ranges &sr, const Ranges &dr, int sm_count, int layer, int copy,
              int64_t *chunks) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 5, &hp, nullptr, nullptr);
+    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 4, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
     const int all = layer < 0;
@@ -67,7 +67,11 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                                       all ? 0 : layer, slices);
     const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
     const uint32_t rc = (uint32_t)a.g.row_chunks;
-    const uint32_t U = all ? KVR_UNROLL : KVR_UNROLL_LAYER;
+    // units in flight per thread, as the kernel instance the launch picks
+    const uint32_t U = hp.g.conv == KVR_CONV_NONE
+                           ? (all ? KVR_UNROLL : KVR_UNROLL_LAYER)
+                           : (all ? KVR_UNROLL : KVR_UNROLL_LAYER_CONVERT) /
+                                 (hp.g.conv == KVR_CONV_BF16_TO_E4M3 ? 2 : 1);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
@@ -185,7 +189,7 @@ int64_t emu_walk_ex(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *d
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, 5, &hp,
+    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, 4, &hp,
                                         nullptr, nullptr);
     if (st != KVR_OK) return st;
     const int64_t n = (int64_t)hp.items.size();
