@@ -189,18 +189,28 @@ def test_pools_the_gpu_cannot_reach_are_refused():
 
 def test_launch_shape_fills_the_gpu_per_layer():
     """128 tiles of 64 decode tokens per layer: a per-layer launch splits them to cover
-    every SM; a whole-prompt launch holds every (layer, tile) task."""
+    every SM; a whole-prompt launch holds every (layer, tile) task. The relayout
+    matches the oracle in both modes."""
     import torch
     w = wl.custom("shape", 9, num_layers=4, num_components=2, kv_heads=8, head_dim=128,
                   elem_bytes=2, src_tp=2, dst_tp=1, src_block=16, dst_block=64,
                   seq_lens=[2048] * 4)
-    src = [torch.zeros(w.src_shape(), dtype=torch.int16, device="cuda")
-           for _ in range(w.src_tp)]
-    dst = [torch.zeros(w.dst_shape(), dtype=torch.int16, device="cuda")
-           for _ in range(w.dst_tp)]
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    with RelayoutPlan(src, dst, **w.geometry()) as plan:
-        grid_all, grid_layer, tile = plan.launch_shape
+    ref = _ref(w, src_np)
+    for mode in ("all", "layer"):
+        dst = to_device(w.dst_pools_numpy(), 2)
+        with RelayoutPlan(src, dst, **w.geometry()) as plan:
+            grid_all, grid_layer, tile = plan.launch_shape
+            if mode == "all":
+                plan.run_all()
+            else:
+                for layer in range(w.num_layers):
+                    plan.run_layer(layer)
+            torch.cuda.synchronize()
+        for a, b in zip(ref, to_host(dst, w)):
+            np.testing.assert_array_equal(b, a)
     assert tile == 64
     items = 4 * 2048 // 64
     assert grid_layer % items == 0 and grid_layer >= sms

@@ -240,7 +240,7 @@ def test_emulated_kernel_matches_oracle(emu, case, sms):
         np.testing.assert_array_equal(a, b)
     per = _pools(w, w.dst_pools_numpy())
     for l in range(w.num_layers):
-        _emu_run(emu, w, src, per, layer=l, sms=sms)
+        assert _emu_run(emu, w, src, per, layer=l, sms=sms) * w.num_layers == n
     for a, b in zip(ref, per):
         np.testing.assert_array_equal(a, b)
     check_dst(w, whole, expected_from_src(w, src), w._sentinel_value(0xFF))
@@ -261,7 +261,7 @@ def test_full_size_launches_stay_in_bounds(emu, name):
     desc = kr._Desc(s, d, **w.geometry())
     per_layer = w.seq_lens.sum() * w.num_components * w.kv_heads * w.head_dim * w.elem_bytes
     n = ctypes.c_int64()
-    layers = [-1] if name == "llama70b" else [0, w.num_layers - 1]
+    layers = [-1, 0, w.num_layers - 1] if name == "llama70b" else [0, w.num_layers - 1]
     for l in layers:
         assert emu.emu_check(ctypes.byref(desc.desc), SMS, l, ctypes.byref(n)) == 0
         assert n.value * 16 == (per_layer * (w.num_layers if l < 0 else 1))
@@ -358,7 +358,7 @@ def test_convert_launches_stay_in_bounds(emu, name, direction):
     cv = kr._Convert(**conv)
     n = ctypes.c_int64()
     units_per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim // 16
-    layers = [-1] if name == "llama70b" else [0, w.num_layers - 1]
+    layers = [-1, 0, w.num_layers - 1] if name == "llama70b" else [0, w.num_layers - 1]
     for l in layers:
         assert emu.emu_check_convert(ctypes.byref(desc.desc), ctypes.byref(cv.conv), SMS, l,
                                      ctypes.byref(n)) == 0
