@@ -121,10 +121,12 @@ def _strerror(status: int) -> str:
 
 
 def _ptr(x) -> int:
-    """Device address of a torch tensor (or an int that already is one)."""
+    """Address of a torch tensor or numpy array (or an int that already is one)."""
     if isinstance(x, int):
         return x
-    return int(x.data_ptr())
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x.ctypes.data)
 
 
 class _Desc:
@@ -174,7 +176,8 @@ class _Convert:
 class _Layout:
     """Keeps a C layout descriptor and its base-address array alive."""
 
-    def __init__(self, bases, block_stride, token_stride, head_stride):
+    def __init__(self, bases, block_stride, token_stride, head_stride, shape=None,
+                 elem_bytes=None):
         self.bases = (ctypes.c_void_p * max(1, len(bases)))(*[_ptr(x) for x in bases])
         lay = KvrLayout()
         lay.bases = ctypes.cast(self.bases, ctypes.c_void_p)
@@ -187,8 +190,11 @@ class _Layout:
 def layout_of_views(views):
     """A side's layout from its views: ``views[shard][layer][component]`` are tensors
     (torch or numpy) shaped [block][token][head][dim] with a contiguous last
-    dimension and the same strides. Returns the dict RelayoutPlan takes."""
-    bases, strides = [], None
+    dimension, the same strides and the same element size. Returns the dict
+    RelayoutPlan takes; besides the bases and strides it records the views'
+    smallest extents (``shape``) and element size, which the plan checks against
+    the geometry (the C library sees addresses only)."""
+    bases, strides, shape, elem = [], None, None, None
     for per_shard in views:
         for per_layer in per_shard:
             for v in per_layer:
@@ -203,11 +209,74 @@ def layout_of_views(views):
                 if len(st) != 4 or st[3] != es:
                     raise ValueError("views must be [block][token][head][dim], dim contiguous")
                 if strides is None:
-                    strides = st[:3]
-                elif st[:3] != strides:
-                    raise ValueError("all views of a side must share their strides")
+                    strides, shape, elem = st[:3], tuple(int(x) for x in v.shape), es
+                elif st[:3] != strides or es != elem:
+                    raise ValueError("all views of a side must share their strides and "
+                                     "element size")
+                else:
+                    shape = tuple(min(a, int(b)) for a, b in zip(shape, v.shape))
+    if strides is None:
+        raise ValueError("no views")
     return dict(bases=bases, block_stride=strides[0], token_stride=strides[1],
-                head_stride=strides[2])
+                head_stride=strides[2], shape=shape, elem_bytes=elem)
+
+
+_DTYPE_BYTES = {DTYPE_BF16: 2, DTYPE_FP8_E4M3: 1}
+
+
+def _nbytes(x):
+    """Bytes of a torch tensor or numpy array; None for a bare address."""
+    if isinstance(x, int):
+        return None
+    if hasattr(x, "element_size") and hasattr(x, "numel"):
+        return int(x.numel()) * int(x.element_size())
+    if hasattr(x, "nbytes"):
+        return int(x.nbytes)
+    return None
+
+
+def _contiguous(x) -> bool:
+    if hasattr(x, "is_contiguous"):
+        return bool(x.is_contiguous())
+    flags = getattr(x, "flags", None)
+    return flags is None or bool(flags["C_CONTIGUOUS"])
+
+
+def _check_extents(src_pools, dst_pools, convert, src_layout, dst_layout, g):
+    """The C library checks pool addresses, not allocation sizes: make sure every
+    pool tensor and every described view holds what the geometry addresses, so an
+    undersized tensor raises here instead of being written past its end. Geometry
+    the library itself refuses (zero sizes, heads not divisible) is left to it."""
+    es_src = g["elem_bytes"]
+    es_dst = es_src if convert is None else _DTYPE_BYTES.get(int(convert["dst_dtype"]), es_src)
+    for side, pools, layout, es in (("src", src_pools, src_layout, es_src),
+                                    ("dst", dst_pools, dst_layout, es_dst)):
+        T, H = g[f"{side}_tp"], g["kv_heads"]
+        if T < 1 or H < 1 or H % T:
+            continue
+        need_shape = (g[f"{side}_num_blocks"], g[f"{side}_block"], H // T, g["head_dim"])
+        if layout is not None:
+            shape, elem = layout.get("shape"), layout.get("elem_bytes")
+            if elem is not None and elem != es:
+                raise ValueError(f"{side} views hold {elem}-byte elements; the relayout "
+                                 f"{'reads' if side == 'src' else 'writes'} {es}-byte ones")
+            if shape is not None and any(h < n for h, n in zip(shape, need_shape)):
+                raise ValueError(f"{side} views are {list(shape)} ([block][token][head][dim]); "
+                                 f"the geometry addresses {list(need_shape)}")
+            continue
+        if pools is None:
+            continue
+        need = g["num_layers"] * g["num_components"] * es
+        for x in need_shape:
+            need *= x
+        for k, p in enumerate(pools):
+            if not _contiguous(p):
+                raise ValueError(f"{side} pool {k} is not contiguous: describe a strided "
+                                 f"pool with a layout (layout_of_views)")
+            have = _nbytes(p)
+            if have is not None and have < need:
+                raise ValueError(f"{side} pool {k} holds {have} bytes; the geometry "
+                                 f"addresses {need}")
 
 
 def _layout_arg(layout):
@@ -217,6 +286,7 @@ def _layout_arg(layout):
 def desc_bytes(src_pools, dst_pools, convert=None, src_layout=None, dst_layout=None,
                **geometry):
     """Validate a descriptor on the host; return (bytes_read, bytes_written)."""
+    _check_extents(src_pools, dst_pools, convert, src_layout, dst_layout, geometry)
     d = _Desc(src_pools, dst_pools, **geometry)
     r, w = ctypes.c_int64(), ctypes.c_int64()
     if src_layout is not None or dst_layout is not None:
@@ -251,6 +321,7 @@ def relayout_all_prealloc(src_pools, dst_pools, stream=None, **geometry):
     stream capture. Calls share the array: calls that overlap on the GPU (on
     different, unordered streams) race.
     """
+    _check_extents(src_pools, dst_pools, None, None, None, geometry)
     d = _Desc(src_pools, dst_pools, **geometry)
     st = library().kv_relayout_all_prealloc(ctypes.byref(d.desc), _stream_handle(stream))
     if st != 0:
@@ -283,6 +354,7 @@ class RelayoutPlan:
     def __init__(self, src_pools, dst_pools, convert=None, src_layout=None, dst_layout=None,
                  **geometry):
         self._h = None
+        _check_extents(src_pools, dst_pools, convert, src_layout, dst_layout, geometry)
         self._d = _Desc(src_pools, dst_pools, **geometry)
         self.num_layers = geometry["num_layers"]
         h = ctypes.c_void_p()
@@ -408,8 +480,10 @@ def staging_geometry(geometry, side):
 
 def staging_layout(buf, num_layers, num_components):
     """Layout of a staging tensor shaped [L][C][tokens][H][D] (one shard)."""
+    if len(buf.shape) != 5 or tuple(buf.shape[:2]) != (num_layers, num_components):
+        raise ValueError(f"staging buffer is {list(buf.shape)}; expected "
+                         f"[{num_layers}][{num_components}][tokens][heads][head_dim]")
     L, C, T, H, D = buf.shape
-    assert (L, C) == (num_layers, num_components)
     return layout_of_views([[[buf[l, c].reshape(T, 1, H, D) for c in range(C)]
                              for l in range(L)]])
 

@@ -222,3 +222,38 @@ def test_interleaved_views_are_accepted_exactly(emu):
                                   for i, b in enumerate(bases)])
     assert status_of(lambda: kr.desc_bytes(s, None, dst_layout=last_block, **g)) == \
         "KVR_ERR_POOL_OVERLAP"
+
+
+def test_binding_refuses_tensors_smaller_than_the_geometry(emu):
+    """The C library sees addresses only; the binding checks that the pools, views
+    and staging buffers it is given hold everything the geometry addresses."""
+    w = _w(6)
+    g = w.geometry()
+    src = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
+    dst = [_aligned(w.dst_shape(), np.uint16) for _ in range(w.dst_tp)]
+    assert kr.desc_bytes(src, dst, **g)[0] > 0
+    short = _aligned((int(np.prod(w.dst_shape())) - 1,), np.uint16)
+    with pytest.raises(ValueError, match="dst pool 1"):
+        kr.desc_bytes(src, [dst[0], short], **g)
+    with pytest.raises(ValueError, match="src pool 0 holds"):
+        kr.desc_bytes([src[0].reshape(-1)[:-8]] + src[1:], dst, **g)
+    with pytest.raises(ValueError, match="src pool 0 is not contiguous"):
+        kr.desc_bytes([src[0][:, :, ::2]] + src[1:], dst, **g)
+    # views: one block too few, and the wrong element size
+    L, C, N, B, Hl, D = w.dst_shape()
+    views = [[[b[l, c] for c in range(C)] for l in range(L)] for b in dst]
+    assert kr.desc_bytes(src, None, dst_layout=kr.layout_of_views(views), **g)[0] > 0
+    fewer = [[[b[l, c][:-1] for c in range(C)] for l in range(L)] for b in dst]
+    with pytest.raises(ValueError, match="dst views"):
+        kr.desc_bytes(src, None, dst_layout=kr.layout_of_views(fewer), **g)
+    wide = [_aligned((L, C, N, B, Hl, D), np.uint32) for _ in range(w.dst_tp)]
+    wide_views = [[[b[l, c] for c in range(C)] for l in range(L)] for b in wide]
+    with pytest.raises(ValueError, match="4-byte elements"):
+        kr.desc_bytes(src, None, dst_layout=kr.layout_of_views(wide_views), **g)
+    # staging buffers: the batch's token count, all heads
+    total = int(w.seq_lens.sum())
+    stage = _aligned((L_, C_, total - 1, w.kv_heads, w.head_dim), np.uint16)
+    with pytest.raises(ValueError, match="dst views"):
+        kr.pack_plan(src, stage, **g)
+    with pytest.raises(ValueError, match="staging buffer"):
+        kr.pack_plan(src, stage[0], **g)
