@@ -265,7 +265,7 @@ def oracle_sample(w, src_layers, budget_s, reps_cap=1000, conv=None):
         dst = [np.zeros(wk.dst_shape(), {1: np.uint8, 2: np.uint16}[dst_es])
                for _ in range(wk.dst_tp)]
         per_layer = elems * (w.elem_bytes + dst_es)
-        per = len(conv["scales"]) // w.num_layers
+        per = w.num_components * (w.kv_heads if conv["per_head"] else 1)   # scales per layer
         geo = wk.geometry()
         geo.pop("elem_bytes")
     moved, spent, reps = 0, 0.0, 0
@@ -333,6 +333,35 @@ def host_link_ceiling(torch, dev, read_bytes, write_bytes, steps):
                     "streams)"}
 
 
+def algorithmic_bytes(w, conv):
+    """Bytes one whole-prompt hand-off reads plus writes (both arms' metric)."""
+    elems = int(w.seq_lens.sum()) * w.num_layers * w.num_components * w.kv_heads * w.head_dim
+    dst_es = w.elem_bytes if conv is None else (2 if conv["dst_dtype"] == BF16 else 1)
+    return elems * (w.elem_bytes + dst_es)
+
+
+def dtype_label(w, args, conv):
+    if conv is not None:
+        return args.convert.replace("_to_", "->")
+    return "bf16" if w.values == "randn" else f"u{8 * w.elem_bytes}"
+
+
+def data_label(w):
+    values = "randn bf16 values" if w.values == "randn" else \
+        f"random {8 * w.elem_bytes}-bit patterns"
+    return f"synthetic (seeded {values} in the prefill pools, seeded random block tables)"
+
+
+def workload_config(args, w, conv):
+    """The ``config`` keys both arms report for the same workload."""
+    return {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
+            "mode": "whole-prompt (all layers, one launch per step)",
+            "convert": None if conv is None else
+            f"{args.convert} (FP8 = E4M3, one scale per layer, component and head)",
+            "prompts_per_step": w.num_requests, "tokens_per_step": int(w.seq_lens.sum()),
+            "bytes_per_step": algorithmic_bytes(w, conv)}
+
+
 def cpu_threads_used():
     return 1  # the oracle is a single-threaded loop nest
 
@@ -361,6 +390,8 @@ def run_ours(args):
     dst = w_dst.dst_pools_torch(dev)
     plan = RelayoutPlan(src, dst, convert=conv, **w.geometry())
     bytes_step = plan.bytes_read + plan.bytes_written
+    if bytes_step != algorithmic_bytes(w, conv):
+        raise SystemExit("bench.py: the plan's byte count differs from the workload's")
     stream = torch.cuda.current_stream(dev)
 
     uuid = None
@@ -554,15 +585,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("bf16" if w.values == "randn" else f"u{8 * w.elem_bytes}") if conv is None
-        else args.convert.replace("_to_", "->"),
-        "data": "synthetic (seeded randn bf16 pools, seeded random block tables)",
-        "config": {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
-                   "mode": "whole-prompt (all layers, one launch per step)",
-                   "convert": None if conv is None else
-                   f"{args.convert} (FP8 = E4M3, one scale per layer, component and head)",
-                   "prompts_per_step": prompts, "tokens_per_step": int(w.seq_lens.sum()),
-                   "bytes_per_step": bytes_step,
+        "dtype": dtype_label(w, args, conv),
+        "data": data_label(w),
+        "config": {**workload_config(args, w, conv),
                    "l2": "inputs larger than L2 (no flush)" if bytes_step > 2 * 129e6 else
                          "working set fits in L2 (launch-bound case)",
                    "parallelism": f"replica per GPU x{world}"},
@@ -613,20 +638,21 @@ def run_reference(args):
     w = wl.get(args.config)
     if args.layers:
         w = w.with_layers(args.layers)
+    w, _, conv = conversion(args, w)
     # per step: a bounded sample of layers, sized so W + K steps take about two minutes
     probe = w.with_layers(1)
     src1 = probe.src_pools_numpy()
-    _, t1, _, _ = oracle_sample(probe, [a for a in src1], 0.0, reps_cap=1)
+    _, t1, _, _ = oracle_sample(probe, [a for a in src1], 0.0, reps_cap=1, conv=conv)
     per_layer_s = max(t1, 1e-4)
     total = args.steps + args.warmup
     n = int(max(1, min(w.num_layers, 120.0 / (total * per_layer_s))))
     wk = w.with_layers(n)
     src = wk.src_pools_numpy()
     for _ in range(args.warmup):
-        oracle_sample(wk, src, 0.0, reps_cap=1)
+        oracle_sample(wk, src, 0.0, reps_cap=1, conv=conv)
     moved, spent = 0, 0.0
     for _ in range(args.steps):
-        m, s, _, _ = oracle_sample(wk, src, 0.0, reps_cap=1)
+        m, s, _, _ = oracle_sample(wk, src, 0.0, reps_cap=1, conv=conv)
         moved += m
         spent += s
     gbs = moved / spent / 1e9
@@ -637,9 +663,10 @@ def run_reference(args):
     out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": f"{w.name}: {WORKLOAD_TEXT.get(args.config, args.config)}",
-                      "sample_layers_per_step": n},
+           "vs_baseline": None, "dtype": dtype_label(w, args, conv),
+           "data": data_label(w),
+           "config": {**workload_config(args, w, conv), "sample_layers_per_step": n,
+                      "parallelism": "CPU oracle, one host thread"},
            "cpu_baseline": cpu,
            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
