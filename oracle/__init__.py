@@ -17,7 +17,22 @@ Two independent definitions live here:
   followed by a write through a list of decode slots. It is only used on
   small inputs, as a cross-check of the C loop nest.
 
-Parity status: every function is pinned (see ``tests/test_oracle_pins.py``).
+The converting relayout (``relayout_convert``: BF16 <-> FP8 E4M3 with a
+scale, section "布局转换") and the layout-generic relayout
+(``relayout_general``: any [block][token][head][dim] views per shard, layer
+and component, same section) are further loop nests in ``kv_oracle.c``.
+
+Parity status: every function is pinned against the pages and the
+mathematics, not against itself: ``tests/test_oracle_pins.py`` (byte counts,
+tagged brute force, inverse re-shard, reduction to a copy, the pd.py
+restatement), ``tests/test_oracle_convert_pins.py`` (E4M3 decode at fixed points and
+against torch's float8_e4m3fn, encode against torch, saturation and NaN,
+BF16 rounding against torch, placement reduced to a copy of codes or values,
+NaN signs through both directions), ``tests/test_oracle_layout_pins.py``
+(standard views reduce to ``relayout`` and ``relayout_convert``; head-major
+blocks, per-layer buffers, K/V interleaving and the staging buffer against
+transposes and pd.py's gather) and
+``tests/test_oracle_mutants.py`` (planted mistakes that the pins must catch).
 """
 from __future__ import annotations
 
