@@ -11,7 +11,8 @@ decode TP8 (block 32): 1.34 GB read and 1.34 GB written per step.
 Printed: one JSON line (rank 0). ``value`` is the whole-job relayout
 throughput in GB/s of algorithmic bytes (read + written), device-timed with
 CUDA events over exactly K steps after W warm-up steps, max over ranks.
-Extra keys: the per-layer launch mode (eager and CUDA-graph), ``e2e`` (the
+Extra keys: the per-layer launch mode (eager and CUDA-graph), launches of a
+group of layers each (``layer_groups``, CUDA graph), ``e2e`` (the
 same metric through the public API with the pools in pinned host memory and
 both copies inside the timed region), ``roofline`` (HBM), ``cpu_baseline``
 (the CPU oracle on a bounded sample of the same workload) and the SM clocks
@@ -84,9 +85,12 @@ def parse_args(argv=None):
     p.add_argument("--sm-sweep", default="",
                    help="comma-separated SM counts: also time the whole-prompt relayout on "
                         "streams limited to that many SMs (green contexts)")
-    p.add_argument("--modes", default="all,layer,graph",
+    p.add_argument("--modes", default="all,layer,graph,groups",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
-                        "eager launches), graph (per-layer launches replayed from a CUDA graph)")
+                        "eager launches), graph (per-layer launches replayed from a CUDA "
+                        "graph), groups (launches of --groups layers each, from a CUDA graph)")
+    p.add_argument("--groups", default="2,4,8,16",
+                   help="layers per launch for the groups measurement")
     return p.parse_args(argv)
 
 
@@ -447,6 +451,30 @@ def run_ours(args):
                 plan.run_layer(layer)
         stream.wait_stream(cap)
         ms_graph = timed(g.replay, K)
+    layer_groups = None
+    if "groups" in modes:
+        # layer groups: ceil(L / n) launches of n layers each (kv_relayout_layers), the
+        # way an engine that computes prefill n layers per round would hand KV over;
+        # captured in a CUDA graph like the per-layer launches
+        layer_groups = {}
+        for n in [int(x) for x in args.groups.split(",") if x]:
+            if n < 2 or n >= L:
+                continue
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                for first in range(0, L, n):
+                    plan.run_layers(first, min(n, L - first))
+            stream.wait_stream(cap)
+            ms = timed(g.replay, K)
+            launches = -(-L // n)
+            layer_groups[str(n)] = {
+                "gbs": round(whole_job_gbs(bytes_step, K, world, ms * 1e-3), 2),
+                "ms_per_prompt": round(ms / K / w.num_requests, 5),
+                "us_per_launch": round(ms * 1e3 / K / launches, 3),
+                "launches_per_step": launches}
+            del g
 
     # the whole-prompt relayout on streams limited to a number of SMs
     sm_sweep = None
@@ -606,6 +634,7 @@ def run_ours(args):
                 "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
                 "launches_per_step": L, "steps": K},
         },
+        "layer_groups": layer_groups,
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),

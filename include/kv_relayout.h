@@ -216,6 +216,20 @@ kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream);
 /* Move all layers of every request: one kernel launch on `stream`. */
 kvr_status kv_relayout_all(const kvr_plan *plan, void *stream);
 
+/*
+ * Move layers [first, first + count) of every request: one kernel launch on
+ * `stream`. Asynchronous. For an engine that computes prefill a group of
+ * layers at a time (page "PD multiplexing: splitting prefill and decode by SM
+ * on one GPU", section "SGLang's PD multiplexing": a round computes
+ * split_forward_token_budget // prompt tokens layers) and hands each group
+ * over as it finishes. count == 1 is kv_relayout_layer(); first == 0 with
+ * count == L is kv_relayout_all(); any split of [0, L) into ranges gives the
+ * same bytes as kv_relayout_all(). KVR_ERR_LAYER_RANGE unless
+ * 0 <= first, 1 <= count and first + count <= L.
+ */
+kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
+                              void *stream);
+
 /* Bytes one kv_relayout_all() reads and writes (per layer: divide by L). */
 kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
                                   int64_t *bytes_written);

@@ -414,12 +414,35 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     }
 
     const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
+    hp->avg_chunks = avg_chunks;
+    hp->sm_count = sm_count;
+    hp->layer_resident = layer_resident;
     hp->slices_layer = choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident);
-    hp->slices_all =
-        choose_slices((int64_t)L * n_items, avg_chunks, sm_count, KVR_TARGET_CTAS_PER_SM);
-    while ((int64_t)L * n_items * hp->slices_all > INT32_MAX && hp->slices_all > 1)
-        --hp->slices_all;
+    hp->slices_all = kvr_range_slices(*hp, L);
     return KVR_OK;
+}
+
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, bool *per_layer) {
+    const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
+    const int64_t slots = (int64_t)std::max(hp.sm_count, 1) *
+                          (hp.layer_resident > 0 ? hp.layer_resident : KVR_LAYER_CTAS_PER_SM);
+    if (count == 1) {
+        *slices = hp.slices_layer;
+        *per_layer = true;
+    } else if (tasks < slots) {
+        *slices = choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count, hp.layer_resident);
+        *per_layer = true;
+    } else {
+        *slices = kvr_range_slices(hp, count);
+        *per_layer = false;
+    }
+}
+
+int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count) {
+    const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
+    int32_t s = choose_slices(tasks, hp.avg_chunks, hp.sm_count, KVR_TARGET_CTAS_PER_SM);
+    while (tasks * s > INT32_MAX && s > 1) --s;
+    return s;
 }
 
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,

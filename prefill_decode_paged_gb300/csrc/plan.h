@@ -60,7 +60,21 @@ struct KvrHostPlan {
     int64_t bytes_written = 0;         // bytes one full relayout writes
     int32_t slices_all = 1;            // slices per item, whole-prompt launch
     int32_t slices_layer = 1;          // slices per item, per-layer launch
+    int64_t avg_chunks = 0;            // average units of an item
+    int32_t sm_count = 0;              // SMs of the device the plan was built for
+    int32_t layer_resident = 0;        // CTAs of the per-layer kernel an SM holds (0: unknown)
 };
+
+// Slices per item of a launch over `count` (>= 2) layers, shaped like a
+// whole-prompt launch (count == num_layers gives slices_all).
+int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count);
+
+// Shape of a kv_relayout_layers() launch over `count` layers: slices per item,
+// and whether it runs the per-layer kernel instance (true for one layer, and
+// for a range whose (layer, item) tasks fit in one wave of that kernel: such
+// a launch is short and latency-bound like a single layer's) or the
+// whole-prompt one.
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, bool *per_layer);
 
 // Validate `d` with its layouts (NULL: the standard layout of d's pools) and
 // the conversion `cv` (NULL: bit copy); when `hp` is non-NULL also build the

@@ -448,6 +448,17 @@ extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
     return launch(plan, 0, plan->host.num_layers, plan->host.slices_all, false, stream);
 }
 
+extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
+                                         void *stream) {
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    const int32_t L = plan->host.num_layers;
+    if (first < 0 || count < 1 || first >= L || count > L - first) return KVR_ERR_LAYER_RANGE;
+    int32_t slices = 1;
+    bool per_layer = true;
+    kvr_range_launch(plan->host, count, &slices, &per_layer);
+    return launch(plan, first, count, slices, per_layer, stream);
+}
+
 extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,
                                              int64_t *bytes_written) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;

@@ -29,7 +29,7 @@ EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
            "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
            "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy",
-           "kv_relayout_plan_launch_shape")
+           "kv_relayout_plan_launch_shape", "kv_relayout_layers")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 
@@ -109,6 +109,8 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_sm_stream_destroy.argtypes = [p]
         lib.kv_relayout_plan_launch_shape.restype = i32
         lib.kv_relayout_plan_launch_shape.argtypes = [p, p, p, p]
+        lib.kv_relayout_layers.restype = i32
+        lib.kv_relayout_layers.argtypes = [p, i32, i32, p]
         _lib = lib
     return _lib
 
@@ -402,6 +404,14 @@ class RelayoutPlan:
         st = library().kv_relayout_layer(self._handle(), int(layer), _stream_handle(stream))
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_layer")
+
+    def run_layers(self, first: int, count: int, stream=None):
+        """Layers [first, first + count), one launch on ``stream`` (default: torch's
+        current stream)."""
+        st = library().kv_relayout_layers(self._handle(), int(first), int(count),
+                                          _stream_handle(stream))
+        if st != 0:
+            raise KVRelayoutError(st, "kv_relayout_layers")
 
     def _handle(self):
         if self._h is None:

@@ -49,28 +49,35 @@ Ranges given_ranges(const uint64_t *pairs, int64_t n) {
 }
 
 // Walk one launch exactly as the kernel's loops do (CTA by CTA, row window by
-// row window, thread by thread). Every row must lie inside one of its side's
-// ranges and every unit address be 16-byte aligned. copy != 0 (bit copies
-// only): move the bytes. Returns the number of bad rows or units (all
-// skipped), or a negative kvr_status; *chunks receives the units visited.
+// row window, thread by thread): count < 0 is kv_relayout_all(), otherwise
+// kv_relayout_layers(first, count) (count == 1: kv_relayout_layer(first)).
+// Every row must lie inside one of its side's ranges and every unit address
+// be 16-byte aligned. copy != 0 (bit copies only): move the bytes. Returns the
+// number of bad rows or units (all skipped), or a negative kvr_status;
+// *chunks receives the units visited.
 int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, const kvr_convert *cv,
-             const Ranges &sr, const Ranges &dr, int sm_count, int layer, int copy,
+             const Ranges &sr, const Ranges &dr, int sm_count, int first, int count, int copy,
              int64_t *chunks) {
     KvrHostPlan hp;
     kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 4, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
-    const int all = layer < 0;
-    const int32_t slices = all ? hp.slices_all : hp.slices_layer;
+    const int all = count < 0;
+    if (!all && (first < 0 || count < 1 || first + count > hp.num_layers))
+        return KVR_ERR_LAYER_RANGE;
+    int32_t slices = hp.slices_all;
+    bool per_layer = false;                      // the per-layer kernel instance
+    if (!all) kvr_range_launch(hp, count, &slices, &per_layer);
+    const int32_t layer0 = all ? 0 : first, layers = all ? hp.num_layers : count;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
                                       hp.factors.data(), hp.src_base.data(), hp.dst_base.data(),
-                                      all ? 0 : layer, slices);
-    const uint64_t grid = (uint64_t)(all ? hp.num_layers : 1) * a.tasks_per_layer;
+                                      layer0, slices);
+    const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     // units in flight per thread, as the kernel instance the launch picks
     const uint32_t U = hp.g.conv == KVR_CONV_NONE
-                           ? (all ? KVR_UNROLL : KVR_UNROLL_LAYER)
-                           : (all ? KVR_UNROLL : KVR_UNROLL_LAYER_CONVERT) /
+                           ? (per_layer ? KVR_UNROLL_LAYER : KVR_UNROLL)
+                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL) /
                                  (hp.g.conv == KVR_CONV_BF16_TO_E4M3 ? 2 : 1);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
@@ -81,7 +88,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
         KvrItem it;
         uint32_t q0, q1;
         kvr_task(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
-        if (q0 > q1 || l < 0 || l >= hp.num_layers) {
+        if (q0 > q1 || l < layer0 || l >= layer0 + layers) {
             ++bad;
             continue;
         }
@@ -153,7 +160,7 @@ int64_t emu_relayout(const kvr_desc *d, int sm_count, int32_t layer, int64_t *ch
                             d->elem_bytes),
                 pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
                             d->dst_block_size, d->elem_bytes),
-                sm_count, layer, 1, chunks);
+                sm_count, layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, 1, chunks);
 }
 
 // Bounds/alignment check of every address of a launch (pools are never touched).
@@ -163,7 +170,7 @@ int64_t emu_check(const kvr_desc *d, int sm_count, int32_t layer, int64_t *chunk
                             d->elem_bytes),
                 pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
                             d->dst_block_size, d->elem_bytes),
-                sm_count, layer, 0, chunks);
+                sm_count, layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, 0, chunks);
 }
 
 // The same check for a converting relayout (units of 16 elements).
@@ -174,7 +181,7 @@ int64_t emu_check_convert(const kvr_desc *d, const kvr_convert *cv, int sm_count
                             d->elem_bytes),
                 pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
                             d->dst_block_size, dst_es(d, cv)),
-                sm_count, layer, 0, chunks);
+                sm_count, layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, 0, chunks);
 }
 
 // Any layouts: every row must fall inside the [lo, hi) pairs given per side.
@@ -183,7 +190,19 @@ int64_t emu_walk_ex(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *d
                     const uint64_t *dst_ranges, int64_t n_dst, int sm_count, int32_t layer,
                     int32_t copy, int64_t *chunks) {
     return walk(d, sl, dl, cv, given_ranges(src_ranges, n_src), given_ranges(dst_ranges, n_dst),
-                sm_count, layer, copy, chunks);
+                sm_count, layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, copy, chunks);
+}
+
+// kv_relayout_layers(first, count) on host pools through the kernel's
+// decomposition (copy != 0: move the bytes; 0: bounds check only).
+int64_t emu_relayout_range(const kvr_desc *d, int sm_count, int32_t first, int32_t count,
+                           int32_t copy, int64_t *chunks) {
+    return walk(d, nullptr, nullptr, nullptr,
+                pool_ranges(d->src_pools, d->src_tp, d, d->src_num_blocks, d->src_block_size,
+                            d->elem_bytes),
+                pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
+                            d->dst_block_size, d->elem_bytes),
+                sm_count, first, count, copy, chunks);
 }
 
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].

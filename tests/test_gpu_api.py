@@ -215,3 +215,35 @@ def test_launch_shape_fills_the_gpu_per_layer():
     items = 4 * 2048 // 64
     assert grid_layer % items == 0 and grid_layer >= sms
     assert grid_all % (items * w.num_layers) == 0
+
+
+@pytest.mark.parametrize("groups", [[4], [1, 3], [2, 2], [3, 1], [1, 2, 1]])
+def test_layer_ranges_match_the_oracle(groups):
+    """kv_relayout_layers over any split of the layers equals the whole relayout."""
+    import torch
+    w = _small()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        first = 0
+        for count in groups:
+            plan.run_layers(first, count)
+            first += count
+        torch.cuda.synchronize()
+    for a, b in zip(_ref(w, src_np), to_host(dst, w)):
+        np.testing.assert_array_equal(b, a)
+
+
+def test_layer_range_errors_are_statuses():
+    import torch
+    w = _small()
+    src = to_device(w.src_pools_numpy(), 2)
+    dst = to_device(w.dst_pools_numpy(), 2)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        for first, count in ((-1, 1), (0, 0), (3, 2), (4, 1), (0, 5)):
+            with pytest.raises(KVRelayoutError) as e:
+                plan.run_layers(first, count)
+            assert e.value.name == "KVR_ERR_LAYER_RANGE"
+        plan.run_layers(0, 4)
+        torch.cuda.synchronize()

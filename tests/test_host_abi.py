@@ -392,3 +392,47 @@ def test_geometry_past_the_kernels_32_bit_indices_is_unsupported(cuda_lib):
     assert st(**dict(base, dst_block=1 << 24)) == "KVR_ERR_UNSUPPORTED"
     # the largest decode block whose units still fit: 2^22 * 256 = 2^30 units
     assert st(**dict(base, dst_block=1 << 22)) == "KVR_OK"
+
+
+def _emu_range(emu, w, src, dst, first, count, copy=1, sms=SMS):
+    emu.emu_relayout_range.restype = ctypes.c_int64
+    emu.emu_relayout_range.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+    d = _host_desc(w, src, dst) if copy else kr._Desc(src, dst, **w.geometry())
+    n = ctypes.c_int64()
+    bad = emu.emu_relayout_range(ctypes.byref(d.desc), sms, first, count, copy, ctypes.byref(n))
+    return bad, n.value
+
+
+@pytest.mark.parametrize("groups", [[5], [1, 1, 1, 1, 1], [2, 3], [3, 2], [1, 3, 1]])
+def test_emulated_layer_ranges_match_the_oracle(emu, groups):
+    """Any split of the layers into ranges, one launch per range, gives the oracle's
+    result; each launch visits exactly its layers' units."""
+    w = wl.custom("rng", 31, num_layers=5, num_components=2, kv_heads=8, head_dim=64,
+                  elem_bytes=2, src_tp=4, dst_tp=2, src_block=16, dst_block=64,
+                  seq_lens=[300, 1, 77, 0, 129])
+    src = _pools(w, w.src_pools_numpy())
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src, ref, **w.geometry())
+    dst = _pools(w, w.dst_pools_numpy())
+    per_layer_units = int(w.seq_lens.sum()) * 2 * 8 * 64 * 2 // 16
+    first = 0
+    for count in groups:
+        bad, n = _emu_range(emu, w, src, dst, first, count)
+        assert bad == 0 and n == count * per_layer_units
+        first += count
+    for a, b in zip(ref, dst):
+        np.testing.assert_array_equal(a, b)
+    check_dst(w, dst, expected_from_src(w, src), w._sentinel_value(0xFF))
+
+
+def test_full_size_layer_ranges_stay_in_bounds(emu):
+    w = wl.get("llama70b")
+    s, d = fake_pools(w)
+    per_layer_units = 4096 * 2 * 8 * 128 * 2 // 16
+    for first, count in ((0, 8), (72, 8), (0, 80), (40, 2), (79, 1)):
+        bad, n = _emu_range(emu, w, s, d, first, count, copy=0)
+        assert bad == 0 and n == count * per_layer_units, (first, count)
+    for first, count in ((-1, 2), (79, 2), (0, 81)):
+        bad, _ = _emu_range(emu, w, s, d, first, count, copy=0)
+        assert bad == kr.KVRelayoutError(-7, "").status
