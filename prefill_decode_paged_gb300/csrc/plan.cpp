@@ -441,6 +441,15 @@ void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, boo
 int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count) {
     const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
     int32_t s = choose_slices(tasks, hp.avg_chunks, hp.sm_count, KVR_TARGET_CTAS_PER_SM);
+    // large items (decode blocks of many tokens) of a bit copy are cut until a
+    // CTA reads at most KVR_MAX_CTA_BYTES, so the grid does not end in a long
+    // partial wave; the converting kernels (more registers, fewer resident
+    // CTAs) measured faster with the larger CTAs, so they are left whole
+    const int64_t item_bytes =
+        hp.g.conv == KVR_CONV_NONE ? hp.avg_chunks * hp.g.src_unit_bytes : 0;
+    const int64_t most = std::max<int64_t>(1, hp.avg_chunks / KVR_MIN_SLICE_CHUNKS);
+    const int64_t want = std::min<int64_t>(most, ceil_div(item_bytes, KVR_MAX_CTA_BYTES));
+    if (want > s) s = (int32_t)want;
     while (tasks * s > INT32_MAX && s > 1) --s;
     return s;
 }

@@ -37,6 +37,11 @@
 #ifndef KVR_MIN_SLICE_CHUNKS
 #define KVR_MIN_SLICE_CHUNKS 512
 #endif
+// Whole-prompt (and multi-layer) bit-copy launches also slice items until no
+// CTA reads more than this many bytes (items of large decode blocks).
+#ifndef KVR_MAX_CTA_BYTES
+#define KVR_MAX_CTA_BYTES (64 * 1024)
+#endif
 // Token tiles hold whole decode blocks and grow (in whole decode blocks)
 // until a tile moves about this many bytes per layer.
 #ifndef KVR_TARGET_ITEM_BYTES
