@@ -418,11 +418,12 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     hp->sm_count = sm_count;
     hp->layer_resident = layer_resident;
     hp->slices_layer = choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident);
-    hp->slices_all = kvr_range_slices(*hp, L);
+    hp->slices_all = kvr_range_slices(*hp, L, 0);
     return KVR_OK;
 }
 
-void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, bool *per_layer) {
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms,
+                      int32_t *slices, bool *per_layer) {
     const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
     const int64_t slots = (int64_t)std::max(hp.sm_count, 1) *
                           (hp.layer_resident > 0 ? hp.layer_resident : KVR_LAYER_CTAS_PER_SM);
@@ -433,23 +434,27 @@ void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, boo
         *slices = choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count, hp.layer_resident);
         *per_layer = true;
     } else {
-        *slices = kvr_range_slices(hp, count);
+        *slices = kvr_range_slices(hp, count, stream_sms);
         *per_layer = false;
     }
 }
 
-int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count) {
+int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sms) {
     const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
-    int32_t s = choose_slices(tasks, hp.avg_chunks, hp.sm_count, KVR_TARGET_CTAS_PER_SM);
-    // large items (decode blocks of many tokens) of a bit copy are cut until a
-    // CTA reads at most KVR_MAX_CTA_BYTES, so the grid does not end in a long
-    // partial wave; the converting kernels (more registers, fewer resident
-    // CTAs) measured faster with the larger CTAs, so they are left whole
-    const int64_t item_bytes =
-        hp.g.conv == KVR_CONV_NONE ? hp.avg_chunks * hp.g.src_unit_bytes : 0;
-    const int64_t most = std::max<int64_t>(1, hp.avg_chunks / KVR_MIN_SLICE_CHUNKS);
-    const int64_t want = std::min<int64_t>(most, ceil_div(item_bytes, KVR_MAX_CTA_BYTES));
-    if (want > s) s = (int32_t)want;
+    const bool limited = stream_sms > 0 && stream_sms < hp.sm_count;
+    int32_t s = choose_slices(tasks, hp.avg_chunks, limited ? stream_sms : hp.sm_count,
+                              KVR_TARGET_CTAS_PER_SM);
+    // large items (decode blocks of many tokens) of a bit copy on the whole
+    // device are cut until a CTA reads at most KVR_MAX_CTA_BYTES, so the grid
+    // does not end in a long partial wave; the converting kernels (more
+    // registers, fewer resident CTAs) measured faster with the larger CTAs,
+    // and so did every launch on an SM-limited stream, so those stay whole
+    if (!limited && hp.g.conv == KVR_CONV_NONE) {
+        const int64_t item_bytes = hp.avg_chunks * hp.g.src_unit_bytes;
+        const int64_t most = std::max<int64_t>(1, hp.avg_chunks / KVR_MIN_SLICE_CHUNKS);
+        const int64_t want = std::min<int64_t>(most, ceil_div(item_bytes, KVR_MAX_CTA_BYTES));
+        if (want > s) s = (int32_t)want;
+    }
     while (tasks * s > INT32_MAX && s > 1) --s;
     return s;
 }

@@ -71,15 +71,25 @@ struct KvrHostPlan {
 };
 
 // Slices per item of a launch over `count` (>= 2) layers, shaped like a
-// whole-prompt launch (count == num_layers gives slices_all).
-int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count);
+// whole-prompt launch (count == num_layers gives slices_all). `stream_sms`:
+// the SMs of the green context the launch's stream runs on (0: the whole
+// device). On the whole device a bit copy's items are also cut to at most
+// KVR_MAX_CTA_BYTES read per CTA (HBM-bound: balance pays); on fewer SMs the
+// launch is latency-bound per SM and larger CTAs amortize their row-table
+// prologue, so items are only sliced to fill those SMs.
+int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sms);
 
 // Shape of a kv_relayout_layers() launch over `count` layers: slices per item,
 // and whether it runs the per-layer kernel instance (true for one layer, and
 // for a range whose (layer, item) tasks fit in one wave of that kernel: such
 // a launch is short and latency-bound like a single layer's) or the
 // whole-prompt one.
-void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t *slices, bool *per_layer);
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms,
+                      int32_t *slices, bool *per_layer);
+
+// SMs of the green context `stream` (a cudaStream_t) belongs to, or 0 when it
+// belongs to none or the driver cannot say (sm_stream.cpp).
+int32_t kvr_stream_green_sms(void *stream);
 
 // Validate `d` with its layouts (NULL: the standard layout of d's pools) and
 // the conversion `cv` (NULL: bit copy); when `hp` is non-NULL also build the

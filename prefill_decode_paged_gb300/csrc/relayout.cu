@@ -445,7 +445,12 @@ extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, voi
 
 extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
-    return launch(plan, 0, plan->host.num_layers, plan->host.slices_all, false, stream);
+    // a stream on a green context with fewer SMs gets a grid shaped for them
+    const int32_t green = kvr_stream_green_sms(stream);
+    const int32_t slices = green > 0 && green < plan->host.sm_count
+                               ? kvr_range_slices(plan->host, plan->host.num_layers, green)
+                               : plan->host.slices_all;
+    return launch(plan, 0, plan->host.num_layers, slices, false, stream);
 }
 
 extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
@@ -455,7 +460,8 @@ extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, in
     if (first < 0 || count < 1 || first >= L || count > L - first) return KVR_ERR_LAYER_RANGE;
     int32_t slices = 1;
     bool per_layer = true;
-    kvr_range_launch(plan->host, count, &slices, &per_layer);
+    kvr_range_launch(plan->host, count, count > 1 ? kvr_stream_green_sms(stream) : 0, &slices,
+                     &per_layer);
     return launch(plan, first, count, slices, per_layer, stream);
 }
 

@@ -19,6 +19,7 @@
 #include <new>
 
 #include "kv_relayout.h"
+#include "plan.h"
 
 struct kvr_sm_stream {
     CUgreenCtx ctx = nullptr;
@@ -75,7 +76,33 @@ bool load(Driver *d) {
            entry("cuStreamDestroy", &d->stream_destroy);
 }
 
+using PFN_StreamGetGreenCtx = CUresult (*)(CUstream, CUgreenCtx *);
+using PFN_GreenCtxGetDevResource = CUresult (*)(CUgreenCtx, CUdevResource *, CUdevResourceType);
+
+struct GreenQuery {
+    PFN_StreamGetGreenCtx stream_green = nullptr;
+    PFN_GreenCtxGetDevResource resource = nullptr;
+    bool ok = false;
+};
+
+GreenQuery load_query() {
+    GreenQuery q;
+    q.ok = entry("cuStreamGetGreenCtx", &q.stream_green) &&
+           entry("cuGreenCtxGetDevResource", &q.resource);
+    return q;
+}
+
 }  // namespace
+
+int32_t kvr_stream_green_sms(void *stream) {
+    static const GreenQuery q = load_query();
+    if (!q.ok || stream == nullptr) return 0;
+    CUgreenCtx g = nullptr;
+    if (q.stream_green((CUstream)stream, &g) != CUDA_SUCCESS || g == nullptr) return 0;
+    CUdevResource r;
+    if (q.resource(g, &r, CU_DEV_RESOURCE_TYPE_SM) != CUDA_SUCCESS) return 0;
+    return (int32_t)r.sm.smCount;
+}
 
 extern "C" kvr_status kv_relayout_sm_stream_create(int32_t sm_count, kvr_sm_stream **out,
                                                    void **stream, int32_t *sms_granted) {

@@ -23,4 +23,9 @@ CASES = {
     "big_block_1_to_64": lambda: wl.custom("f", 6, num_layers=1, num_components=2, kv_heads=4,
                                            head_dim=64, elem_bytes=2, src_tp=1, dst_tp=4,
                                            src_block=1, dst_block=64, seq_lens=[1000, 63]),
+    # 256-token decode blocks of 8 x 128 heads: 1 MB tiles, cut into <= 64 KB slices
+    "huge_block_16_to_256": lambda: wl.custom("g", 7, num_layers=2, num_components=2,
+                                              kv_heads=8, head_dim=128, elem_bytes=2,
+                                              src_tp=2, dst_tp=1, src_block=16,
+                                              dst_block=256, seq_lens=[600, 256, 1]),
 }

@@ -67,7 +67,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
         return KVR_ERR_LAYER_RANGE;
     int32_t slices = hp.slices_all;
     bool per_layer = false;                      // the per-layer kernel instance
-    if (!all) kvr_range_launch(hp, count, &slices, &per_layer);
+    if (!all) kvr_range_launch(hp, count, 0, &slices, &per_layer);
     const int32_t layer0 = all ? 0 : first, layers = all ? hp.num_layers : count;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
                                       hp.factors.data(), hp.src_base.data(), hp.dst_base.data(),

@@ -65,6 +65,17 @@ def test_enumerate_block_sizes_and_tp(tp):
         _gpu_vs_oracle(w, w.src_pools_numpy())
 
 
+@pytest.mark.parametrize("bd,lens", [(256, [1000, 256, 1, 511]), (512, [2048, 700]),
+                                     (1024, [1500])])
+def test_large_decode_blocks(bd, lens):
+    """Decode blocks of 256-1024 tokens: 0.5-2 MB tiles, cut into slices of at most
+    64 KB read per CTA in whole-prompt launches, partial last blocks."""
+    w = wl.custom(f"big{bd}", 300 + bd, num_layers=3, num_components=2, kv_heads=8,
+                  head_dim=128, elem_bytes=2, src_tp=2, dst_tp=1, src_block=16, dst_block=bd,
+                  seq_lens=lens)
+    _gpu_vs_oracle(w, w.src_pools_numpy())
+
+
 @pytest.mark.parametrize("es,head_dim", [(1, 16), (1, 80), (2, 8), (2, 72), (4, 4), (4, 36)])
 def test_element_widths_and_row_sizes(es, head_dim):
     w = wl.custom(f"es{es}", 200 + es * 100 + head_dim, num_layers=2, num_components=2,

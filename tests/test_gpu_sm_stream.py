@@ -47,3 +47,31 @@ def test_sm_stream_rejects_more_sms_than_the_gpu_has():
     with pytest.raises(KVRelayoutError) as e:
         SmStream(total + 1)
     assert e.value.name == "KVR_ERR_INVALID_ARG"
+
+
+def test_layer_ranges_on_an_sm_limited_stream():
+    """Launches on a green-context stream are shaped for its SMs; the bytes are the
+    same as on the whole GPU."""
+    import torch
+    w = wl.custom("smr", 18, num_layers=5, num_components=2, kv_heads=8, head_dim=128,
+                  elem_bytes=2, src_tp=2, dst_tp=1, src_block=16, dst_block=256,
+                  seq_lens=[2000, 300])
+    src_np = w.src_pools_numpy()
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src_np, ref, **w.geometry())
+    src = to_device(src_np, 2)
+    with SmStream(16) as s:
+        ext = torch.cuda.ExternalStream(s.handle)
+        for split in ([5], [2, 3], [1, 4]):
+            dst = to_device(w.dst_pools_numpy(), 2)
+            with RelayoutPlan(src, dst, **w.geometry()) as plan:
+                first = 0
+                for count in split:
+                    if count == w.num_layers:
+                        plan.run_all(s.handle)
+                    else:
+                        plan.run_layers(first, count, s.handle)
+                    first += count
+                ext.synchronize()
+            for a, b in zip(ref, to_host(dst, w)):
+                np.testing.assert_array_equal(b, a)
