@@ -3,7 +3,9 @@
 Public API (see ``include/kv_relayout.h`` for the C ABI it binds):
 
 * :class:`RelayoutPlan` -- validate a batch and upload its work list;
-  ``run_all()`` moves every layer in one launch, ``run_layer(l)`` one layer.
+  ``run_all()`` moves every layer in one launch, ``run_layer(l)`` one layer,
+  ``run_layers(first, count)`` a range of layers; ``launch_shape`` reports the
+  grids it chose.
 * :func:`desc_bytes` -- host-only validation and byte count.
 * :func:`layout_of_views` -- describe any physical layout (per-layer tensors, K/V
   interleaved, head-major blocks ...) for ``RelayoutPlan(src_layout=..., dst_layout=...)``.
