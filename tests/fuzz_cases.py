@@ -1,0 +1,32 @@
+"""Seeded random geometries for the fuzz tests (CPU emulator and GPU parity).
+
+Every draw is a valid hand-off: H divisible by both TP degrees, rows of a whole
+number of 16-byte units, lengths from 0 to a few blocks of either side (ragged
+tails on both), optional shared prefill prefix, pools with slack.
+"""
+import numpy as np
+
+import workloads as wl
+
+
+def random_workload(seed: int, max_tokens: int = 700):
+    rng = np.random.default_rng([seed, 77])
+    es = int(rng.choice([1, 2, 4]))
+    tps = [1, 2, 3, 4, 6, 8]
+    H = int(rng.choice([1, 2, 4, 6, 8, 12, 16]))
+    src_tp = int(rng.choice([t for t in tps if H % t == 0]))
+    dst_tp = int(rng.choice([t for t in tps if H % t == 0]))
+    d_choices = [d for d in (8, 16, 24, 32, 64, 72, 128, 576) if (d * es) % 16 == 0]
+    D = int(rng.choice(d_choices))
+    C = int(rng.choice([1, 2]))
+    L = int(rng.integers(1, 5))
+    bp = int(rng.choice([1, 3, 8, 16, 32, 64]))
+    bd = int(rng.choice([1, 5, 16, 32, 64, 256]))
+    R = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.integers(0, max_tokens, size=R)]
+    if rng.random() < 0.3:
+        lens[int(rng.integers(0, R))] = 0
+    shared = int(rng.integers(0, 3)) if bp > 1 and R > 1 else 0
+    return wl.custom(f"fz{seed}", 1000 + seed, num_layers=L, num_components=C, kv_heads=H,
+                     head_dim=D, elem_bytes=es, src_tp=src_tp, dst_tp=dst_tp, src_block=bp,
+                     dst_block=bd, seq_lens=lens, shared_prefix=shared)

@@ -436,3 +436,32 @@ def test_full_size_layer_ranges_stay_in_bounds(emu):
     for first, count in ((-1, 2), (79, 2), (0, 81)):
         bad, _ = _emu_range(emu, w, s, d, first, count, copy=0)
         assert bad == kr.KVRelayoutError(-7, "").status
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_fuzzed_geometries_on_the_emulated_kernel(emu, seed):
+    """Random valid geometries: every launch mode of the kernel's decomposition, walked
+    on the CPU with bounds checks, equals the oracle."""
+    from fuzz_cases import random_workload
+    w = random_workload(seed)
+    src = _pools(w, w.src_pools_numpy())
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src, ref, **w.geometry())
+    sms = [1, 7, SMS][seed % 3]
+    whole = _pools(w, w.dst_pools_numpy())
+    _emu_run(emu, w, src, whole, sms=sms)
+    for a, b in zip(ref, whole):
+        np.testing.assert_array_equal(a, b)
+    per = _pools(w, w.dst_pools_numpy())
+    for l in range(w.num_layers):
+        _emu_run(emu, w, src, per, layer=l, sms=sms)
+    for a, b in zip(ref, per):
+        np.testing.assert_array_equal(a, b)
+    if w.num_layers > 1:
+        rng_ = _pools(w, w.dst_pools_numpy())
+        bad, _ = _emu_range(emu, w, src, rng_, 0, w.num_layers - 1, sms=sms)
+        assert bad == 0
+        bad, _ = _emu_range(emu, w, src, rng_, w.num_layers - 1, 1, sms=sms)
+        assert bad == 0
+        for a, b in zip(ref, rng_):
+            np.testing.assert_array_equal(a, b)
