@@ -32,6 +32,7 @@ import datetime
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -366,6 +367,25 @@ def workload_config(args, w, conv):
             "bytes_per_step": algorithmic_bytes(w, conv)}
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model, as the kernel reports it (best effort)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model name"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", text, re.M)
+        if m:
+            return m.group(1).strip()
+    part = re.search(r"^CPU part\s*:\s*(\S+)$", text, re.M)
+    impl = re.search(r"^CPU implementer\s*:\s*(\S+)$", text, re.M)
+    if part:
+        return f"{platform.machine()} (implementer {impl.group(1) if impl else '?'}, " \
+               f"part {part.group(1)})"
+    return platform.machine()
+
+
 def cpu_threads_used():
     return 1  # the oracle is a single-threaded loop nest
 
@@ -431,6 +451,17 @@ def run_ours(args):
     K = args.steps
     # whole-prompt: one launch per step
     ms_all = timed(lambda: plan.run_all(stream), K)
+    # single launches: 20 whole-prompt launches, each timed alone (median, best)
+    singles = []
+    for _ in range(20):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        plan.run_all(stream)
+        e1.record(stream)
+        e1.synchronize()
+        singles.append(e0.elapsed_time(e1))
+    launch_ms = {"median": round(statistics.median(singles), 5), "best": round(min(singles), 5),
+                 "samples": len(singles)}
     modes = set(args.modes.split(","))
     L = w.num_layers
     ms_layer = ms_graph = None
@@ -593,7 +624,7 @@ def run_ours(args):
                "sample": f"{reps} pass(es) of the oracle over the first {nl} of {L} layers of "
                          f"the same workload ({moved} bytes read+written in {sec:.1f} s), "
                          f"host copies of the same prefill pools",
-               "host_cpus": os.cpu_count()}
+               "host_cpus": os.cpu_count(), "host_cpu": host_cpu_model()}
 
     hbm_peak, peak_src = measured_hbm_peak()
     avg_launch_ms = ms_all / K
@@ -620,6 +651,7 @@ def run_ours(args):
                          "working set fits in L2 (launch-bound case)",
                    "parallelism": f"replica per GPU x{world}"},
         "ms_per_prompt": round(ms_all / K / prompts, 5),
+        "launch_ms": launch_ms,
         "pct_of_hbm_peak": round(100 * achieved / hbm_peak, 2),
         "pct_of_nominal_hbm": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "per_layer": {
@@ -688,7 +720,7 @@ def run_reference(args):
     step_ms = spent * 1e3 / args.steps
     cpu = {"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle", "cores": cpu_threads_used(),
            "sample": f"each step: the oracle over the first {n} of {w.num_layers} layers of the "
-                     f"workload (all prompts, all heads)", "host_cpus": os.cpu_count()}
+                     f"workload (all prompts, all heads)", "host_cpus": os.cpu_count(), "host_cpu": host_cpu_model()}
     out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
