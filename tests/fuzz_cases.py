@@ -9,14 +9,17 @@ import numpy as np
 import workloads as wl
 
 
-def random_workload(seed: int, max_tokens: int = 700):
+def random_workload(seed: int, max_tokens: int = 700, elem_bytes=None, head_dim_multiple=1):
+    """``elem_bytes`` fixes the element width; ``head_dim_multiple`` restricts head_dim
+    (16 for a converting relayout, whose units are 16 elements)."""
     rng = np.random.default_rng([seed, 77])
-    es = int(rng.choice([1, 2, 4]))
+    es = int(rng.choice([1, 2, 4])) if elem_bytes is None else int(elem_bytes)
     tps = [1, 2, 3, 4, 6, 8]
     H = int(rng.choice([1, 2, 4, 6, 8, 12, 16]))
     src_tp = int(rng.choice([t for t in tps if H % t == 0]))
     dst_tp = int(rng.choice([t for t in tps if H % t == 0]))
-    d_choices = [d for d in (8, 16, 24, 32, 64, 72, 128, 576) if (d * es) % 16 == 0]
+    d_choices = [d for d in (8, 16, 24, 32, 64, 72, 128, 576)
+                 if (d * es) % 16 == 0 and d % head_dim_multiple == 0]
     D = int(rng.choice(d_choices))
     C = int(rng.choice([1, 2]))
     L = int(rng.integers(1, 5))

@@ -72,9 +72,12 @@ def _run_gpu(w, src_np, dst_np, conv, mode):
     with RelayoutPlan(src, dst, convert=conv, **w.geometry()) as plan:
         if mode == "all":
             plan.run_all()
-        else:
+        elif mode == "layer":
             for layer in range(w.num_layers):
                 plan.run_layer(layer)
+        else:                                  # layer ranges
+            plan.run_layers(0, w.num_layers - 1)
+            plan.run_layers(w.num_layers - 1, 1)
         torch.cuda.synchronize()
     return [t.cpu().numpy().view(a.dtype) for t, a in zip(dst, dst_np)]
 
@@ -169,3 +172,20 @@ def test_llama70b_quantize_full_size_sampled_layers():
         torch.cuda.synchronize()
     for a, b in zip(dst, per):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzzed_conversions(seed):
+    """Random valid geometries, both directions, per-head or per-(layer, component)
+    scales, random bit patterns: every launch mode equals the converting oracle."""
+    from fuzz_cases import random_workload
+    quant = seed % 2 == 0
+    w = random_workload(seed, max_tokens=400, elem_bytes=2 if quant else 1,
+                        head_dim_multiple=16)
+    rng = np.random.default_rng(seed + 500)
+    per_head = (seed // 2) % 2
+    src_dtype, dst_dtype = (DTYPE_BF16, DTYPE_FP8_E4M3) if quant else (DTYPE_FP8_E4M3,
+                                                                        DTYPE_BF16)
+    scales = _scales(rng, w, per_head) if quant else _scales(rng, w, per_head, 0.5, 1e3)
+    modes = ("all", "layer", "ranges") if w.num_layers > 1 else ("all", "layer")
+    _check(w, _src_bits(rng, w, src_dtype), src_dtype, dst_dtype, per_head, scales, modes)
