@@ -464,7 +464,7 @@ def run_ours(args):
                  "samples": len(singles)}
     modes = set(args.modes.split(","))
     L = w.num_layers
-    ms_layer = ms_graph = None
+    ms_layer = ms_graph = ms_graph_nw = None
     k_layer = max(1, K // 4)
     if "layer" in modes:
         # per-layer, eager: L launches per step from Python
@@ -482,6 +482,18 @@ def run_ours(args):
                 plan.run_layer(layer)
         stream.wait_stream(cap)
         ms_graph = timed(g.replay, K)
+        del g
+        # the same launches where each but the first passes KVR_LAUNCH_NO_WAIT: they
+        # follow another hand-off launch and their layers are ready before it (all are)
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for layer in range(L):
+                plan.run_layers(layer, 1, wait_for_previous=layer == 0)
+        stream.wait_stream(cap)
+        ms_graph_nw = timed(g.replay, K)
+        del g
     layer_groups = None
     if "groups" in modes:
         # layer groups: ceil(L / n) launches of n layers each (kv_relayout_layers), the
@@ -665,6 +677,13 @@ def run_ours(args):
                 "ms_per_prompt": round(ms_graph / K / prompts, 5),
                 "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
                 "launches_per_step": L, "steps": K},
+            "cuda_graph_no_wait": None if ms_graph_nw is None else {
+                "gbs": round(whole_job_gbs(bytes_step, K, world, ms_graph_nw * 1e-3), 2),
+                "ms_per_prompt": round(ms_graph_nw / K / prompts, 5),
+                "us_per_launch": round(ms_graph_nw * 1e3 / K / L, 3),
+                "launches_per_step": L, "steps": K,
+                "what": "launches 2..L pass KVR_LAUNCH_NO_WAIT (each follows another "
+                        "hand-off launch; every layer is ready before the first)"},
         },
         "layer_groups": layer_groups,
         "gpu_launches": K,

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
     // Wait for the grid this launch follows in its stream before touching any
     // pool, then let the next launch start early (programmatic dependent
     // launch; both are no-ops without it). Per-layer launches wait later.
-    if (!EARLY) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!EARLY && !a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
     int32_t layer;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
     kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
     if (q0 >= q1) {
         // a CTA without rows still orders itself after the previous grid
-        if (EARLY) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (EARLY && !a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
     const uint32_t rc = (uint32_t)a.g.row_chunks;
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
             if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
         }
         if (EARLY && !waited) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
             waited = true;
         }
         __syncthreads();
@@ -249,13 +249,13 @@ KvrKernel pick_kernel(int32_t conv, bool per_layer) {
 }
 
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
-                  bool per_layer, void *stream) {
+                  bool per_layer, void *stream, bool no_wait = false) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
-    const KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt,
-                                      p->dev_factors, p->dev_src_base, p->dev_dst_base,
-                                      layer0, slices);
+    KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt, p->dev_factors,
+                                p->dev_src_base, p->dev_dst_base, layer0, slices);
+    a.no_wait = no_wait ? 1 : 0;
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
 
@@ -453,16 +453,22 @@ extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
     return launch(plan, 0, plan->host.num_layers, slices, false, stream);
 }
 
-extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
-                                         void *stream) {
-    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+extern "C" kvr_status kv_relayout_layers_ex(const kvr_plan *plan, int32_t first, int32_t count,
+                                            uint32_t flags, void *stream) {
+    if (plan == nullptr || (flags & ~KVR_LAUNCH_NO_WAIT) != 0) return KVR_ERR_INVALID_ARG;
     const int32_t L = plan->host.num_layers;
     if (first < 0 || count < 1 || first >= L || count > L - first) return KVR_ERR_LAYER_RANGE;
     int32_t slices = 1;
     bool per_layer = true;
     kvr_range_launch(plan->host, count, count > 1 ? kvr_stream_green_sms(stream) : 0, &slices,
                      &per_layer);
-    return launch(plan, first, count, slices, per_layer, stream);
+    return launch(plan, first, count, slices, per_layer, stream,
+                  (flags & KVR_LAUNCH_NO_WAIT) != 0);
+}
+
+extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
+                                         void *stream) {
+    return kv_relayout_layers_ex(plan, first, count, 0u, stream);
 }
 
 extern "C" kvr_status kv_relayout_plan_bytes(const kvr_plan *plan, int64_t *bytes_read,

@@ -29,9 +29,10 @@ EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
            "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
            "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy",
-           "kv_relayout_plan_launch_shape", "kv_relayout_layers")
+           "kv_relayout_plan_launch_shape", "kv_relayout_layers", "kv_relayout_layers_ex")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
+LAUNCH_NO_WAIT = 1
 
 
 class KVRelayoutError(RuntimeError):
@@ -111,6 +112,8 @@ def library() -> ctypes.CDLL:
         lib.kv_relayout_plan_launch_shape.argtypes = [p, p, p, p]
         lib.kv_relayout_layers.restype = i32
         lib.kv_relayout_layers.argtypes = [p, i32, i32, p]
+        lib.kv_relayout_layers_ex.restype = i32
+        lib.kv_relayout_layers_ex.argtypes = [p, i32, i32, ctypes.c_uint32, p]
         _lib = lib
     return _lib
 
@@ -405,11 +408,15 @@ class RelayoutPlan:
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_layer")
 
-    def run_layers(self, first: int, count: int, stream=None):
+    def run_layers(self, first: int, count: int, stream=None, wait_for_previous=True):
         """Layers [first, first + count), one launch on ``stream`` (default: torch's
-        current stream)."""
-        st = library().kv_relayout_layers(self._handle(), int(first), int(count),
-                                          _stream_handle(stream))
+        current stream). ``wait_for_previous=False`` passes KVR_LAUNCH_NO_WAIT: only
+        when the work just before this launch on the stream is another hand-off launch
+        and everything this launch reads and writes was ready before that one was made
+        (see ``kv_relayout_layers_ex`` in the C header)."""
+        flags = 0 if wait_for_previous else LAUNCH_NO_WAIT
+        st = library().kv_relayout_layers_ex(self._handle(), int(first), int(count), flags,
+                                             _stream_handle(stream))
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_layers")
 

@@ -247,3 +247,40 @@ def test_layer_range_errors_are_statuses():
             assert e.value.name == "KVR_ERR_LAYER_RANGE"
         plan.run_layers(0, 4)
         torch.cuda.synchronize()
+
+
+def test_no_wait_launches_after_hand_off_launches():
+    """Back-to-back single-layer launches where every launch but the first passes
+    KVR_LAUNCH_NO_WAIT (each follows another hand-off launch of the same plan; all
+    prefill rows were ready before the first): same bytes as one whole launch,
+    eager and captured in a CUDA graph."""
+    import torch
+    w = wl.custom("nw", 13, num_layers=6, num_components=2, kv_heads=8, head_dim=128,
+                  elem_bytes=2, src_tp=4, dst_tp=8, src_block=16, dst_block=32,
+                  seq_lens=[1500, 77, 640])
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, 2)
+    ref = _ref(w, src_np)
+    for graph in (False, True):
+        dst = to_device(w.dst_pools_numpy(), 2)
+        with RelayoutPlan(src, dst, **w.geometry()) as plan:
+            def launches():
+                for layer in range(w.num_layers):
+                    plan.run_layers(layer, 1, wait_for_previous=layer == 0)
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream()
+                cap.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.graph(g, stream=cap):
+                    launches()
+                torch.cuda.current_stream().wait_stream(cap)
+                g.replay()
+            else:
+                launches()
+            torch.cuda.synchronize()
+        for a, b in zip(ref, to_host(dst, w)):
+            np.testing.assert_array_equal(b, a)
+    with RelayoutPlan(src, to_device(w.dst_pools_numpy(), 2), **w.geometry()) as plan:
+        st = plan._handle()
+        from prefill_decode_paged_gb300.kv_relayout import library
+        assert library().kv_relayout_layers_ex(st, 0, 1, 2, None) == -1   # unknown flag
