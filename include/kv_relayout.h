@@ -241,9 +241,12 @@ kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count
  * the kernel may start early (programmatic dependent launch) and build its
  * work tables, but it waits for that kernel to finish before it touches a
  * pool, which is what orders a hand-off after the kernel that wrote its
- * prefill rows. KVR_LAUNCH_NO_WAIT drops that wait, so back-to-back
- * hand-off launches stream into each other instead of draining between
- * launches (on the 70B workload, 80 single-layer launches: 5.3 -> 6.9 TB/s).
+ * prefill rows. KVR_LAUNCH_NO_WAIT moves that wait to the end of the launch,
+ * after its copies: the launch reads and writes the pools while the kernel
+ * before it may still run, and still completes only after that kernel (work
+ * queued after it on the stream sees both), so back-to-back hand-off
+ * launches stream into each other instead of draining between launches (on
+ * the 70B workload, 80 single-layer launches: 5.3 -> 6.7 TB/s).
  * Pass it only when the work just before this launch on `stream` is another
  * hand-off launch (of this plan, or of a plan whose decode views do not meet
  * this one's) and every prefill row this launch reads, and every decode block

@@ -100,7 +100,8 @@ struct KvrArgs {
     const uint64_t *dst_base;           // [Td][L][C] addresses of the decode views
     int32_t layer0;                     // first layer of this launch
     int32_t slices;                     // tasks per item
-    int32_t no_wait;                    // 1: do not wait for the previous grid (caller's call)
+    int32_t no_wait;                    // 1: wait for the previous grid after the copies, not
+                                        // before them (the caller's call)
     uint32_t tasks_per_layer;           // n_items * slices
     KvrDiv div_tasks_per_layer, div_slices;
 };

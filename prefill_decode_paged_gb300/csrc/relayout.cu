@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(KVR_THREADS)
     uint32_t q0, q1;
     kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
     if (q0 >= q1) {
-        // a CTA without rows still orders itself after the previous grid
-        if (EARLY && !a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+        // a CTA without rows still orders itself after the previous grid (and a
+        // launch without the early wait still completes after it)
+        if (EARLY || a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
     const uint32_t rc = (uint32_t)a.g.row_chunks;
@@ -226,6 +227,9 @@ __global__ void __launch_bounds__(KVR_THREADS)
         }
         __syncthreads();
     }
+    // A launch that skipped the wait before its copies still finishes only after
+    // the previous grid, so work queued after it on the stream sees both.
+    if (a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 using KvrKernel = void (*)(KvrArgs);

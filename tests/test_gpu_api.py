@@ -277,9 +277,13 @@ def test_no_wait_launches_after_hand_off_launches():
                 g.replay()
             else:
                 launches()
+            # work queued right after the chain on the same stream sees every launch's
+            # writes: the copies below run before any host synchronization
+            snap = [t.clone() for t in dst]
             torch.cuda.synchronize()
-        for a, b in zip(ref, to_host(dst, w)):
+        for a, b, c in zip(ref, to_host(dst, w), to_host(snap, w)):
             np.testing.assert_array_equal(b, a)
+            np.testing.assert_array_equal(c, a)
     with RelayoutPlan(src, to_device(w.dst_pools_numpy(), 2), **w.geometry()) as plan:
         st = plan._handle()
         from prefill_decode_paged_gb300.kv_relayout import library
