@@ -249,11 +249,13 @@ kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count
  * the 70B workload, 80 single-layer launches: 5.3 -> 6.7 TB/s).
  * Pass it only when the work just before this launch on `stream` is another
  * hand-off launch (of this plan, or of a plan whose decode views do not meet
- * this one's) and every prefill row this launch reads, and every decode block
- * it writes, was ready before that launch was made (for example the layers
- * that are already computed, handed over one launch each on a stream that
- * carries only the hand-off). A launch right after any other kernel or copy
- * must not pass it.
+ * this one's), and every prefill row this launch reads and every decode block
+ * it writes was last written by work queued on `stream` before the latest
+ * hand-off launch made without the flag (such a launch lets later launches
+ * start only after it has waited for everything before it). For example: the
+ * layers that are already computed, handed over one launch each, the first
+ * without the flag. A launch right after any other kernel or copy must not
+ * pass it.
  */
 kvr_status kv_relayout_layers_ex(const kvr_plan *plan, int32_t first, int32_t count,
                                  uint32_t flags, void *stream);

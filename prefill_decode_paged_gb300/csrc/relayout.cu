@@ -152,9 +152,12 @@ __global__ void __launch_bounds__(KVR_THREADS)
 
     // Wait for the grid this launch follows in its stream before touching any
     // pool, then let the next launch start early (programmatic dependent
-    // launch; both are no-ops without it). Per-layer launches wait later.
+    // launch; both are no-ops without it). Per-layer launches wait later, and
+    // let the next launch start only once they have waited: a launch that does
+    // not wait first (no_wait) may only begin after everything queued before
+    // the last launch that did wait has finished.
     if (!EARLY && !a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
+    if (!EARLY || a.no_wait) asm volatile("griddepcontrol.launch_dependents;");
 
     int32_t layer;
     KvrItem it;
@@ -184,7 +187,10 @@ __global__ void __launch_bounds__(KVR_THREADS)
             if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
         }
         if (EARLY && !waited) {
-            if (!a.no_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!a.no_wait) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                asm volatile("griddepcontrol.launch_dependents;");
+            }
             waited = true;
         }
         __syncthreads();

@@ -412,8 +412,9 @@ class RelayoutPlan:
         """Layers [first, first + count), one launch on ``stream`` (default: torch's
         current stream). ``wait_for_previous=False`` passes KVR_LAUNCH_NO_WAIT: only
         when the work just before this launch on the stream is another hand-off launch
-        and everything this launch reads and writes was ready before that one was made
-        (see ``kv_relayout_layers_ex`` in the C header)."""
+        and everything this launch reads and writes was written by work queued before
+        the latest hand-off launch made with ``wait_for_previous=True`` (see
+        ``kv_relayout_layers_ex`` in the C header)."""
         flags = 0 if wait_for_previous else LAUNCH_NO_WAIT
         st = library().kv_relayout_layers_ex(self._handle(), int(first), int(count), flags,
                                              _stream_handle(stream))
