@@ -307,34 +307,38 @@ def conversion(args, w):
     return fp8, w, dict(src_dtype=E4M3, dst_dtype=BF16, per_head=True, scales=scales)
 
 
-def host_link_ceiling(torch, dev, read_bytes, write_bytes, steps):
-    """What the host link itself gives for one step's traffic: pinned host -> HBM
-    copy of the bytes the step reads, concurrently with an HBM -> pinned host copy
-    of the bytes it writes (cudaMemcpyAsync on two streams; wall clock)."""
-    h_in = torch.empty(read_bytes, dtype=torch.uint8, pin_memory=True)
-    h_out = torch.empty(write_bytes, dtype=torch.uint8, pin_memory=True)
-    d_in = torch.empty(read_bytes, dtype=torch.uint8, device=dev)
-    d_out = torch.zeros(write_bytes, dtype=torch.uint8, device=dev)
-    h_in.fill_(1)
+def host_link_ceiling(torch, dev, pairs_in, pairs_out, steps):
+    """What the host link gives on the e2e measurement's own pinned buffers: every
+    (pinned host, device) pair of ``pairs_in`` copied host -> HBM concurrently with
+    every (device, pinned host) pair of ``pairs_out`` copied HBM -> host
+    (cudaMemcpyAsync on two streams; wall clock; bytes of both directions)."""
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    moved = sum(h.numel() * h.element_size() for h, _ in pairs_in) + \
+        sum(h.numel() * h.element_size() for _, h in pairs_out)
 
     def once():
         with torch.cuda.stream(up):
-            d_in.copy_(h_in, non_blocking=True)
+            for h, d in pairs_in:
+                d.copy_(h, non_blocking=True)
         with torch.cuda.stream(down):
-            h_out.copy_(d_out, non_blocking=True)
+            for d, h in pairs_out:
+                h.copy_(d, non_blocking=True)
     for _ in range(3):
         once()
     torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        once()
-    torch.cuda.synchronize(dev)
-    sec = (time.perf_counter() - t0) / steps
-    return {"gbs": round((read_bytes + write_bytes) / sec / 1e9, 2),
-            "ms_per_step": round(sec * 1e3, 4),
-            "what": "pinned host -> HBM copy of the bytes a step reads, concurrent with an "
-                    "HBM -> pinned host copy of the bytes it writes (cudaMemcpyAsync, two "
+    rounds = []
+    for _ in range(5):      # the copy engines' rate varies between rounds: keep the best
+        t0 = time.perf_counter()
+        for _ in range(max(1, steps // 2)):
+            once()
+        torch.cuda.synchronize(dev)
+        rounds.append((time.perf_counter() - t0) / max(1, steps // 2))
+    sec = min(rounds)
+    return {"gbs": round(moved / sec / 1e9, 2), "ms_per_step": round(sec * 1e3, 4),
+            "gbs_median": round(moved / statistics.median(rounds) / 1e9, 2),
+            "rounds": len(rounds), "bytes_per_step": int(moved),
+            "what": "the e2e measurement's pinned pools: every prefill pool host -> HBM "
+                    "concurrent with every decode pool HBM -> host (cudaMemcpyAsync, two "
                     "streams)"}
 
 
@@ -596,8 +600,8 @@ def run_ours(args):
         for h, t in zip(h_dst, dst):
             if not torch.equal(h.to(dev), t):
                 raise SystemExit("bench.py: host-pool relayout differs from the HBM one")
-        e2e["link_ceiling"] = host_link_ceiling(torch, dev, plan.bytes_read,
-                                                plan.bytes_written, args.e2e_steps)
+        e2e["link_ceiling"] = host_link_ceiling(torch, dev, list(zip(h_src, src)),
+                                                list(zip(dst, h_dst)), args.e2e_steps)
         e2e["frac_of_link"] = round(e2e["value"] / e2e["link_ceiling"]["gbs"], 4)
 
         def staged_step():
