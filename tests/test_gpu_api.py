@@ -288,3 +288,15 @@ def test_no_wait_launches_after_hand_off_launches():
         st = plan._handle()
         from prefill_decode_paged_gb300.kv_relayout import library
         assert library().kv_relayout_layers_ex(st, 0, 1, 2, None) == -1   # unknown flag
+
+
+def test_plain_c_client_on_the_gpu():
+    """A C99 program (kv_relayout.h, cudaMalloc, no Python in the loop) plans and runs
+    whole-prompt, per-layer and layer-range launches; every decode byte matches the
+    C oracle."""
+    import subprocess
+    from test_host_abi import build_abi_client
+    exe = build_abi_client()
+    out = subprocess.run([exe, "gpu"], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert "gpu: ok" in out.stdout

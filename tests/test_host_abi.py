@@ -465,3 +465,39 @@ def test_fuzzed_geometries_on_the_emulated_kernel(emu, seed):
         assert bad == 0
         for a, b in zip(ref, rng_):
             np.testing.assert_array_equal(a, b)
+
+
+ABI_CLIENT_SRC = os.path.join(ROOT, "tests", "csrc", "abi_client.c")
+ABI_CLIENT = os.path.join(ROOT, "tests", "_build", "abi_client")
+
+
+def build_abi_client():
+    """gcc -std=c99 against the C header alone, linked to the library and the oracle."""
+    kbuild.build()
+    oracle.build()
+    cuda = os.path.dirname(os.path.dirname(kbuild.nvcc_path()))
+    lib_dir = os.path.dirname(kr.LIB_PATH)
+    ora = oracle.build()
+    os.makedirs(os.path.dirname(ABI_CLIENT), exist_ok=True)
+    cuda_lib = next(d for d in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib"))
+                    if os.path.isdir(d))
+    # the header on its own is strict ISO C99 (the CUDA runtime header the client
+    # also includes is not, so the client itself is built without -pedantic)
+    subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-fsyntax-only", "-x", "c", "-I", kbuild.INCLUDE, "-"],
+                   input='#include "kv_relayout.h"\n', text=True, check=True)
+    cmd = ["gcc", "-std=c99", "-O1", "-Wall", "-Wextra", "-Werror",
+           "-I", kbuild.INCLUDE, "-I", os.path.join(cuda, "include"), ABI_CLIENT_SRC,
+           kr.LIB_PATH, ora, "-L", cuda_lib, "-lcudart",
+           f"-Wl,-rpath,{lib_dir}:{os.path.dirname(ora)}:{cuda_lib}", "-o", ABI_CLIENT]
+    subprocess.run(cmd, check=True)
+    return ABI_CLIENT
+
+
+def test_plain_c_client_validates_on_the_host():
+    """A C99 program that includes only kv_relayout.h: byte counts and the documented
+    error statuses, on fake pool addresses (no GPU call)."""
+    exe = build_abi_client()
+    out = subprocess.run([exe, "host"], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "host: ok" in out.stdout
