@@ -526,10 +526,15 @@ def run_ours(args):
     # the whole-prompt relayout on streams limited to a number of SMs
     sm_sweep = None
     if args.sm_sweep:
-        from prefill_decode_paged_gb300 import SmStream
+        from prefill_decode_paged_gb300 import KVRelayoutError, SmStream
         sm_sweep = {}
         for want in [int(x) for x in args.sm_sweep.split(",") if x]:
-            with SmStream(want) as sms:
+            try:
+                sms = SmStream(want)
+            except KVRelayoutError as e:      # no green contexts here: say so, go on
+                sm_sweep[str(want)] = {"unavailable": e.name}
+                continue
+            with sms:
                 ext = torch.cuda.ExternalStream(sms.handle, device=dev)
                 steps = max(1, K // 4)
                 for _ in range(3):
