@@ -25,7 +25,12 @@
  * Readings taken where the page is silent (each is listed in the design doc):
  *   - pool layout, one buffer per TP shard: [L][C][N][B][H_local][D] of
  *     es-byte elements (C = 2 for K and V, C = 1 for an MLA latent);
- *   - TP shard s holds the contiguous head range [s*H/T, (s+1)*H/T);
+ *   - TP shard s holds the contiguous head range [s*H/T, (s+1)*H/T) when
+ *     T <= H (H_local = H/T); when T > H (more cards than KV heads, e.g. an
+ *     MLA latent under TP) each head is held whole by T/H consecutive cards,
+ *     shards h*T/H .. (h+1)*T/H - 1 (H_local = 1), and the hand-off reads a
+ *     head from the first prefill card that holds it and writes it to every
+ *     decode card that holds it;
  *   - one block table per side, shared by all shards of that side;
  *   - elements are copied as es raw bytes: no conversion, NaN payloads kept.
  *
@@ -34,6 +39,24 @@
  */
 #include <stdint.h>
 #include <stddef.h>
+
+/* A TP degree a side can have for H KV heads: a divisor of H (each card a
+ * head range) or a multiple of it (each head on T/H cards). */
+static int tp_ok(int64_t kv_heads, int64_t tp)
+{
+    return tp >= 1 && kv_heads >= 1 && (kv_heads % tp == 0 || tp % kv_heads == 0);
+}
+
+/* Heads on one card, and cards that hold one head. */
+static int64_t heads_per_card(int64_t kv_heads, int64_t tp)
+{
+    return tp <= kv_heads ? kv_heads / tp : 1;
+}
+
+static int64_t cards_per_head(int64_t kv_heads, int64_t tp)
+{
+    return tp <= kv_heads ? 1 : tp / kv_heads;
+}
 
 /* Bytes of KV cache one token occupies, summed over layers, components,
  * heads and head dimension ("KV/token", section "传输的代价"). */
@@ -69,7 +92,8 @@ int64_t kvo_transfer_bytes(int32_t num_layers, int32_t num_components,
  * Request r owns src_bt[src_off[r] ...] and dst_bt[dst_off[r] ...]; entry k
  * of a table is the physical block that holds tokens [k*B, (k+1)*B).
  *
- * Returns 0, or -1 when the head count is not divisible by a TP degree.
+ * Returns 0, or -1 when a TP degree neither divides the head count nor is a
+ * multiple of it.
  */
 int kvo_relayout(int32_t layer_begin, int32_t layer_end,
                  int32_t num_layers, int32_t num_components,
@@ -82,11 +106,13 @@ int kvo_relayout(int32_t layer_begin, int32_t layer_end,
                  const int64_t *src_off, const int32_t *src_bt,
                  const int64_t *dst_off, const int32_t *dst_bt)
 {
-    if (kv_heads % src_tp != 0 || kv_heads % dst_tp != 0)
+    if (!tp_ok(kv_heads, src_tp) || !tp_ok(kv_heads, dst_tp))
         return -1;
     (void)num_layers;
-    const int64_t src_heads = kv_heads / src_tp; /* heads per prefill card */
-    const int64_t dst_heads = kv_heads / dst_tp; /* heads per decode card */
+    const int64_t src_heads = heads_per_card(kv_heads, src_tp); /* heads per prefill card */
+    const int64_t dst_heads = heads_per_card(kv_heads, dst_tp); /* heads per decode card */
+    const int64_t src_copies = cards_per_head(kv_heads, src_tp);
+    const int64_t dst_copies = cards_per_head(kv_heads, dst_tp);
     const int64_t C = num_components;
     const int64_t D = head_dim;
 
@@ -101,12 +127,13 @@ int kvo_relayout(int32_t layer_begin, int32_t layer_end,
                     /* decode side: slot = block_ids[t // Bd] * Bd + t % Bd */
                     const int64_t dblk = dst_bt[dst_off[r] + t / dst_block];
                     const int64_t doff = t % dst_block;
-                    for (int64_t h = 0; h < kv_heads; ++h) {
-                        /* head h lives on prefill card h / (H/Tp) ... */
-                        const int64_t sp = h / src_heads;
+                    for (int64_t h = 0; h < kv_heads; ++h)
+                    for (int64_t k = 0; k < dst_copies; ++k) {
+                        /* head h is read from the first prefill card holding it ... */
+                        const int64_t sp = (h / src_heads) * src_copies;
                         const int64_t sh = h % src_heads;
-                        /* ... and goes to decode card h / (H/Td) */
-                        const int64_t dp = h / dst_heads;
+                        /* ... and goes to the k-th decode card holding it */
+                        const int64_t dp = (h / dst_heads) * dst_copies + k;
                         const int64_t dh = h % dst_heads;
                         for (int64_t e = 0; e < D; ++e) {
                             const int64_t s_elem =
@@ -253,7 +280,7 @@ int kvo_relayout_convert(int32_t layer_begin, int32_t layer_end,
                          const int64_t *src_off, const int32_t *src_bt,
                          const int64_t *dst_off, const int32_t *dst_bt)
 {
-    if (kv_heads % src_tp != 0 || kv_heads % dst_tp != 0)
+    if (!tp_ok(kv_heads, src_tp) || !tp_ok(kv_heads, dst_tp))
         return -1;
     if (!((src_dtype == KVO_BF16 && dst_dtype == KVO_E4M3) ||
           (src_dtype == KVO_E4M3 && dst_dtype == KVO_BF16)))
@@ -261,8 +288,10 @@ int kvo_relayout_convert(int32_t layer_begin, int32_t layer_end,
     (void)num_layers;
     const int64_t src_es = src_dtype == KVO_BF16 ? 2 : 1;
     const int64_t dst_es = dst_dtype == KVO_BF16 ? 2 : 1;
-    const int64_t src_heads = kv_heads / src_tp;
-    const int64_t dst_heads = kv_heads / dst_tp;
+    const int64_t src_heads = heads_per_card(kv_heads, src_tp);
+    const int64_t dst_heads = heads_per_card(kv_heads, dst_tp);
+    const int64_t src_copies = cards_per_head(kv_heads, src_tp);
+    const int64_t dst_copies = cards_per_head(kv_heads, dst_tp);
     const int64_t C = num_components;
     const int64_t D = head_dim;
 
@@ -275,10 +304,11 @@ int kvo_relayout_convert(int32_t layer_begin, int32_t layer_end,
                     const int64_t soff = t % src_block;
                     const int64_t dblk = dst_bt[dst_off[r] + t / dst_block];
                     const int64_t doff = t % dst_block;
-                    for (int64_t h = 0; h < kv_heads; ++h) {
-                        const int64_t sp = h / src_heads;
+                    for (int64_t h = 0; h < kv_heads; ++h)
+                    for (int64_t k = 0; k < dst_copies; ++k) {
+                        const int64_t sp = (h / src_heads) * src_copies;
                         const int64_t sh = h % src_heads;
-                        const int64_t dp = h / dst_heads;
+                        const int64_t dp = (h / dst_heads) * dst_copies + k;
                         const int64_t dh = h % dst_heads;
                         const float s = per_head ? scales[(l * C + c) * kv_heads + h]
                                                  : scales[l * C + c];
@@ -399,7 +429,7 @@ int kvo_relayout_general(int32_t layer_begin, int32_t layer_end,
                          const int64_t *src_off, const int32_t *src_bt,
                          const int64_t *dst_off, const int32_t *dst_bt)
 {
-    if (kv_heads % src_tp != 0 || kv_heads % dst_tp != 0)
+    if (!tp_ok(kv_heads, src_tp) || !tp_ok(kv_heads, dst_tp))
         return -1;
     const int converting = src_dtype != 0;
     if (converting && !((src_dtype == KVO_BF16 && dst_dtype == KVO_E4M3) ||
@@ -409,8 +439,10 @@ int kvo_relayout_general(int32_t layer_begin, int32_t layer_end,
         return -1;
     const int64_t src_es = !converting ? elem_bytes : (src_dtype == KVO_BF16 ? 2 : 1);
     const int64_t dst_es = !converting ? elem_bytes : (dst_dtype == KVO_BF16 ? 2 : 1);
-    const int64_t src_heads = kv_heads / src_tp;
-    const int64_t dst_heads = kv_heads / dst_tp;
+    const int64_t src_heads = heads_per_card(kv_heads, src_tp);
+    const int64_t dst_heads = heads_per_card(kv_heads, dst_tp);
+    const int64_t src_copies = cards_per_head(kv_heads, src_tp);
+    const int64_t dst_copies = cards_per_head(kv_heads, dst_tp);
     const int64_t C = num_components;
     const int64_t L = num_layers;
 
@@ -423,10 +455,11 @@ int kvo_relayout_general(int32_t layer_begin, int32_t layer_end,
                     const int64_t soff = t % src_block;
                     const int64_t dblk = dst_bt[dst_off[r] + t / dst_block];
                     const int64_t doff = t % dst_block;
-                    for (int64_t h = 0; h < kv_heads; ++h) {
-                        const int64_t sp = h / src_heads;
+                    for (int64_t h = 0; h < kv_heads; ++h)
+                    for (int64_t k = 0; k < dst_copies; ++k) {
+                        const int64_t sp = (h / src_heads) * src_copies;
                         const int64_t sh = h % src_heads;
-                        const int64_t dp = h / dst_heads;
+                        const int64_t dp = (h / dst_heads) * dst_copies + k;
                         const int64_t dh = h % dst_heads;
                         const uint8_t *src_row = (const uint8_t *)(uintptr_t)
                             src_base[(sp * L + l) * C + c] + sblk * s_block_stride +

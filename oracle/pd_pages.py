@@ -10,7 +10,9 @@ computes one slot per prompt position from its own block table and writes the
 gathered rows there. Section "布局转换" adds the TP difference: each side
 keeps 1/T of the KV heads per card, so the gathered array is the prefill
 cards' head ranges put side by side, and the decode side takes its own head
-range out of it.
+range out of it. With more cards than heads (the reading taken for T > H),
+T/H consecutive cards hold the same head: the gather takes each head from the
+first card of its group, and every card of a decode group receives its head.
 
 Unlike the C loop nest, the gather here reads whole physical blocks (a
 request's tokens are its blocks laid end to end in table order) and the
@@ -29,9 +31,12 @@ def _shard_view(pool, num_layers, num_components, num_blocks, block, heads, head
 def gather_prefill(src_pools, layer, comp, block_ids, n, *, num_layers, num_components,
                    kv_heads, head_dim, src_tp, src_block, src_num_blocks):
     """pd.py ``prefill()`` gather of one layer/component: -> [n, kv_heads, head_dim]."""
-    hp = kv_heads // src_tp
+    hp = kv_heads // src_tp if src_tp <= kv_heads else 1
+    group = src_tp // kv_heads if src_tp > kv_heads else 1      # cards holding one head
     per_card = []
-    for pool in src_pools:
+    for card, pool in enumerate(src_pools):
+        if card % group:
+            continue                       # a further copy of a head already gathered
         v = _shard_view(pool, num_layers, num_components, src_num_blocks, src_block, hp,
                         head_dim)
         blocks = v[layer, comp][np.asarray(block_ids, dtype=np.int64)]   # [nb, Bp, hp, D]
@@ -43,14 +48,16 @@ def admit_decode(dst_pools, layer, comp, block_ids, rows, *, num_layers, num_com
                  kv_heads, head_dim, dst_tp, dst_block, dst_num_blocks):
     """pd.py ``admit()`` write of one layer/component from gathered ``rows``."""
     n = rows.shape[0]
-    hd = kv_heads // dst_tp
+    hd = kv_heads // dst_tp if dst_tp <= kv_heads else 1
+    group = dst_tp // kv_heads if dst_tp > kv_heads else 1
     slots = np.array([block_ids[p // dst_block] * dst_block + p % dst_block
                       for p in range(n)], dtype=np.int64)
     for card, pool in enumerate(dst_pools):
         v = _shard_view(pool, num_layers, num_components, dst_num_blocks, dst_block, hd,
                         head_dim)
         flat = v[layer, comp].reshape(dst_num_blocks * dst_block, hd, head_dim)
-        flat[slots] = rows[:, card * hd:(card + 1) * hd, :]
+        first = (card // group) * hd         # the card's first head
+        flat[slots] = rows[:, first:first + hd, :]
 
 
 def relayout(src_pools, dst_pools, *, num_layers, num_components, kv_heads, head_dim,

@@ -2,7 +2,9 @@
 
 A request's KV, for one layer and component, is its physical blocks laid end
 to end in table order, cut at the prompt length; the TP shards of one side
-hold consecutive head ranges, laid side by side along the head axis. These
+hold consecutive head ranges, laid side by side along the head axis (with more
+shards than heads, each group of T/H consecutive shards holds one head: any
+one of them, ``replica``, gives that head's rows). These
 helpers use only that meaning (numpy reshapes and fancy indexing over whole
 blocks), never the per-token slot arithmetic, so they can judge both the
 oracle and the CUDA path without repeating either's index expressions.
@@ -12,25 +14,36 @@ from __future__ import annotations
 import numpy as np
 
 
-def request_rows(pools, shape, layer, comp, ids, n):
-    """Tokens [0, n) of one request as [n, H, D] (shards side by side)."""
+def copies(pools, kv_heads):
+    """Shards that hold one head (1 unless a side has more shards than heads)."""
+    if kv_heads is None or len(pools) <= kv_heads:
+        return 1
+    return len(pools) // kv_heads
+
+
+def request_rows(pools, shape, layer, comp, ids, n, kv_heads=None, replica=0):
+    """Tokens [0, n) of one request as [n, H, D] (shards side by side; of each group
+    of shards holding the same head, the ``replica``-th)."""
     L, C, N, B, Hl, D = shape
     parts = []
-    for pool in pools:
+    for pool in pools[replica::copies(pools, kv_heads)]:
         v = pool.reshape(shape)
         parts.append(v[layer, comp][np.asarray(ids, dtype=np.int64)].reshape(-1, Hl, D)[:n])
     return np.concatenate(parts, axis=1)
 
 
-def write_request_rows(pools, shape, layer, comp, ids, rows):
-    """Inverse of :func:`request_rows`: put [n, H, D] rows into the request's blocks."""
+def write_request_rows(pools, shape, layer, comp, ids, rows, kv_heads=None):
+    """Inverse of :func:`request_rows`: put [n, H, D] rows into the request's blocks
+    (every shard of a group holding the same head gets it)."""
     L, C, N, B, Hl, D = shape
     ids = np.asarray(ids, dtype=np.int64)
     n = rows.shape[0]
+    g = copies(pools, kv_heads)
     for s, pool in enumerate(pools):
         v = pool.reshape(shape)
         buf = v[layer, comp][ids].reshape(len(ids) * B, Hl, D)
-        buf[:n] = rows[:, s * Hl:(s + 1) * Hl]
+        first = (s // g) * Hl
+        buf[:n] = rows[:, first:first + Hl]
         v[layer, comp][ids] = buf.reshape(len(ids), B, Hl, D)
 
 
@@ -85,7 +98,8 @@ def tagged_src(w, poison):
             continue
         for l in range(w.num_layers):
             for c in range(w.num_components):
-                write_request_rows(pools, w.src_shape(), l, c, src_ids(w, r), tags[l, c])
+                write_request_rows(pools, w.src_shape(), l, c, src_ids(w, r), tags[l, c],
+                                   w.kv_heads)
     return pools, expected
 
 
@@ -99,7 +113,8 @@ def expected_from_src(w, src_pools, layers=None):
         if n:
             for l in layers:
                 for c in range(w.num_components):
-                    rows[l, c] = request_rows(src_pools, w.src_shape(), l, c, src_ids(w, r), n)
+                    rows[l, c] = request_rows(src_pools, w.src_shape(), l, c, src_ids(w, r), n,
+                                              w.kv_heads)
         out.append(rows)
     return out
 
@@ -112,9 +127,12 @@ def check_dst(w, dst_pools, expected, sentinel, layers=None):
             continue
         for l in layers:
             for c in range(w.num_components):
-                got = request_rows(dst_pools, w.dst_shape(), l, c, dst_ids(w, r), n)
-                np.testing.assert_array_equal(got, expected[r][l, c],
-                                              err_msg=f"request {r} layer {l} comp {c}")
+                for k in range(copies(dst_pools, w.kv_heads)):
+                    got = request_rows(dst_pools, w.dst_shape(), l, c, dst_ids(w, r), n,
+                                       w.kv_heads, replica=k)
+                    np.testing.assert_array_equal(
+                        got, expected[r][l, c], err_msg=f"request {r} layer {l} comp {c} "
+                                                        f"copy {k}")
     slot = covered_mask(w.dst_shape(), w.dst_off, w.dst_bt, w.seq_lens)
     cover = full_mask(w.dst_shape(), slot)
     for pool in dst_pools:

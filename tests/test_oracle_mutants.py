@@ -19,8 +19,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "kv_oracle.c")
 
 MUTANTS = {
-    "src_shard_by_dst_heads": ("const int64_t sp = h / src_heads;",
-                               "const int64_t sp = h / dst_heads;"),
+    "src_shard_by_dst_heads": ("const int64_t sp = (h / src_heads) * src_copies;",
+                               "const int64_t sp = (h / dst_heads) * src_copies;"),
     "dst_local_head_by_src_heads": ("const int64_t dh = h % dst_heads;",
                                     "const int64_t dh = h % src_heads;"),
     "src_table_index_by_dst_block": ("src_bt[src_off[r] + t / src_block]",
@@ -104,6 +104,39 @@ LAYOUT_BATTERY = textwrap.dedent("""
     P.test_standard_views_reduce_to_the_converting_oracle(lib, "dequant")
 """)
 
+REPLICA_MUTANTS = {
+    "read_from_the_last_copy": ("const int64_t sp = (h / src_heads) * src_copies;",
+                                "const int64_t sp = (h / src_heads) * src_copies + "
+                                "(src_copies - 1);"),
+    "only_the_first_copy_written": ("for (int64_t k = 0; k < dst_copies; ++k) {",
+                                    "for (int64_t k = 0; k < 1; ++k) {"),
+    "copy_index_dropped": ("const int64_t dp = (h / dst_heads) * dst_copies + k;",
+                           "const int64_t dp = (h / dst_heads) * dst_copies;"),
+    "copies_counted_on_the_wrong_side": (
+        "const int64_t dst_copies = cards_per_head(kv_heads, dst_tp);",
+        "const int64_t dst_copies = cards_per_head(kv_heads, src_tp);"),
+    "copies_ignored": ("return tp <= kv_heads ? 1 : tp / kv_heads;", "return 1;"),
+    "copies_as_extra_heads": ("return tp <= kv_heads ? kv_heads / tp : 1;",
+                              "return tp <= kv_heads ? kv_heads / tp : tp / kv_heads;"),
+}
+
+REPLICA_BATTERY = textwrap.dedent("""
+    import sys
+    sys.path[:0] = [{root!r}, {tests!r}]
+    import oracle, test_oracle_replica_pins as P
+    lib = oracle.load({lib!r})
+    for H in (1, 2):
+        for tp in P.REPLICATED_TP:
+            P.test_tagged_heads_reach_every_decode_copy_from_the_first_prefill_copy(lib, H, tp)
+    for H, tp in [(1, (1, 8)), (2, (8, 2)), (8, (4, 16))]:
+        P.test_pd_py_restatement_agrees_with_replication(lib, H, tp)
+    for H, tp_d in [(1, 4), (2, 4)]:
+        P.test_decode_copies_equal_the_unreplicated_relayout(lib, H, tp_d)
+    for H, tp_s in [(1, 4), (2, 8)]:
+        P.test_prefill_copies_reduce_to_the_first_copy(lib, H, tp_s)
+    P.test_replication_in_the_converting_and_layout_nests(lib)
+""")
+
 BATTERY = textwrap.dedent("""
     import sys
     sys.path[:0] = [{root!r}, {tests!r}]
@@ -142,6 +175,20 @@ def test_unmutated_oracle_passes_the_battery(tmp_path):
     assert res.returncode == 0, res.stderr[-3000:]
     res = _battery(lib, LAYOUT_BATTERY)
     assert res.returncode == 0, res.stderr[-3000:]
+    res = _battery(lib, REPLICA_BATTERY)
+    assert res.returncode == 0, res.stderr[-3000:]
+
+
+@pytest.mark.parametrize("name", sorted(REPLICA_MUTANTS))
+def test_replica_mutant_is_caught(tmp_path, name):
+    """Head-replication mistakes, planted in every loop nest, fail the replica pins."""
+    old, new = REPLICA_MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) >= 1, f"mutation site for {name} not in the oracle"
+    lib = _build(tmp_path, name, text.replace(old, new))
+    res = _battery(lib, REPLICA_BATTERY)
+    assert res.returncode != 0, f"mutant {name} survived the replica pins"
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

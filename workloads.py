@@ -14,7 +14,10 @@ permutation of each pool, request after request, so a request's blocks are
 scattered over the pool.
 
 Pool layout (one buffer per TP shard): [L][C][N][B][H / T][D] elements of
-``elem_bytes`` bytes, C = 2 for K and V, C = 1 for an MLA latent.
+``elem_bytes`` bytes, C = 2 for K and V, C = 1 for an MLA latent; a side with
+more shards than KV heads (T > H, a multiple of H) holds one head per shard
+([L][C][N][B][1][D]). Every shard's values are drawn independently, replicas
+included.
 
 The five named workloads:
 
@@ -43,6 +46,11 @@ SENTINEL_BYTE = 0xFF          # decode pools start as all-ones bit patterns (0xF
 POOL_SLACK = 1.25             # pools hold 1.25x the blocks the batch needs
 
 _INT_DTYPES = {1: np.uint8, 2: np.uint16, 4: np.uint32}
+
+
+def heads_per_shard(kv_heads: int, tp: int) -> int:
+    """Head rows per token in one shard pool: H / T, or 1 when T > H."""
+    return kv_heads // tp if tp <= kv_heads else 1
 
 
 @dataclasses.dataclass(frozen=True, eq=False)
@@ -74,11 +82,11 @@ class Workload:
 
     def src_shape(self):
         return (self.num_layers, self.num_components, self.src_num_blocks, self.src_block,
-                self.kv_heads // self.src_tp, self.head_dim)
+                heads_per_shard(self.kv_heads, self.src_tp), self.head_dim)
 
     def dst_shape(self):
         return (self.num_layers, self.num_components, self.dst_num_blocks, self.dst_block,
-                self.kv_heads // self.dst_tp, self.head_dim)
+                heads_per_shard(self.kv_heads, self.dst_tp), self.head_dim)
 
     def src_pool_bytes(self) -> int:
         return int(np.prod(self.src_shape(), dtype=np.int64)) * self.elem_bytes
