@@ -60,6 +60,9 @@ WORKLOAD_TEXT = {
                        "-> TP2 block 64"),
     "dsv3mla": ("DeepSeek-V3 MLA latent: 61 layers, one 576-dim bf16 latent per token; 64 "
                 "prompts lognormal(median 4096) clipped to [1024, 16384]; block 64 -> 16; TP1"),
+    "dsv3mla_tp8": ("DeepSeek-V3 MLA latent replicated over TP8 on both sides: 61 layers, "
+                    "576-dim bf16 latent; the first 8 prompts of the dsv3mla draw; block 64 -> "
+                    "16; read from the first prefill copy, written to all 8 decode copies"),
     "tiny": "tiny: 2 layers, 2 KV heads, head_dim 64, fp16 bits; 1 x 100 tokens; 16 -> 32",
 }
 
@@ -72,7 +75,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama70b",
                    choices=["llama70b", "llama8b", "qwen32k", "qwen32k_ragged", "dsv3mla",
-                            "tiny"])
+                            "dsv3mla_tp8", "tiny"])
     p.add_argument("--layers", type=int, default=None,
                    help="use only the first N layers of the workload (small profiling cases)")
     p.add_argument("--e2e-steps", type=int, default=20)

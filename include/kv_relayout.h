@@ -26,10 +26,16 @@
  * such memory (KVR_ERR_POOL_ADDRESS otherwise).
  *
  * Pool layout. Each TP shard of each side is ONE contiguous buffer of
- *   [num_layers][num_components][num_blocks][block_size][kv_heads / tp][head_dim]
+ *   [num_layers][num_components][num_blocks][block_size][H_local][head_dim]
  * elements of elem_bytes bytes. Components: 2 = K then V planes, 1 = a single
- * latent plane (MLA). Shard s holds the contiguous head range
- * [s * H / tp, (s + 1) * H / tp).
+ * latent plane (MLA). A TP degree tp that divides H: H_local = H / tp and
+ * shard s holds the contiguous head range [s * H / tp, (s + 1) * H / tp).
+ * A TP degree that is a multiple of H (more cards than KV heads, as when GQA
+ * heads or an MLA latent are replicated across TP ranks): H_local = 1 and
+ * head h is held whole by the tp / H consecutive shards h * tp / H ..
+ * (h + 1) * tp / H - 1. The relayout reads such a head from the first prefill
+ * shard that holds it and writes it to every decode shard that holds it
+ * (every copy counts in the bytes written). Any other tp is refused.
  *
  * Block tables. CSR over requests: request r owns table entries
  * bt[off[r]] .. bt[off[r + 1] - 1]; entry k is the physical block holding the
@@ -66,7 +72,8 @@ extern "C" {
 typedef enum kvr_status {
     KVR_OK = 0,
     KVR_ERR_INVALID_ARG = -1,   /* NULL pointer, non-positive size, bad offsets, negative length */
-    KVR_ERR_UNSUPPORTED = -2,   /* elem_bytes not 1/2/4, H % tp != 0, tp > KVR_MAX_TP, too large */
+    KVR_ERR_UNSUPPORTED = -2,   /* elem_bytes not 1/2/4, tp neither divides nor is a multiple
+                                   of H, tp > KVR_MAX_TP, too large */
     KVR_ERR_ALIGNMENT = -3,     /* a pool not 16-byte aligned, or head_dim * elem_bytes % 16 != 0 */
     KVR_ERR_BLOCK_RANGE = -4,   /* a used block id outside [0, num_blocks) */
     KVR_ERR_TABLE_SHORT = -5,   /* a request has fewer than ceil(n / B) table entries */
@@ -85,8 +92,8 @@ typedef struct kvr_desc {
     int32_t kv_heads;          /* H >= 1: global KV heads (1 for an MLA latent) */
     int32_t head_dim;          /* D >= 1: elements per head row */
     int32_t elem_bytes;        /* es: 1, 2 or 4 */
-    int32_t src_tp;            /* Tp: prefill shard pools, 1..KVR_MAX_TP, divides H */
-    int32_t dst_tp;            /* Td: decode shard pools, 1..KVR_MAX_TP, divides H */
+    int32_t src_tp;            /* Tp: prefill shard pools, 1..KVR_MAX_TP, divides H or a multiple of it */
+    int32_t dst_tp;            /* Td: decode shard pools, 1..KVR_MAX_TP, divides H or a multiple of it */
     int32_t src_block_size;    /* Bp >= 1 tokens per prefill block */
     int32_t dst_block_size;    /* Bd >= 1 tokens per decode block */
     int64_t src_num_blocks;    /* Np >= 1 blocks in each prefill shard pool */
@@ -131,7 +138,8 @@ typedef struct kvr_convert {
 /*
  * Validate *desc on the host and compute the bytes one full relayout reads
  * and writes (each = sum_r n_r * L * C * H * D * es, the page's "KV per token
- * times prompt length", section "传输的代价"). Makes no CUDA call and
+ * times prompt length", section "传输的代价"; writes times Td / H when the
+ * decode side replicates heads). Makes no CUDA call and
  * dereferences no device pointer. Either output pointer may be NULL.
  */
 kvr_status kv_relayout_desc_bytes(const kvr_desc *desc, int64_t *bytes_read,
@@ -154,8 +162,9 @@ kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
  *   bases[(s * L + l) * C + c] + b * block_stride + t * token_stride
  *                              + h * head_stride + e * element size,
  * i.e. head rows (dim) are contiguous and the three strides are shared by all
- * views of the side. Examples: the standard layout [L][C][N][B][H/T][D];
- * one K and one V tensor per layer; K and V interleaved per block
+ * views of the side (H_local local heads, as above). Examples: the standard
+ * layout [L][C][N][B][H_local][D]; one K and one V tensor per layer; K and V
+ * interleaved per block
  * ([N][C][B][H][D]); head-major blocks ([N][H][B][D]); a contiguous
  * [tokens][heads][dim] staging buffer seen as blocks of one token.
  * Requirements: every base 16-byte aligned and non-NULL; strides >= 0 and

@@ -13,10 +13,14 @@
 // a per-layer launch with few items still fills the GPU.
 //
 // Inside an item, ROW r (one head row: D elements) is ordered
-// [token o][component c][head h], and chunk q = r * row_chunks + k is the
-// k-th UNIT of row r. A unit is 16 bytes of the row when elements are copied
-// as bits; when the element type changes on the way (BF16 <-> FP8 E4M3) it is
-// 16 elements: 32 bytes on the BF16 side, 16 on the FP8 side. Consecutive
+// [token o][component c][head h][decode copy k], and chunk q = r * row_chunks
+// + k is the k-th UNIT of row r. A decode side with more TP shards than KV
+// heads holds each head on Td/H consecutive shards, so a head row is written
+// once per copy (k < Td/H; one copy otherwise) and read each time from the
+// same prefill row, which the copies' loads, issued side by side, find in L2.
+// A unit is 16 bytes of the row when elements are copied as bits; when the
+// element type changes on the way (BF16 <-> FP8 E4M3) it is 16 elements: 32
+// bytes on the BF16 side, 16 on the FP8 side. Consecutive
 // threads read and write consecutive units of one head row, and the rows of
 // one token follow each other.
 #pragma once
@@ -76,6 +80,11 @@ enum KvrConv : int32_t {
 
 struct KvrGeom {
     int32_t L, C, H, Hp, Hd, Bp, Bd;
+    // TP degrees above H replicate heads: scopies = Tp/H prefill shards (the
+    // first is read) and dcopies = Td/H decode shards (all written) hold one
+    // head; 1 when the side's TP degree divides H. Hx = H * dcopies rows per
+    // (token, component).
+    int32_t scopies, dcopies, Hx;
     int32_t src_row_bytes;      // D * source element bytes, a multiple of 16
     int32_t dst_row_bytes;      // D * destination element bytes, a multiple of 16
     int32_t row_chunks;         // units per row
@@ -83,7 +92,9 @@ struct KvrGeom {
     int32_t dst_unit_bytes;     // bytes one unit writes (16, or 32 to a BF16 side)
     int32_t conv;               // KvrConv
     int32_t per_head;           // conversion scales per (layer, component[, head])
-    KvrDiv div_rc, div_H, div_C, div_Hp, div_Hd, div_Bp, div_Bd;
+    KvrDiv div_rc, div_Hx, div_C, div_Hd, div_Bp, div_Bd;
+    KvrDiv div_sgrp;            // by Hp * dcopies: rows of one prefill shard's heads
+    KvrDiv div_dcop;            // by dcopies
     // byte strides of each side's [block][token][head] view (rows are contiguous)
     int64_t s_block_stride, s_token_stride, s_head_stride;
     int64_t d_block_stride, d_token_stride, d_head_stride;
@@ -114,7 +125,7 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     const uint32_t idx = a.div_slices.div(rem);
     const uint32_t slice = rem - idx * (uint32_t)a.slices;
     const KvrItem it = items[idx];
-    const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.H * a.g.row_chunks;
+    const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.Hx * a.g.row_chunks;
     *layer = a.layer0 + (int32_t)lt;
     *item = it;
     *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);
@@ -126,8 +137,8 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
 KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
                     const int32_t *dbt, const uint64_t *src_base, const uint64_t *dst_base,
                     uint32_t r, uint64_t *saddr, uint64_t *daddr, uint32_t *fidx) {
-    const uint32_t oc = g.div_H.div(r);
-    const uint32_t h = r - oc * (uint32_t)g.H;
+    const uint32_t oc = g.div_Hx.div(r);
+    const uint32_t hv = r - oc * (uint32_t)g.Hx;      // head h = hv / dcopies, copy hv % dcopies
     const uint32_t o = g.div_C.div(oc);
     const uint32_t c = oc - o * (uint32_t)g.C;
     const uint32_t t = (uint32_t)it.t0 + o;
@@ -139,11 +150,15 @@ KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const in
     const uint32_t dbi = g.div_Bd.div(t);
     const uint32_t dof = t - dbi * (uint32_t)g.Bd;
     const int64_t db = dbt[it.dbt_off + (int32_t)dbi];
-    // head h: prefill shard h / Hp (local h % Hp), decode shard h / Hd (local h % Hd)
-    const uint32_t s_sh = g.div_Hp.div(h);
-    const uint32_t s_loc = h - s_sh * (uint32_t)g.Hp;
-    const uint32_t d_sh = g.div_Hd.div(h);
-    const uint32_t d_loc = h - d_sh * (uint32_t)g.Hd;
+    // head h: prefill shard (h / Hp) * scopies (the first that holds it), local
+    // h % Hp; decode shard (h / Hd) * dcopies + copy, local h % Hd, which is
+    // hv / Hd and hv % Hd (Hd = 1 whenever dcopies > 1)
+    const uint32_t sg = g.div_sgrp.div(hv);
+    const uint32_t s_loc = g.div_dcop.div(hv - sg * (uint32_t)g.Hp * (uint32_t)g.dcopies);
+    const uint32_t s_sh = sg * (uint32_t)g.scopies;
+    const uint32_t h = sg * (uint32_t)g.Hp + s_loc;
+    const uint32_t d_sh = g.div_Hd.div(hv);
+    const uint32_t d_loc = hv - d_sh * (uint32_t)g.Hd;
     const uint32_t plane = (uint32_t)layer * (uint32_t)g.C + c;
     const uint64_t sv = src_base[s_sh * (uint32_t)g.L * (uint32_t)g.C + plane];
     const uint64_t dv = dst_base[d_sh * (uint32_t)g.L * (uint32_t)g.C + plane];

@@ -4,8 +4,9 @@
 // (sections "实现" and "布局转换") needs to be well defined: each prompt
 // position has a prefill block and a decode block (tables long enough, ids in
 // range), no two positions land on the same decode slot (no decode block used
-// twice), and every head belongs to exactly one shard on each side (H
-// divisible by both TP degrees).
+// twice), and every head has a home on each side: a TP degree T that divides
+// H gives each shard H/T heads; a multiple of H gives each head T/H shards
+// (read from the first on the prefill side, written to all on the decode side).
 #include <stdint.h>
 #include <string.h>
 
@@ -235,7 +236,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
         return KVR_ERR_INVALID_ARG;
     if (es != 1 && es != 2 && es != 4) return KVR_ERR_UNSUPPORTED;
     if (Tp > KVR_MAX_TP || Td > KVR_MAX_TP) return KVR_ERR_UNSUPPORTED;
-    if (H % Tp != 0 || H % Td != 0) return KVR_ERR_UNSUPPORTED;
+    if ((H % Tp != 0 && Tp % H != 0) || (H % Td != 0 && Td % H != 0)) return KVR_ERR_UNSUPPORTED;
 
     // element types: a bit copy, or BF16 <-> E4M3 with positive finite scales
     int32_t conv = KVR_CONV_NONE;
@@ -264,11 +265,14 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     const int64_t unit_src = conv == KVR_CONV_NONE ? 16 : 16 * (int64_t)es;
     const int64_t unit_dst = conv == KVR_CONV_NONE ? 16 : 16 * es_dst;
     const int64_t row_units = src_row / unit_src;
-    const int32_t Hp = H / Tp, Hd = H / Td;
+    // heads per shard, and shards per head (above 1 when T > H)
+    const int32_t Hp = Tp <= H ? H / Tp : 1, Hd = Td <= H ? H / Td : 1;
+    const int32_t scopies = Tp <= H ? 1 : Tp / H, dcopies = Td <= H ? 1 : Td / H;
+    const int64_t Hx = (int64_t)H * dcopies;   // decode head rows per (token, component)
 
     // one item's units must stay below 2^31 (32-bit chunk indices)
     int64_t item_chunks = 0;
-    if (!mul_fits({(int64_t)Bd, C, H, row_units}, &item_chunks) || item_chunks > INT32_MAX)
+    if (!mul_fits({(int64_t)Bd, C, Hx, row_units}, &item_chunks) || item_chunks > INT32_MAX)
         return KVR_ERR_UNSUPPORTED;
 
     // the views of both sides
@@ -316,17 +320,19 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     if (st != KVR_OK) return st;
 
     int64_t bytes_read = 0, bytes_written = 0;
+    // each head is read once and written to every decode shard that holds it
     if (!mul_fits({tokens, (int64_t)L, C, H, src_row}, &bytes_read) ||
-        !mul_fits({tokens, (int64_t)L, C, H, dst_row}, &bytes_written))
+        !mul_fits({tokens, (int64_t)L, C, Hx, dst_row}, &bytes_written))
         return KVR_ERR_UNSUPPORTED;
     if (bytes_read_out) *bytes_read_out = bytes_read;
     if (bytes_written_out) *bytes_written_out = bytes_written;
     if (hp == nullptr) return KVR_OK;
 
     // token tiles: whole decode blocks, about KVR_TARGET_ITEM_BYTES read per layer
-    const int64_t blk_bytes_all_heads = (int64_t)Bd * C * H * src_row;
+    // (a replicated head's rows count once per decode copy: each is a row to move)
+    const int64_t blk_bytes_all_heads = (int64_t)Bd * C * Hx * src_row;
     int64_t per_tile = std::max<int64_t>(1, KVR_TARGET_ITEM_BYTES / blk_bytes_all_heads);
-    per_tile = std::min<int64_t>(per_tile, INT32_MAX / ((int64_t)Bd * C * H * row_units));
+    per_tile = std::min<int64_t>(per_tile, INT32_MAX / ((int64_t)Bd * C * Hx * row_units));
     const int64_t tile = std::max<int64_t>(1, per_tile) * Bd;
 
     // launch sizes: CTAs = layers x items x slices must fit a 32-bit grid
@@ -341,6 +347,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
 
     KvrGeom &g = hp->g;
     g.L = L; g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
+    g.scopies = scopies; g.dcopies = dcopies; g.Hx = (int32_t)Hx;
     g.src_row_bytes = (int32_t)src_row;
     g.dst_row_bytes = (int32_t)dst_row;
     g.row_chunks = (int32_t)row_units;
@@ -349,10 +356,11 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     g.conv = conv;
     g.per_head = cv != nullptr ? cv->per_head : 0;
     g.div_rc = kvr_make_div((uint32_t)g.row_chunks);
-    g.div_H = kvr_make_div((uint32_t)H);
+    g.div_Hx = kvr_make_div((uint32_t)Hx);
     g.div_C = kvr_make_div((uint32_t)C);
-    g.div_Hp = kvr_make_div((uint32_t)Hp);
     g.div_Hd = kvr_make_div((uint32_t)Hd);
+    g.div_sgrp = kvr_make_div((uint32_t)(Hp * dcopies));
+    g.div_dcop = kvr_make_div((uint32_t)dcopies);
     g.div_Bp = kvr_make_div((uint32_t)Bp);
     g.div_Bd = kvr_make_div((uint32_t)Bd);
     g.s_block_stride = src.bs;
@@ -413,7 +421,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
         return KVR_ERR_NOMEM;
     }
 
-    const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
+    const int64_t avg_chunks = n_items ? tokens * C * Hx * row_units / n_items : 0;
     hp->avg_chunks = avg_chunks;
     hp->sm_count = sm_count;
     hp->layer_resident = layer_resident;

@@ -251,15 +251,18 @@ def _check_extents(src_pools, dst_pools, convert, src_layout, dst_layout, g):
     """The C library checks pool addresses, not allocation sizes: make sure every
     pool tensor and every described view holds what the geometry addresses, so an
     undersized tensor raises here instead of being written past its end. Geometry
-    the library itself refuses (zero sizes, heads not divisible) is left to it."""
+    the library itself refuses (zero sizes, a TP degree that neither divides nor is a
+    multiple of the head count) is left to it."""
     es_src = g["elem_bytes"]
     es_dst = es_src if convert is None else _DTYPE_BYTES.get(int(convert["dst_dtype"]), es_src)
     for side, pools, layout, es in (("src", src_pools, src_layout, es_src),
                                     ("dst", dst_pools, dst_layout, es_dst)):
         T, H = g[f"{side}_tp"], g["kv_heads"]
-        if T < 1 or H < 1 or H % T:
+        if T < 1 or H < 1 or (H % T and T % H):
             continue
-        need_shape = (g[f"{side}_num_blocks"], g[f"{side}_block"], H // T, g["head_dim"])
+        # heads per shard: H / T, or 1 when T > H (each head held by T / H shards)
+        need_shape = (g[f"{side}_num_blocks"], g[f"{side}_block"], max(H // T, 1),
+                      g["head_dim"])
         if layout is not None:
             shape, elem = layout.get("shape"), layout.get("elem_bytes")
             if elem is not None and elem != es:

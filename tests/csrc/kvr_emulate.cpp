@@ -26,12 +26,14 @@ struct Ranges {
     }
 };
 
-// The standard layout: one pool per shard, [L][C][N][B][H/T][D].
+// The standard layout: one pool per shard, [L][C][N][B][H_local][D].
 Ranges pool_ranges(const void *const *pools, int32_t T, const kvr_desc *d, int64_t N, int32_t B,
                    int64_t es) {
     Ranges r;
-    const int64_t bytes = (int64_t)d->num_layers * d->num_components * N * B *
-                          (d->kv_heads / T) * d->head_dim * es;
+    // heads per shard: H / T, or 1 when T > H (each head on T / H shards)
+    const int64_t hl = T <= d->kv_heads ? d->kv_heads / T : 1;
+    const int64_t bytes = (int64_t)d->num_layers * d->num_components * N * B * hl *
+                          d->head_dim * es;
     for (int32_t s = 0; s < T; ++s) {
         r.lo.push_back((uint64_t)(uintptr_t)pools[s]);
         r.hi.push_back((uint64_t)(uintptr_t)pools[s] + (uint64_t)bytes);

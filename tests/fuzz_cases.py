@@ -1,7 +1,8 @@
 """Seeded random geometries for the fuzz tests (CPU emulator and GPU parity).
 
-Every draw is a valid hand-off: H divisible by both TP degrees, rows of a whole
-number of 16-byte units, lengths from 0 to a few blocks of either side (ragged
+Every draw is a valid hand-off: each TP degree divides H or (about one side in
+four) is a multiple of it, so heads are replicated; rows of a whole number of
+16-byte units, lengths from 0 to a few blocks of either side (ragged
 tails on both), optional shared prefill prefix, pools with slack.
 """
 import numpy as np
@@ -18,6 +19,13 @@ def random_workload(seed: int, max_tokens: int = 700, elem_bytes=None, head_dim_
     H = int(rng.choice([1, 2, 4, 6, 8, 12, 16]))
     src_tp = int(rng.choice([t for t in tps if H % t == 0]))
     dst_tp = int(rng.choice([t for t in tps if H % t == 0]))
+    # a second stream decides replication, so the draws below stay those of the seed
+    rep = np.random.default_rng([seed, 78])
+    multiples = [m for m in (2, 4, 8, 16) if H * m <= 16]
+    if multiples and rep.random() < 0.25:
+        src_tp = H * int(rep.choice(multiples))
+    if multiples and rep.random() < 0.25:
+        dst_tp = H * int(rep.choice(multiples))
     d_choices = [d for d in (8, 16, 24, 32, 64, 72, 128, 576)
                  if (d * es) % 16 == 0 and d % head_dim_multiple == 0]
     D = int(rng.choice(d_choices))

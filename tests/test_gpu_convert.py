@@ -108,6 +108,12 @@ SMALL = {
                            dst_tp=2, src_block=3, dst_block=5, seq_lens=[40, 0, 17, 1]),
     "block_1_to_64": dict(num_layers=1, num_components=2, kv_heads=4, head_dim=128, src_tp=1,
                           dst_tp=4, src_block=1, dst_block=64, seq_lens=[1000, 63]),
+    # replicated heads: a per-head scale belongs to the head, whichever copy holds it
+    "rep_h2_tp8_to_tp16": dict(num_layers=2, num_components=2, kv_heads=2, head_dim=32,
+                               src_tp=8, dst_tp=16, src_block=16, dst_block=5,
+                               seq_lens=[77, 16]),
+    "mla_tp2_to_tp4": dict(num_layers=2, num_components=1, kv_heads=1, head_dim=576, src_tp=2,
+                           dst_tp=4, src_block=64, dst_block=16, seq_lens=[129, 1]),
 }
 
 

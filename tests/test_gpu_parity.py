@@ -115,7 +115,9 @@ def test_inverse_restores_prefill_pools():
 def _properties(w, src, dst):
     """Count and sum of the moved elements, on every layer (any size)."""
     import torch
-    per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim
+    # replicated heads: count the first prefill copy of each head, every decode copy
+    scop, dcop = max(1, w.src_tp // w.kv_heads), max(1, w.dst_tp // w.kv_heads)
+    per_layer = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim * dcop
     sentinel = -1  # 0xFFFF as int16; randn bf16 never produces this NaN pattern
     counts = sum((t != sentinel).sum(dim=tuple(range(1, t.dim()))) for t in dst)
     assert torch.all(counts == per_layer), counts.tolist()
@@ -123,7 +125,7 @@ def _properties(w, src, dst):
     m = torch.from_numpy(slot).cuda()
     L, C = w.num_layers, w.num_components
     want = sum(t.view(L, C, w.src_num_blocks, w.src_block, -1)[:, :, m].sum(
-        dim=(1, 2, 3), dtype=torch.int64) for t in src)
+        dim=(1, 2, 3), dtype=torch.int64) for t in src[::scop]) * dcop
     got = sum(torch.where(t == sentinel, torch.zeros_like(t), t).view(L, -1).sum(
         dim=1, dtype=torch.int64) for t in dst)
     assert torch.equal(want, got)
@@ -149,7 +151,7 @@ def test_full_size_in_full(name):
     _properties(w, src, dst)
 
 
-@pytest.mark.parametrize("name", ["qwen32k", "qwen32k_ragged", "dsv3mla"])
+@pytest.mark.parametrize("name", ["qwen32k", "qwen32k_ragged", "dsv3mla", "dsv3mla_tp8"])
 def test_full_size_sampled_layers(name):
     import torch
     w = wl.get(name)

@@ -161,6 +161,36 @@ def test_every_error_is_a_status(cuda_lib):
     assert status_of(ok(dst=[s[0] + 16] + d[1:])) == "KVR_ERR_POOL_OVERLAP"
 
 
+def test_replicated_heads_bytes_and_refusals(cuda_lib):
+    """A TP degree that is a multiple of H replicates heads: each is read once and
+    written to every decode shard that holds it; a degree that neither divides nor is
+    a multiple of H is refused."""
+    for H, tp, copies in ((1, (1, 8), 8), (2, (8, 1), 1), (2, (4, 8), 4), (8, (8, 16), 2),
+                          (1, (16, 16), 16)):
+        w = wl.custom("r", 7, num_layers=3, num_components=2, kv_heads=H, head_dim=64,
+                      elem_bytes=2, src_tp=tp[0], dst_tp=tp[1], src_block=16, dst_block=32,
+                      seq_lens=[100, 40, 0])
+        s, d = fake_pools(w)
+        r, wr = kr.desc_bytes(s, d, **w.geometry())
+        assert r == 140 * 3 * 2 * H * 64 * 2
+        assert wr == copies * r
+    w = wl.custom("r", 7, num_layers=1, num_components=2, kv_heads=2, head_dim=64,
+                  elem_bytes=2, src_tp=2, dst_tp=2, src_block=16, dst_block=32, seq_lens=[5])
+    s, d = fake_pools(w)
+    for tp in ((3, 2), (2, 3), (5, 1), (1, 5)):                 # neither divisor nor multiple
+        big_s = [s[0] + k * (1 << 24) for k in range(tp[0])]
+        big_d = [d[-1] + (1 << 32) + k * (1 << 24) for k in range(tp[1])]
+        assert status_of(lambda: kr.desc_bytes(big_s, big_d, **_geo(w, src_tp=tp[0],
+                                                                     dst_tp=tp[1]))) \
+            == "KVR_ERR_UNSUPPORTED"
+    # decode copies of one head are separate pools: sharing one is an overlap
+    w = wl.custom("r", 7, num_layers=1, num_components=1, kv_heads=1, head_dim=64,
+                  elem_bytes=2, src_tp=1, dst_tp=4, src_block=16, dst_block=16, seq_lens=[5])
+    s, d = fake_pools(w)
+    assert status_of(lambda: kr.desc_bytes(s, [d[0], d[1], d[1], d[3]], **w.geometry())) \
+        == "KVR_ERR_POOL_OVERLAP"
+
+
 def test_permitted_edge_cases(cuda_lib):
     w = wl.custom("e", 6, num_layers=2, num_components=2, kv_heads=8, head_dim=64, elem_bytes=2,
                   src_tp=4, dst_tp=8, src_block=16, dst_block=32, seq_lens=[96, 40, 0])
@@ -234,8 +264,11 @@ def test_emulated_kernel_matches_oracle(emu, case, sms):
     oracle.relayout(src, ref, **w.geometry())
     whole = _pools(w, w.dst_pools_numpy())
     n = _emu_run(emu, w, src, whole, sms=sms)
-    assert n * 16 == oracle.transfer_bytes(w.num_layers, w.num_components, w.kv_heads,
-                                           w.head_dim, w.elem_bytes, w.seq_lens)
+    # one unit per 16 bytes written: each decode copy of a replicated head is written
+    copies = max(1, w.dst_tp // w.kv_heads)
+    assert n * 16 == copies * oracle.transfer_bytes(w.num_layers, w.num_components,
+                                                    w.kv_heads, w.head_dim, w.elem_bytes,
+                                                    w.seq_lens)
     for a, b in zip(ref, whole):
         np.testing.assert_array_equal(a, b)
     per = _pools(w, w.dst_pools_numpy())
@@ -247,7 +280,7 @@ def test_emulated_kernel_matches_oracle(emu, case, sms):
 
 
 @pytest.mark.parametrize("name", ["llama8b", "llama70b", "qwen32k", "qwen32k_ragged",
-                                  "dsv3mla"])
+                                  "dsv3mla", "dsv3mla_tp8"])
 def test_full_size_launches_stay_in_bounds(emu, name):
     """Every address of the full-size launches, against the full pool extents.
 
@@ -259,7 +292,9 @@ def test_full_size_launches_stay_in_bounds(emu, name):
     w = wl.get(name)
     s, d = fake_pools(w)
     desc = kr._Desc(s, d, **w.geometry())
-    per_layer = w.seq_lens.sum() * w.num_components * w.kv_heads * w.head_dim * w.elem_bytes
+    # units are 16 bytes written: every decode copy of a replicated head counts
+    per_layer = (w.seq_lens.sum() * w.num_components * w.kv_heads * w.head_dim * w.elem_bytes
+                 * max(1, w.dst_tp // w.kv_heads))
     n = ctypes.c_int64()
     layers = [-1, 0, w.num_layers - 1] if name == "llama70b" else [0, w.num_layers - 1]
     for l in layers:

@@ -19,7 +19,7 @@ more shards than KV heads (T > H, a multiple of H) holds one head per shard
 ([L][C][N][B][1][D]). Every shard's values are drawn independently, replicas
 included.
 
-The five named workloads:
+The named workloads:
 
 =========  ==============================================================
 tiny       L2 C2 H2 D64 fp16 bit patterns; 1 x 100 tokens; 16 -> 32;
@@ -33,6 +33,10 @@ qwen32k    L64 C2 H8 D128 bf16 N(0,1); 4 x 32768 (ragged variant:
 dsv3mla    L61 C1 H1 D576 bf16 N(0,1) latent; 64 prompts, lognormal
            (median 4096, sigma ln(4)/2), rounded, clipped to
            [1024, 16384]; 64 -> 16; TP1 -> TP1; 1.25x            (seed 4)
+dsv3mla_   the same latent with TP8 on both sides, every shard holding
+ tp8       the whole latent (read from the first prefill copy, written
+           to all 8 decode copies); the first 8 prompts of the
+           dsv3mla draw; 64 -> 16; 1.25x                         (seed 4)
 =========  ==============================================================
 """
 from __future__ import annotations
@@ -277,6 +281,16 @@ def dsv3mla() -> Workload:
                   head_dim=576, src_tp=1, dst_tp=1, src_block=64, dst_block=16)
 
 
+def dsv3mla_tp8() -> Workload:
+    """The MLA latent replicated over TP8 on both sides (8 prompts of the dsv3mla draw:
+    8 decode copies of the whole batch stay within a few tens of GB)."""
+    def lens(rng):
+        x = rng.lognormal(mean=math.log(4096.0), sigma=math.log(4.0) / 2.0, size=64)
+        return np.clip(np.rint(x), 1024, 16384).astype(np.int64)[:8]
+    return _named("dsv3mla_tp8", 4, lens, num_layers=61, num_components=1, kv_heads=1,
+                  head_dim=576, src_tp=8, dst_tp=8, src_block=64, dst_block=16)
+
+
 NAMED = {
     "tiny": tiny,
     "llama8b": llama8b,
@@ -284,6 +298,7 @@ NAMED = {
     "qwen32k": qwen32k,
     "qwen32k_ragged": lambda: qwen32k(ragged=True),
     "dsv3mla": dsv3mla,
+    "dsv3mla_tp8": dsv3mla_tp8,
 }
 
 
