@@ -265,14 +265,15 @@ def oracle_sample(w, src_layers, budget_s, reps_cap=1000, conv=None):
     n = len(src_layers[0])
     wk = dataclasses.replace(w, num_layers=n)
     elems = int(w.seq_lens.sum()) * w.num_components * w.kv_heads * w.head_dim
+    copies = decode_copies(w)
     if conv is None:
         dst = wk.dst_pools_numpy()
-        per_layer = 2 * elems * w.elem_bytes
+        per_layer = elems * w.elem_bytes * (1 + copies)
     else:
         dst_es = 2 if conv["dst_dtype"] == BF16 else 1
         dst = [np.zeros(wk.dst_shape(), {1: np.uint8, 2: np.uint16}[dst_es])
                for _ in range(wk.dst_tp)]
-        per_layer = elems * (w.elem_bytes + dst_es)
+        per_layer = elems * (w.elem_bytes + dst_es * copies)
         per = w.num_components * (w.kv_heads if conv["per_head"] else 1)   # scales per layer
         geo = wk.geometry()
         geo.pop("elem_bytes")
@@ -345,11 +346,18 @@ def host_link_ceiling(torch, dev, pairs_in, pairs_out, steps):
                     "streams)"}
 
 
+def decode_copies(w):
+    """Decode shards that hold each head: Td / H when the decode TP degree exceeds the
+    head count (heads replicated), else 1."""
+    return max(1, w.dst_tp // w.kv_heads)
+
+
 def algorithmic_bytes(w, conv):
-    """Bytes one whole-prompt hand-off reads plus writes (both arms' metric)."""
+    """Bytes one whole-prompt hand-off reads plus writes (both arms' metric): every
+    head is read once and written to each decode shard that holds it."""
     elems = int(w.seq_lens.sum()) * w.num_layers * w.num_components * w.kv_heads * w.head_dim
     dst_es = w.elem_bytes if conv is None else (2 if conv["dst_dtype"] == BF16 else 1)
-    return elems * (w.elem_bytes + dst_es)
+    return elems * (w.elem_bytes + dst_es * decode_copies(w))
 
 
 def dtype_label(w, args, conv):

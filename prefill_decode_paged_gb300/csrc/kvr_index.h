@@ -80,11 +80,6 @@ enum KvrConv : int32_t {
 
 struct KvrGeom {
     int32_t L, C, H, Hp, Hd, Bp, Bd;
-    // TP degrees above H replicate heads: scopies = Tp/H prefill shards (the
-    // first is read) and dcopies = Td/H decode shards (all written) hold one
-    // head; 1 when the side's TP degree divides H. Hx = H * dcopies rows per
-    // (token, component).
-    int32_t scopies, dcopies, Hx;
     int32_t src_row_bytes;      // D * source element bytes, a multiple of 16
     int32_t dst_row_bytes;      // D * destination element bytes, a multiple of 16
     int32_t row_chunks;         // units per row
@@ -92,12 +87,20 @@ struct KvrGeom {
     int32_t dst_unit_bytes;     // bytes one unit writes (16, or 32 to a BF16 side)
     int32_t conv;               // KvrConv
     int32_t per_head;           // conversion scales per (layer, component[, head])
-    KvrDiv div_rc, div_Hx, div_C, div_Hd, div_Bp, div_Bd;
+    KvrDiv div_rc;
+    KvrDiv div_Hx;              // by Hx (below): decode head rows per (token, component)
+    KvrDiv div_C;
     KvrDiv div_sgrp;            // by Hp * dcopies: rows of one prefill shard's heads
-    KvrDiv div_dcop;            // by dcopies
+    KvrDiv div_Hd, div_Bp, div_Bd;
     // byte strides of each side's [block][token][head] view (rows are contiguous)
     int64_t s_block_stride, s_token_stride, s_head_stride;
     int64_t d_block_stride, d_token_stride, d_head_stride;
+    // TP degrees above H replicate heads: scopies = Tp/H prefill shards (the
+    // first is read) and dcopies = Td/H decode shards (all written) hold one
+    // head; 1 when the side's TP degree divides H. Hx = H * dcopies rows per
+    // (token, component).
+    int32_t scopies, dcopies, Hx;
+    KvrDiv div_dcop;            // by dcopies
 };
 
 // Kernel parameter block (passed by value as a __grid_constant__).
@@ -117,7 +120,8 @@ struct KvrArgs {
     KvrDiv div_tasks_per_layer, div_slices;
 };
 
-// Task -> (layer, item, chunk range [q0, q1) of the item).
+// Task -> (layer, item, chunk range [q0, q1) of the item). REP as in kvr_row.
+template <bool REP>
 KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,
                      KvrItem *item, uint32_t *q0, uint32_t *q1) {
     const uint32_t lt = a.div_tasks_per_layer.div(task);
@@ -125,7 +129,7 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     const uint32_t idx = a.div_slices.div(rem);
     const uint32_t slice = rem - idx * (uint32_t)a.slices;
     const KvrItem it = items[idx];
-    const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.Hx * a.g.row_chunks;
+    const uint64_t total = (uint64_t)it.ntok * a.g.C * (REP ? a.g.Hx : a.g.H) * a.g.row_chunks;
     *layer = a.layer0 + (int32_t)lt;
     *item = it;
     *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);
@@ -133,12 +137,17 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
 }
 
 // Row r of an item -> address of its prefill row, address of its decode row,
-// and the index of its conversion scale.
+// and the index of its conversion scale. REP: a side's TP degree exceeds H
+// (scopies or dcopies above 1); without it every head sits on one shard per
+// side and the row's head is hv itself, which keeps the index chain of the
+// plain relayout as short as it can be.
+template <bool REP>
 KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const int32_t *sbt,
                     const int32_t *dbt, const uint64_t *src_base, const uint64_t *dst_base,
                     uint32_t r, uint64_t *saddr, uint64_t *daddr, uint32_t *fidx) {
     const uint32_t oc = g.div_Hx.div(r);
-    const uint32_t hv = r - oc * (uint32_t)g.Hx;      // head h = hv / dcopies, copy hv % dcopies
+    // head h = hv / dcopies, copy hv % dcopies (Hx = H without replication)
+    const uint32_t hv = r - oc * (uint32_t)(REP ? g.Hx : g.H);
     const uint32_t o = g.div_C.div(oc);
     const uint32_t c = oc - o * (uint32_t)g.C;
     const uint32_t t = (uint32_t)it.t0 + o;
@@ -153,10 +162,17 @@ KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const in
     // head h: prefill shard (h / Hp) * scopies (the first that holds it), local
     // h % Hp; decode shard (h / Hd) * dcopies + copy, local h % Hd, which is
     // hv / Hd and hv % Hd (Hd = 1 whenever dcopies > 1)
-    const uint32_t sg = g.div_sgrp.div(hv);
-    const uint32_t s_loc = g.div_dcop.div(hv - sg * (uint32_t)g.Hp * (uint32_t)g.dcopies);
-    const uint32_t s_sh = sg * (uint32_t)g.scopies;
-    const uint32_t h = sg * (uint32_t)g.Hp + s_loc;
+    uint32_t h, s_sh, s_loc;
+    if (REP) {
+        const uint32_t sg = g.div_sgrp.div(hv);
+        s_loc = g.div_dcop.div(hv - sg * (uint32_t)g.Hp * (uint32_t)g.dcopies);
+        s_sh = sg * (uint32_t)g.scopies;
+        h = sg * (uint32_t)g.Hp + s_loc;
+    } else {
+        h = hv;
+        s_sh = g.div_sgrp.div(h);                     // Hp * dcopies = Hp
+        s_loc = h - s_sh * (uint32_t)g.Hp;
+    }
     const uint32_t d_sh = g.div_Hd.div(hv);
     const uint32_t d_loc = hv - d_sh * (uint32_t)g.Hd;
     const uint32_t plane = (uint32_t)layer * (uint32_t)g.C + c;
@@ -168,3 +184,6 @@ KVR_HD void kvr_row(const KvrGeom &g, int32_t layer, const KvrItem &it, const in
                              (int64_t)d_loc * g.d_head_stride);
     *fidx = g.per_head ? plane * (uint32_t)g.H + h : plane;
 }
+
+// Whether a plan's rows need the replicated-head arithmetic of kvr_row.
+KVR_HD bool kvr_replicated(const KvrGeom &g) { return g.scopies > 1 || g.dcopies > 1; }

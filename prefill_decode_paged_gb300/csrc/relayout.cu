@@ -139,7 +139,8 @@ __device__ __forceinline__ void dequant16(const uint4 &c, float s, uint4 *lo, ui
 // (per-layer launches: hides the block-table reads in the previous launch's
 // tail; whole-prompt launches wait first, which measured 1.7 % faster there).
 // A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
-template <int U, int CONV, bool EARLY>
+// REP: the plan replicates heads (a TP degree above H; see kvr_row).
+template <int U, int CONV, bool EARLY, bool REP>
 __global__ void __launch_bounds__(KVR_THREADS)
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
     constexpr int NL = CONV == KVR_CONV_BF16_TO_E4M3 ? 2 : 1;
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
     int32_t layer;
     KvrItem it;
     uint32_t q0, q1;
-    kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
+    kvr_task<REP>(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
     if (q0 >= q1) {
         // a CTA without rows still orders itself after the previous grid (and a
         // launch without the early wait still completes after it)
@@ -182,7 +183,8 @@ __global__ void __launch_bounds__(KVR_THREADS)
         for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
             uint32_t fidx;
             uint64_t sa, da;
-            kvr_row(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da, &fidx);
+            kvr_row<REP>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da,
+                         &fidx);
             rows[r - w0] = make_ulonglong2(sa, da);
             if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
         }
@@ -240,22 +242,30 @@ __global__ void __launch_bounds__(KVR_THREADS)
 
 using KvrKernel = void (*)(KvrArgs);
 
-// Kernel instance for a conversion and launch mode: 8 loads in flight per
-// thread for whole-prompt launches, 4 for per-layer ones.
-KvrKernel pick_kernel(int32_t conv, bool per_layer) {
+// Kernel instance for a conversion, launch mode and head replication: 8 loads
+// in flight per thread for whole-prompt launches, 4 for converting per-layer
+// ones (16-element units of BF16 take two loads each).
+template <bool REP>
+KvrKernel pick_kernel_rep(int32_t conv, bool per_layer) {
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
             return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT / 2,
-                                                   KVR_CONV_BF16_TO_E4M3, true>
-                             : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3, false>;
+                                                   KVR_CONV_BF16_TO_E4M3, true, REP>
+                             : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3, false,
+                                                   REP>;
         case KVR_CONV_E4M3_TO_BF16:
-            return per_layer
-                       ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT, KVR_CONV_E4M3_TO_BF16, true>
-                       : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16, false>;
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT,
+                                                   KVR_CONV_E4M3_TO_BF16, true, REP>
+                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16, false,
+                                                   REP>;
         default:
-            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_NONE, true>
-                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE, false>;
+            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_NONE, true, REP>
+                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE, false, REP>;
     }
+}
+
+KvrKernel pick_kernel(int32_t conv, bool per_layer, bool rep) {
+    return rep ? pick_kernel_rep<true>(conv, per_layer) : pick_kernel_rep<false>(conv, per_layer);
 }
 
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
@@ -279,7 +289,9 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pick_kernel(p->host.g.conv, per_layer), a) == cudaSuccess
+    return cudaLaunchKernelEx(&cfg,
+                              pick_kernel(p->host.g.conv, per_layer, kvr_replicated(p->host.g)),
+                              a) == cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
 }
@@ -382,8 +394,11 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
         const int32_t conv = cv == nullptr ? KVR_CONV_NONE
                              : cv->src_dtype == KVR_DTYPE_BF16 ? KVR_CONV_BF16_TO_E4M3
                                                                 : KVR_CONV_E4M3_TO_BF16;
+        // the per-layer instance this plan will launch (desc is validated below)
+        const bool rep = desc != nullptr && desc->kv_heads > 0 &&
+                         (desc->src_tp > desc->kv_heads || desc->dst_tp > desc->kv_heads);
         int resident = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, pick_kernel(conv, true),
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, pick_kernel(conv, true, rep),
                                                           KVR_THREADS, 0) != cudaSuccess) {
             cudaGetLastError();
             resident = 0;
@@ -600,7 +615,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     // so the launch must be fully ordered after the copies.
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE, false>, a) ==
+    return cudaLaunchKernelEx(&cfg, pick_kernel(KVR_CONV_NONE, false, kvr_replicated(hp.g)), a) ==
                    cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;

@@ -89,7 +89,8 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
         int32_t l;
         KvrItem it;
         uint32_t q0, q1;
-        kvr_task(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
+        (kvr_replicated(a.g) ? kvr_task<true> : kvr_task<false>)(a, (uint32_t)task, a.items, &l,
+                                                                  &it, &q0, &q1);
         if (q0 > q1 || l < layer0 || l >= layer0 + layers) {
             ++bad;
             continue;
@@ -102,8 +103,8 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                 for (uint32_t r = w0 + tid; r < w1; r += KVR_THREADS) {
                     uint32_t fidx;
                     uint64_t sa, da;
-                    kvr_row(a.g, l, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da,
-                            &fidx);
+                    (kvr_replicated(a.g) ? kvr_row<true> : kvr_row<false>)(
+                        a.g, l, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da, &fidx);
                     if (!sr.holds(sa, (uint64_t)a.g.src_row_bytes) ||
                         !dr.holds(da, (uint64_t)a.g.dst_row_bytes) ||
                         (a.g.conv != KVR_CONV_NONE && (int64_t)fidx >= n_factors)) {

@@ -88,3 +88,31 @@ def test_traffic_is_dropped_when_the_kernel_changed(tmp_path, monkeypatch):
         f"kernel_source_sha256: {h}\ntraffic_bytes_per_full_launch: 8000\n")
     assert bench.profiled_traffic("llama70b", 80)[0] == 8000
     assert bench.profiled_traffic("llama70b", 8)[0] == 800
+
+
+@pytest.mark.parametrize("name", ["llama70b", "qwen32k", "dsv3mla", "dsv3mla_tp8"])
+@pytest.mark.parametrize("convert", [None, "bf16_to_fp8"])
+def test_bench_bytes_equal_the_librarys_count(name, convert):
+    """bench.py cross-checks the plan's byte count against its own workload arithmetic;
+    the two must agree for every named workload (replicated decode copies included)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    from prefill_decode_paged_gb300 import kv_relayout as kr
+    w = wl.get(name)
+    base, gap, s, d = 1 << 40, 1 << 20, [], []
+    at = base
+    for _ in range(w.src_tp):
+        s.append(at)
+        at += (w.src_pool_bytes() + gap) // 256 * 256 + 256
+    dst_es = 1 if convert else w.elem_bytes
+    for _ in range(w.dst_tp):
+        d.append(at)
+        at += (w.dst_pool_bytes() * dst_es // w.elem_bytes + gap) // 256 * 256 + 256
+    conv = None
+    if convert:
+        import numpy as np
+        conv = dict(src_dtype=bench.BF16, dst_dtype=2, per_head=0,
+                    scales=np.ones(w.num_layers * w.num_components, np.float32))
+    r, wr = kr.desc_bytes(s, d, convert=conv, **w.geometry())
+    assert r + wr == bench.algorithmic_bytes(w, conv)
