@@ -13,11 +13,11 @@
 // a per-layer launch with few items still fills the GPU.
 //
 // Inside an item, ROW r (one head row: D elements) is ordered
-// [token o][component c][head h][decode copy k], and chunk q = r * row_chunks
-// + k is the k-th UNIT of row r. A decode side with more TP shards than KV
-// heads holds each head on Td/H consecutive shards, so a head row is written
-// once per copy (k < Td/H; one copy otherwise) and read each time from the
-// same prefill row, which the copies' loads, issued side by side, find in L2.
+// [token o][component c][head h], and chunk q = r * row_chunks + k is the
+// k-th UNIT of row r. A decode side with more TP shards than KV heads holds
+// each head on Td/H consecutive shards: a row's decode rows are then
+// [token][component][head][decode copy] (table rows r * Td/H + copy), and
+// each unit is loaded once and stored to every copy.
 // A unit is 16 bytes of the row when elements are copied as bits; when the
 // element type changes on the way (BF16 <-> FP8 E4M3) it is 16 elements: 32
 // bytes on the BF16 side, 16 on the FP8 side. Consecutive
@@ -101,6 +101,7 @@ struct KvrGeom {
     // (token, component).
     int32_t scopies, dcopies, Hx;
     KvrDiv div_dcop;            // by dcopies
+    int32_t win_rows;           // prefill rows per row window when dcopies > 1
 };
 
 // Kernel parameter block (passed by value as a __grid_constant__).
@@ -120,8 +121,8 @@ struct KvrArgs {
     KvrDiv div_tasks_per_layer, div_slices;
 };
 
-// Task -> (layer, item, chunk range [q0, q1) of the item). REP as in kvr_row.
-template <bool REP>
+// Task -> (layer, item, chunk range [q0, q1) of the item). Chunks are units of
+// the prefill rows: with replicated decode heads each is stored to every copy.
 KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,
                      KvrItem *item, uint32_t *q0, uint32_t *q1) {
     const uint32_t lt = a.div_tasks_per_layer.div(task);
@@ -129,7 +130,7 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     const uint32_t idx = a.div_slices.div(rem);
     const uint32_t slice = rem - idx * (uint32_t)a.slices;
     const KvrItem it = items[idx];
-    const uint64_t total = (uint64_t)it.ntok * a.g.C * (REP ? a.g.Hx : a.g.H) * a.g.row_chunks;
+    const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.H * a.g.row_chunks;
     *layer = a.layer0 + (int32_t)lt;
     *item = it;
     *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);

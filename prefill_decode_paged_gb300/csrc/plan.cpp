@@ -348,6 +348,7 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     KvrGeom &g = hp->g;
     g.L = L; g.C = C; g.H = H; g.Hp = Hp; g.Hd = Hd; g.Bp = Bp; g.Bd = Bd;
     g.scopies = scopies; g.dcopies = dcopies; g.Hx = (int32_t)Hx;
+    g.win_rows = KVR_ROW_WINDOW / dcopies;          // a window holds every copy of its rows
     g.src_row_bytes = (int32_t)src_row;
     g.dst_row_bytes = (int32_t)dst_row;
     g.row_chunks = (int32_t)row_units;
@@ -421,7 +422,8 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
         return KVR_ERR_NOMEM;
     }
 
-    const int64_t avg_chunks = n_items ? tokens * C * Hx * row_units / n_items : 0;
+    // units of the prefill rows (each stored to all dcopies decode copies)
+    const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
     hp->avg_chunks = avg_chunks;
     hp->sm_count = sm_count;
     hp->layer_resident = layer_resident;
@@ -458,7 +460,8 @@ int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sm
     // registers, fewer resident CTAs) measured faster with the larger CTAs,
     // and so did every launch on an SM-limited stream, so those stay whole
     if (!limited && hp.g.conv == KVR_CONV_NONE) {
-        const int64_t item_bytes = hp.avg_chunks * hp.g.src_unit_bytes;
+        // bytes written (a replicated head's unit is stored to every copy)
+        const int64_t item_bytes = hp.avg_chunks * hp.g.dst_unit_bytes * hp.g.dcopies;
         const int64_t most = std::max<int64_t>(1, hp.avg_chunks / KVR_MIN_SLICE_CHUNKS);
         const int64_t want = std::min<int64_t>(most, ceil_div(item_bytes, KVR_MAX_CTA_BYTES));
         if (want > s) s = (int32_t)want;

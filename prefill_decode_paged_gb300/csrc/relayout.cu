@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
     int32_t layer;
     KvrItem it;
     uint32_t q0, q1;
-    kvr_task<REP>(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
+    kvr_task(a, blockIdx.x, a.items, &layer, &it, &q0, &q1);
     if (q0 >= q1) {
         // a CTA without rows still orders itself after the previous grid (and a
         // launch without the early wait still completes after it)
@@ -173,67 +173,139 @@ __global__ void __launch_bounds__(KVR_THREADS)
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     const uint32_t r_end = a.g.div_rc.div(q1 - 1) + 1;
 
-    bool waited = !EARLY;
-    for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += KVR_ROW_WINDOW) {
-        const uint32_t w1 = min(w0 + (uint32_t)KVR_ROW_WINDOW, r_end);
-        // 1. one thread per row: the row's two addresses (block tables read here).
-        // The work list, tables and factors are plan data that no kernel writes,
-        // so with EARLY the first window is built before waiting for the
-        // previous grid.
-        for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
-            uint32_t fidx;
-            uint64_t sa, da;
-            kvr_row<REP>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da,
-                         &fidx);
-            rows[r - w0] = make_ulonglong2(sa, da);
-            if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
-        }
-        if (EARLY && !waited) {
-            if (!a.no_wait) {
-                asm volatile("griddepcontrol.wait;" ::: "memory");
-                asm volatile("griddepcontrol.launch_dependents;");
+    if constexpr (REP) {
+        // Replicated heads: units are those of the prefill rows ([token][component]
+        // [head]); the table holds each row's dcopies decode rows, one after
+        // another, and a unit is loaded once and stored to every copy.
+        const uint32_t dc = (uint32_t)a.g.dcopies;
+        const uint32_t wn = (uint32_t)a.g.win_rows;   // prefill rows per window
+        bool waited = !EARLY;
+        for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += wn) {
+            const uint32_t w1 = min(w0 + wn, r_end);
+            const uint32_t t_end = (w1 - w0) * dc;
+            for (uint32_t t = threadIdx.x; t < t_end; t += KVR_THREADS) {
+                uint32_t fidx;
+                uint64_t sa, da;
+                kvr_row<true>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base,
+                              w0 * dc + t, &sa, &da, &fidx);
+                rows[t] = make_ulonglong2(sa, da);
+                if (CONV != KVR_CONV_NONE) row_factor[t] = a.factors[fidx];
             }
-            waited = true;
-        }
-        __syncthreads();
-        // 2. the units of those rows: U in flight per thread
-        const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
-        for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
-            uint4 v[U][NL];
-            unsigned char *to[U];
-            float f[U];
+            if (EARLY && !waited) {
+                if (!a.no_wait) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    asm volatile("griddepcontrol.launch_dependents;");
+                }
+                waited = true;
+            }
+            __syncthreads();
+            const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
+            for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
+                uint4 v[U][NL];
+                float f[U];
 #pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const uint32_t q = base + (uint32_t)k * KVR_THREADS;
-                to[k] = nullptr;
-                f[k] = 0.0f;
-                if (q < qb) {
+                for (int k = 0; k < U; ++k) {
+                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                    f[k] = 0.0f;
+                    if (q < qb) {
+                        const uint32_t r = a.g.div_rc.div(q);
+                        const uint32_t u = q - r * rc;
+                        const ulonglong2 p = rows[(r - w0) * dc];
+#pragma unroll
+                        for (int j = 0; j < NL; ++j)
+                            v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                        if (CONV != KVR_CONV_NONE) f[k] = row_factor[(r - w0) * dc];
+                    }
+                }
+                // the unit's row and offset are recomputed here rather than kept
+                // from the loads (fewer live registers across the loads)
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                    if (q >= qb) continue;
                     const uint32_t r = a.g.div_rc.div(q);
                     const uint32_t u = q - r * rc;
-                    const ulonglong2 p = rows[r - w0];
-#pragma unroll
-                    for (int j = 0; j < NL; ++j)
-                        v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
-                    to[k] = (unsigned char *)p.y + u * DU;
-                    if (CONV != KVR_CONV_NONE) f[k] = row_factor[r - w0];
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                if (to[k] == nullptr) continue;
-                if (CONV == KVR_CONV_NONE) {
-                    store_stream(to[k], v[k][0]);
-                } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
-                    store_stream(to[k], quant16(v[k][0], v[k][NL - 1], f[k]));
-                } else {
+                    const uint32_t ti = (r - w0) * dc;
                     uint4 lo, hi;
-                    dequant16(v[k][0], f[k], &lo, &hi);
-                    store_stream(to[k], lo);
-                    store_stream(to[k] + 16, hi);
+                    if (CONV == KVR_CONV_NONE) {
+                        lo = v[k][0];
+                    } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
+                        lo = quant16(v[k][0], v[k][NL - 1], f[k]);
+                    } else {
+                        dequant16(v[k][0], f[k], &lo, &hi);
+                    }
+                    for (uint32_t c = 0; c < dc; ++c) {
+                        unsigned char *to = (unsigned char *)rows[ti + c].y + u * DU;
+                        store_stream(to, lo);
+                        if (CONV == KVR_CONV_E4M3_TO_BF16) store_stream(to + 16, hi);
+                    }
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
+    } else {
+        bool waited = !EARLY;
+        for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += KVR_ROW_WINDOW) {
+            const uint32_t w1 = min(w0 + (uint32_t)KVR_ROW_WINDOW, r_end);
+            // 1. one thread per row: the row's two addresses (block tables read here).
+            // The work list, tables and factors are plan data that no kernel writes,
+            // so with EARLY the first window is built before waiting for the
+            // previous grid.
+            for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS) {
+                uint32_t fidx;
+                uint64_t sa, da;
+                kvr_row<false>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa,
+                               &da, &fidx);
+                rows[r - w0] = make_ulonglong2(sa, da);
+                if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
+            }
+            if (EARLY && !waited) {
+                if (!a.no_wait) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    asm volatile("griddepcontrol.launch_dependents;");
+                }
+                waited = true;
+            }
+            __syncthreads();
+            // 2. the units of those rows: U in flight per thread
+            const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
+            for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
+                uint4 v[U][NL];
+                unsigned char *to[U];
+                float f[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                    to[k] = nullptr;
+                    f[k] = 0.0f;
+                    if (q < qb) {
+                        const uint32_t r = a.g.div_rc.div(q);
+                        const uint32_t u = q - r * rc;
+                        const ulonglong2 p = rows[r - w0];
+#pragma unroll
+                        for (int j = 0; j < NL; ++j)
+                            v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                        to[k] = (unsigned char *)p.y + u * DU;
+                        if (CONV != KVR_CONV_NONE) f[k] = row_factor[r - w0];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    if (to[k] == nullptr) continue;
+                    if (CONV == KVR_CONV_NONE) {
+                        store_stream(to[k], v[k][0]);
+                    } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
+                        store_stream(to[k], quant16(v[k][0], v[k][NL - 1], f[k]));
+                    } else {
+                        uint4 lo, hi;
+                        dequant16(v[k][0], f[k], &lo, &hi);
+                        store_stream(to[k], lo);
+                        store_stream(to[k] + 16, hi);
+                    }
+                }
+            }
+            __syncthreads();
+        }
     }
     // A launch that skipped the wait before its copies still finishes only after
     // the previous grid, so work queued after it on the stream sees both.

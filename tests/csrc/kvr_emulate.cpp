@@ -84,36 +84,44 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
+    // replicated heads (kvr_replicated): a window of win_rows prefill rows, a
+    // table row per (prefill row, decode copy), one load and dc stores per
+    // unit; otherwise dc = 1 and the table rows are the prefill rows
+    const bool rep = kvr_replicated(a.g);
+    const uint32_t dc = rep ? (uint32_t)a.g.dcopies : 1u;
+    const uint32_t wn = rep ? (uint32_t)a.g.win_rows : (uint32_t)KVR_ROW_WINDOW;
+    if (wn * dc > KVR_ROW_WINDOW || wn == 0) return KVR_ERR_UNSUPPORTED;
     int64_t bad = 0, visited = 0;
     for (uint64_t task = 0; task < grid; ++task) {
         int32_t l;
         KvrItem it;
         uint32_t q0, q1;
-        (kvr_replicated(a.g) ? kvr_task<true> : kvr_task<false>)(a, (uint32_t)task, a.items, &l,
-                                                                  &it, &q0, &q1);
+        kvr_task(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
         if (q0 > q1 || l < layer0 || l >= layer0 + layers) {
             ++bad;
             continue;
         }
         if (q0 == q1) continue;
         const uint32_t r_end = a.g.div_rc.div(q1 - 1) + 1;
-        for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += KVR_ROW_WINDOW) {
-            const uint32_t w1 = w0 + KVR_ROW_WINDOW < r_end ? w0 + KVR_ROW_WINDOW : r_end;
+        for (uint32_t w0 = a.g.div_rc.div(q0); w0 < r_end; w0 += wn) {
+            const uint32_t w1 = w0 + wn < r_end ? w0 + wn : r_end;
+            const uint32_t t_end = (w1 - w0) * dc;
             for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
-                for (uint32_t r = w0 + tid; r < w1; r += KVR_THREADS) {
+                for (uint32_t t = tid; t < t_end; t += KVR_THREADS) {
                     uint32_t fidx;
                     uint64_t sa, da;
-                    (kvr_replicated(a.g) ? kvr_row<true> : kvr_row<false>)(
-                        a.g, l, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa, &da, &fidx);
+                    (rep ? kvr_row<true> : kvr_row<false>)(a.g, l, it, a.sbt, a.dbt, a.src_base,
+                                                           a.dst_base, w0 * dc + t, &sa, &da,
+                                                           &fidx);
                     if (!sr.holds(sa, (uint64_t)a.g.src_row_bytes) ||
                         !dr.holds(da, (uint64_t)a.g.dst_row_bytes) ||
                         (a.g.conv != KVR_CONV_NONE && (int64_t)fidx >= n_factors)) {
                         ++bad;
-                        rows_src[r - w0] = rows_dst[r - w0] = UINT64_MAX;
+                        rows_src[t] = rows_dst[t] = UINT64_MAX;
                         continue;
                     }
-                    rows_src[r - w0] = sa;
-                    rows_dst[r - w0] = da;
+                    rows_src[t] = sa;
+                    rows_dst[t] = da;
                 }
             const uint32_t qa = q0 > w0 * rc ? q0 : w0 * rc;
             const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
@@ -124,20 +132,29 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                         if (q >= qb) continue;
                         const uint32_t r = a.g.div_rc.div(q);
                         const uint32_t u = q - r * rc;
-                        ++visited;
-                        if (r < w0 || r >= w1 || rows_src[r - w0] == UINT64_MAX) {
+                        if (r < w0 || r >= w1) {
                             ++bad;
                             continue;
                         }
-                        const uint64_t from = rows_src[r - w0] + (uint64_t)u * su;
-                        const uint64_t to = rows_dst[r - w0] + (uint64_t)u * du;
-                        if (from % 16 != 0 || to % 16 != 0 ||
-                            (u + 1) * su > (uint32_t)a.g.src_row_bytes ||
-                            (u + 1) * du > (uint32_t)a.g.dst_row_bytes) {
-                            ++bad;
-                            continue;
+                        const uint32_t ti = (r - w0) * dc;
+                        for (uint32_t c = 0; c < dc; ++c) {
+                            ++visited;
+                            // every copy's prefill address is the one the unit is loaded from
+                            if (rows_src[ti + c] == UINT64_MAX || rows_src[ti + c] != rows_src[ti]) {
+                                ++bad;
+                                continue;
+                            }
+                            const uint64_t from = rows_src[ti] + (uint64_t)u * su;
+                            const uint64_t to = rows_dst[ti + c] + (uint64_t)u * du;
+                            if (from % 16 != 0 || to % 16 != 0 ||
+                                (u + 1) * su > (uint32_t)a.g.src_row_bytes ||
+                                (u + 1) * du > (uint32_t)a.g.dst_row_bytes) {
+                                ++bad;
+                                continue;
+                            }
+                            if (copy)
+                                memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from, 16);
                         }
-                        if (copy) memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from, 16);
                     }
                 }
             }
