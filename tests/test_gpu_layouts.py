@@ -28,6 +28,12 @@ def _w(seed, **kw):
     return wl.custom("glay", seed, **base)
 
 
+# a plain head split, and heads replicated on both sides (H = 2 on 4 prefill and
+# 8 decode shards: read from the first prefill copy, written to all decode copies)
+GEOS = {"split": {}, "replicated": dict(kv_heads=2, src_tp=4, dst_tp=8, src_block=5,
+                                        dst_block=16)}
+
+
 def _tables(w):
     g = w.geometry()
     keys = ("num_layers", "num_components", "kv_heads", "head_dim", "src_tp", "dst_tp",
@@ -61,14 +67,15 @@ def decode_family(w, kind, dtype=np.uint16, fill=0xFFFF):
     return bufs, nv, tbufs, tv
 
 
+@pytest.mark.parametrize("geo", sorted(GEOS))
 @pytest.mark.parametrize("kind", ["standard", "hnd", "kv_interleaved"])
 @pytest.mark.parametrize("mode", ["all", "layer"])
-def test_decode_layouts_match_the_oracle(kind, mode):
+def test_decode_layouts_match_the_oracle(kind, mode, geo):
     import torch
-    w = _w(1)
+    w = _w(1, **GEOS[geo])
     src_np = w.src_pools_numpy()
-    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block, 2,
-                               w.head_dim)
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block,
+                               wl.heads_per_shard(w.kv_heads, w.src_tp), w.head_dim)
     ref_bufs, ref_views, _, _ = decode_family(w, kind)
     oracle.relayout_general(sv, ref_views, **_tables(w))
     src = [_np_t(a) for a in src_np]
@@ -137,9 +144,10 @@ def test_layouts_with_conversion(direction):
         assert np.array_equal(t.cpu().numpy().view(dt), a)
 
 
-def test_pack_gives_pd_py_gather_and_unpack_gives_the_direct_relayout():
+@pytest.mark.parametrize("geo", sorted(GEOS))
+def test_pack_gives_pd_py_gather_and_unpack_gives_the_direct_relayout(geo):
     import torch
-    w = _w(5)
+    w = _w(5, **GEOS[geo])
     src_np = w.src_pools_numpy()
     src = [_np_t(a) for a in src_np]
     total = int(w.seq_lens.sum())

@@ -20,12 +20,20 @@ def _w(seed, **kw):
     return wl.custom("lay", seed, **base)
 
 
+# a plain head split, and heads replicated on both sides (H = 2 on 4 prefill and
+# 8 decode shards: read from the first prefill copy, written to all decode copies)
+GEOS = {"split": {}, "replicated": dict(kv_heads=2, src_tp=4, dst_tp=8, src_block=5,
+                                        dst_block=16)}
+
+
 def _std(w, pools, side):
     if side == "src":
         return oracle.standard_views(pools, w.num_layers, w.num_components, w.src_num_blocks,
-                                     w.src_block, w.kv_heads // w.src_tp, w.head_dim)
+                                     w.src_block, wl.heads_per_shard(w.kv_heads, w.src_tp),
+                                     w.head_dim)
     return oracle.standard_views(pools, w.num_layers, w.num_components, w.dst_num_blocks,
-                                 w.dst_block, w.kv_heads // w.dst_tp, w.head_dim)
+                                 w.dst_block, wl.heads_per_shard(w.kv_heads, w.dst_tp),
+                                 w.head_dim)
 
 
 def _alloc(shape, fill):
@@ -87,10 +95,11 @@ def _tables(g):
     return {k: g[k] for k in keys}
 
 
+@pytest.mark.parametrize("geo", sorted(GEOS))
 @pytest.mark.parametrize("kind", ["standard", "hnd", "kv_interleaved", "separate"])
 @pytest.mark.parametrize("mode", ["all", "layer"])
-def test_emulated_kernel_on_decode_layouts(emu, kind, mode):
-    w = _w(1)
+def test_emulated_kernel_on_decode_layouts(emu, kind, mode, geo):
+    w = _w(1, **GEOS[geo])
     src_bufs = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
     for a, b in zip(src_bufs, w.src_pools_numpy()):
         a[...] = b
@@ -105,8 +114,9 @@ def test_emulated_kernel_on_decode_layouts(emu, kind, mode):
         np.testing.assert_array_equal(a, b)
 
 
-def test_emulated_kernel_head_major_prefill(emu):
-    w = _w(2)
+@pytest.mark.parametrize("geo", sorted(GEOS))
+def test_emulated_kernel_head_major_prefill(emu, geo):
+    w = _w(2, **GEOS[geo])
     std_src = w.src_pools_numpy()
     L, C, N, B, Hl, D = w.src_shape()
     hnd = []
@@ -123,8 +133,9 @@ def test_emulated_kernel_head_major_prefill(emu):
         np.testing.assert_array_equal(a, b)
 
 
-def test_emulated_pack_and_unpack_through_a_staging_buffer(emu):
-    w = _w(3)
+@pytest.mark.parametrize("geo", sorted(GEOS))
+def test_emulated_pack_and_unpack_through_a_staging_buffer(emu, geo):
+    w = _w(3, **GEOS[geo])
     src_bufs = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
     for a, b in zip(src_bufs, w.src_pools_numpy()):
         a[...] = b

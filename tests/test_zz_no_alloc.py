@@ -47,9 +47,13 @@ def test_calls_in_a_row_match_the_allocating_entry_point():
     ragged = wl.custom("prealloc_ragged", 33, num_layers=2, num_components=2, kv_heads=6,
                        head_dim=8, elem_bytes=2, src_tp=3, dst_tp=2, src_block=3,
                        dst_block=5, seq_lens=[40, 0, 17, 1])
+    # heads replicated over TP (an MLA latent on 2 prefill and 4 decode shards)
+    replicated = wl.custom("prealloc_replicated", 35, num_layers=2, num_components=1,
+                           kv_heads=1, head_dim=576, elem_bytes=2, src_tp=2, dst_tp=4,
+                           src_block=64, dst_block=16, seq_lens=[300, 65], values="randn")
     # the second call's work list is shorter than the first's, so stale entries of
     # the first call are still in the array behind it; the third call grows again
-    for w in (big, small, ragged, big):
+    for w in (big, small, ragged, big, replicated):
         _both_paths(w)
 
 
