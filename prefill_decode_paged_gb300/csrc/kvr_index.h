@@ -121,6 +121,13 @@ struct KvrArgs {
     KvrDiv div_tasks_per_layer, div_slices;
 };
 
+// Launch modes (kernel instances).
+enum KvrMode : int32_t {
+    KVR_MODE_WHOLE = 0,           // whole prompt or a long layer range: wait, then copy
+    KVR_MODE_LAYER = 1,           // per layer: row table before the wait
+    KVR_MODE_LAYER_PREFETCH = 2,  // per layer, ordered, one wave: also prefetch the rows to L2
+};
+
 // Task -> (layer, item, chunk range [q0, q1) of the item). Chunks are units of
 // the prefill rows: with replicated decode heads each is stored to every copy.
 KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,

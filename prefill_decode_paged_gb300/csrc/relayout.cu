@@ -19,6 +19,7 @@
 // launch's tail.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <new>
 
 #include "kv_relayout.h"
@@ -45,6 +46,12 @@ __device__ __forceinline__ uint4 load_stream(const unsigned char *p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// Fetch [addr, addr + bytes) into L2 (no completion to wait for; bytes a
+// multiple of 16, addr 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(uint64_t addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
@@ -135,14 +142,18 @@ __device__ __forceinline__ void dequant16(const uint4 &c, float s, uint4 *lo, ui
 }
 
 // U: units each thread keeps in flight before its stores. CONV: KvrConv.
-// EARLY: build the first row window before waiting for the previous grid
-// (per-layer launches: hides the block-table reads in the previous launch's
-// tail; whole-prompt launches wait first, which measured 1.7 % faster there).
+// MODE: KVR_MODE_WHOLE, KVR_MODE_LAYER or KVR_MODE_LAYER_PREFETCH. Per-layer
+// modes build the first row window before waiting for the previous grid
+// (hides the block-table reads in the previous launch's tail; whole-prompt
+// launches wait first, which measured 1.7 % faster there); the prefetching
+// one also pulls those rows into L2 before the wait.
 // A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
 // REP: the plan replicates heads (a TP degree above H; see kvr_row).
-template <int U, int CONV, bool EARLY, bool REP>
+template <int U, int CONV, int MODE, bool REP>
 __global__ void __launch_bounds__(KVR_THREADS)
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
+    constexpr bool EARLY = MODE != KVR_MODE_WHOLE;
+    constexpr bool PF = MODE == KVR_MODE_LAYER_PREFETCH;
     constexpr int NL = CONV == KVR_CONV_BF16_TO_E4M3 ? 2 : 1;
     constexpr int NS = CONV == KVR_CONV_E4M3_TO_BF16 ? 2 : 1;
     constexpr uint32_t SU = 16u * NL, DU = 16u * NS;   // bytes read / written per unit
@@ -190,6 +201,11 @@ __global__ void __launch_bounds__(KVR_THREADS)
                               w0 * dc + t, &sa, &da, &fidx);
                 rows[t] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[t] = a.factors[fidx];
+            }
+            if (PF && !waited) {
+                // the first copy of each row this thread built (see the plain branch)
+                for (uint32_t t = threadIdx.x; t < t_end; t += KVR_THREADS)
+                    if (t - (t / dc) * dc == 0) prefetch_l2(rows[t].x, (uint32_t)a.g.src_row_bytes);
             }
             if (EARLY && !waited) {
                 if (!a.no_wait) {
@@ -259,6 +275,17 @@ __global__ void __launch_bounds__(KVR_THREADS)
                 rows[r - w0] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
             }
+            if (PF && !waited) {
+                // Before the grid-dependency wait, pull the prefill rows this
+                // thread just entered into L2, so the loads after the wait hit
+                // L2 instead of starting cold: the wait drains the previous
+                // grid, and its tail no longer leaves HBM idle. Correct for any
+                // previous grid: L2 is where writes from every SM meet, so rows
+                // a producer writes after this prefetch replace the prefetched
+                // lines there, and the loads after the wait see its writes.
+                for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS)
+                    prefetch_l2(rows[r - w0].x, (uint32_t)a.g.src_row_bytes);
+            }
             if (EARLY && !waited) {
                 if (!a.no_wait) {
                     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -317,27 +344,34 @@ using KvrKernel = void (*)(KvrArgs);
 // Kernel instance for a conversion, launch mode and head replication: 8 loads
 // in flight per thread for whole-prompt launches, 4 for converting per-layer
 // ones (16-element units of BF16 take two loads each).
-template <bool REP>
-KvrKernel pick_kernel_rep(int32_t conv, bool per_layer) {
+template <int MODE, bool REP>
+KvrKernel pick_instance(int32_t conv) {
+    constexpr bool LAYER = MODE != KVR_MODE_WHOLE;
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
-            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT / 2,
-                                                   KVR_CONV_BF16_TO_E4M3, true, REP>
-                             : kvr_relayout_kernel<KVR_UNROLL / 2, KVR_CONV_BF16_TO_E4M3, false,
-                                                   REP>;
+            return kvr_relayout_kernel<(LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL) / 2,
+                                       KVR_CONV_BF16_TO_E4M3, MODE, REP>;
         case KVR_CONV_E4M3_TO_BF16:
-            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER_CONVERT,
-                                                   KVR_CONV_E4M3_TO_BF16, true, REP>
-                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_E4M3_TO_BF16, false,
-                                                   REP>;
+            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL,
+                                       KVR_CONV_E4M3_TO_BF16, MODE, REP>;
         default:
-            return per_layer ? kvr_relayout_kernel<KVR_UNROLL_LAYER, KVR_CONV_NONE, true, REP>
-                             : kvr_relayout_kernel<KVR_UNROLL, KVR_CONV_NONE, false, REP>;
+            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER : KVR_UNROLL, KVR_CONV_NONE, MODE,
+                                       REP>;
     }
 }
 
-KvrKernel pick_kernel(int32_t conv, bool per_layer, bool rep) {
-    return rep ? pick_kernel_rep<true>(conv, per_layer) : pick_kernel_rep<false>(conv, per_layer);
+KvrKernel pick_kernel(int32_t conv, int mode, bool rep) {
+    switch (mode) {
+        case KVR_MODE_LAYER:
+            return rep ? pick_instance<KVR_MODE_LAYER, true>(conv)
+                       : pick_instance<KVR_MODE_LAYER, false>(conv);
+        case KVR_MODE_LAYER_PREFETCH:
+            return rep ? pick_instance<KVR_MODE_LAYER_PREFETCH, true>(conv)
+                       : pick_instance<KVR_MODE_LAYER_PREFETCH, false>(conv);
+        default:
+            return rep ? pick_instance<KVR_MODE_WHOLE, true>(conv)
+                       : pick_instance<KVR_MODE_WHOLE, false>(conv);
+    }
 }
 
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
@@ -350,6 +384,17 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     a.no_wait = no_wait ? 1 : 0;
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
+    // Ordered per-layer launches of one wave prefetch their first window's
+    // prefill rows into L2 before the grid-dependency wait: all their CTAs can
+    // be resident while the previous grid drains, so the rows arrive during
+    // its tail. Measured: 70B layers (512 CTAs, one wave) 5292 -> 6205 GB/s;
+    // launches of several waves lost 1.5-3.7 % with the prefetch in their
+    // first wave and up to 0.5 % with it in every CTA, so they go without.
+    // A launch that does not wait first has nothing to overlap.
+    int mode = per_layer ? KVR_MODE_LAYER : KVR_MODE_WHOLE;
+    if (per_layer && !no_wait && p->host.layer_resident > 0 &&
+        grid <= (uint64_t)p->host.sm_count * (uint64_t)p->host.layer_resident)
+        mode = KVR_MODE_LAYER_PREFETCH;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -362,7 +407,7 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg,
-                              pick_kernel(p->host.g.conv, per_layer, kvr_replicated(p->host.g)),
+                              pick_kernel(p->host.g.conv, mode, kvr_replicated(p->host.g)),
                               a) == cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
@@ -469,12 +514,18 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
         // the per-layer instance this plan will launch (desc is validated below)
         const bool rep = desc != nullptr && desc->kv_heads > 0 &&
                          (desc->src_tp > desc->kv_heads || desc->dst_tp > desc->kv_heads);
-        int resident = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, pick_kernel(conv, true, rep),
-                                                          KVR_THREADS, 0) != cudaSuccess) {
+        // CTAs per SM of both per-layer instances (with and without the prefetch)
+        int resident = 0, resident_pf = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &resident, pick_kernel(conv, KVR_MODE_LAYER, rep), KVR_THREADS, 0) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &resident_pf, pick_kernel(conv, KVR_MODE_LAYER_PREFETCH, rep), KVR_THREADS,
+                0) != cudaSuccess) {
             cudaGetLastError();
-            resident = 0;
+            resident = resident_pf = 0;
         }
+        resident = std::min(resident, resident_pf);
         st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, resident, &p->host,
                                  nullptr, nullptr);
     } catch (...) {
@@ -687,7 +738,8 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     // so the launch must be fully ordered after the copies.
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, pick_kernel(KVR_CONV_NONE, false, kvr_replicated(hp.g)), a) ==
+    return cudaLaunchKernelEx(&cfg, pick_kernel(KVR_CONV_NONE, KVR_MODE_WHOLE, kvr_replicated(hp.g)),
+                              a) ==
                    cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
