@@ -223,8 +223,9 @@ kvr_status check_regions(const Side &src, const Side &dst, std::vector<uint64_t>
 
 kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
                                const kvr_layout *dst_layout, const kvr_convert *cv,
-                               int sm_count, int layer_resident, KvrHostPlan *hp,
-                               int64_t *bytes_read_out, int64_t *bytes_written_out) {
+                               int sm_count, int layer_resident, int layer_resident_pf,
+                               KvrHostPlan *hp, int64_t *bytes_read_out,
+                               int64_t *bytes_written_out) {
     if (d == nullptr) return KVR_ERR_INVALID_ARG;
     const int32_t L = d->num_layers, C = d->num_components, H = d->kv_heads, D = d->head_dim;
     const int32_t es = d->elem_bytes, Tp = d->src_tp, Td = d->dst_tp;
@@ -427,25 +428,38 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     hp->avg_chunks = avg_chunks;
     hp->sm_count = sm_count;
     hp->layer_resident = layer_resident;
+    hp->layer_resident_pf = layer_resident_pf;
     hp->slices_layer = choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident);
+    // a layer whose items fit in one wave of the prefetching instance: its grid,
+    // sized to fill that wave, stays within it (choose_layer_slices)
+    hp->slices_layer_pf =
+        layer_resident_pf > 0 && n_items < (int64_t)std::max(sm_count, 1) * layer_resident_pf
+            ? choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident_pf)
+            : 0;
     hp->slices_all = kvr_range_slices(*hp, L, 0);
     return KVR_OK;
 }
 
-void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms,
-                      int32_t *slices, bool *per_layer) {
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, bool no_wait,
+                      int32_t *slices, int32_t *mode) {
     const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
     const int64_t slots = (int64_t)std::max(hp.sm_count, 1) *
                           (hp.layer_resident > 0 ? hp.layer_resident : KVR_LAYER_CTAS_PER_SM);
-    if (count == 1) {
+    const int64_t slots_pf = (int64_t)std::max(hp.sm_count, 1) * hp.layer_resident_pf;
+    if (!no_wait && tasks < slots_pf) {
+        *slices = count == 1 ? hp.slices_layer_pf
+                             : choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count,
+                                                   hp.layer_resident_pf);
+        *mode = KVR_MODE_LAYER_PREFETCH;
+    } else if (count == 1) {
         *slices = hp.slices_layer;
-        *per_layer = true;
+        *mode = KVR_MODE_LAYER;
     } else if (tasks < slots) {
         *slices = choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count, hp.layer_resident);
-        *per_layer = true;
+        *mode = KVR_MODE_LAYER;
     } else {
         *slices = kvr_range_slices(hp, count, stream_sms);
-        *per_layer = false;
+        *mode = KVR_MODE_WHOLE;
     }
 }
 
@@ -499,7 +513,7 @@ extern "C" kvr_status kv_relayout_desc_bytes_ex(const kvr_desc *desc,
     int64_t r = 0, w = 0;
     kvr_status st;
     try {
-        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, 0, 0, nullptr, &r, &w);
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, 0, 0, 0, nullptr, &r, &w);
     } catch (...) {
         return KVR_ERR_NOMEM;
     }

@@ -19,7 +19,13 @@
 #define KVR_UNROLL_LAYER 8       // the same for per-layer bit-copy launches
 #endif
 #ifndef KVR_UNROLL_LAYER_CONVERT
-#define KVR_UNROLL_LAYER_CONVERT 4  // per-layer converting launches (more registers per unit)
+#define KVR_UNROLL_LAYER_CONVERT 4  // per-layer FP8 -> BF16 launches (two stores per unit)
+#endif
+#ifndef KVR_UNROLL_LAYER_QUANT
+#define KVR_UNROLL_LAYER_QUANT 2    // per-layer BF16 -> FP8 launches: units (two loads each)
+#endif
+#ifndef KVR_UNROLL_LAYER_QUANT_PF
+#define KVR_UNROLL_LAYER_QUANT_PF 4 // the same, ordered one-wave launches (L2 prefetch)
 #endif
 #ifndef KVR_ROW_WINDOW
 #define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once
@@ -65,9 +71,12 @@ struct KvrHostPlan {
     int64_t bytes_written = 0;         // bytes one full relayout writes
     int32_t slices_all = 1;            // slices per item, whole-prompt launch
     int32_t slices_layer = 1;          // slices per item, per-layer launch
+    int32_t slices_layer_pf = 0;       // the same for the prefetching instance (ordered
+                                       // launches whose layer fits one wave of it; 0: none)
     int64_t avg_chunks = 0;            // average units of an item
     int32_t sm_count = 0;              // SMs of the device the plan was built for
     int32_t layer_resident = 0;        // CTAs of the per-layer kernel an SM holds (0: unknown)
+    int32_t layer_resident_pf = 0;     // the same for its prefetching instance
 };
 
 // Slices per item of a launch over `count` (>= 2) layers, shaped like a
@@ -80,12 +89,14 @@ struct KvrHostPlan {
 int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sms);
 
 // Shape of a kv_relayout_layers() launch over `count` layers: slices per item,
-// and whether it runs the per-layer kernel instance (true for one layer, and
-// for a range whose (layer, item) tasks fit in one wave of that kernel: such
-// a launch is short and latency-bound like a single layer's) or the
+// and the kernel instance (KvrMode). An ordered launch (no_wait false) whose
+// (layer, item) tasks fit in one wave of the prefetching per-layer instance
+// runs that instance, shaped for it; otherwise one layer, or a range whose
+// tasks fit in one wave of the per-layer instance (short and latency-bound
+// like a single layer), runs the per-layer instance; longer ranges run the
 // whole-prompt one.
-void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms,
-                      int32_t *slices, bool *per_layer);
+void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, bool no_wait,
+                      int32_t *slices, int32_t *mode);
 
 // SMs of the green context `stream` (a cudaStream_t) belongs to, or 0 when it
 // belongs to none or the driver cannot say (sm_stream.cpp).
@@ -95,12 +106,13 @@ int32_t kvr_stream_green_sms(void *stream);
 // the conversion `cv` (NULL: bit copy); when `hp` is non-NULL also build the
 // host plan for a device with `sm_count` SMs. Never touches device memory.
 // Either byte output may be NULL.
-// `layer_resident`: CTAs of the per-layer kernel one SM holds at once (0 when
-// unknown), used to shape per-layer grids.
+// `layer_resident` / `layer_resident_pf`: CTAs of the per-layer kernel and of
+// its prefetching instance one SM holds at once (0 when unknown; 0 for the
+// second: no prefetching launches), used to shape per-layer grids.
 kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
                                const kvr_layout *dst_layout, const kvr_convert *cv,
-                               int sm_count, int layer_resident, KvrHostPlan *hp,
-                               int64_t *bytes_read, int64_t *bytes_written);
+                               int sm_count, int layer_resident, int layer_resident_pf,
+                               KvrHostPlan *hp, int64_t *bytes_read, int64_t *bytes_written);
 
 // Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,

@@ -342,14 +342,20 @@ __global__ void __launch_bounds__(KVR_THREADS)
 using KvrKernel = void (*)(KvrArgs);
 
 // Kernel instance for a conversion, launch mode and head replication: 8 loads
-// in flight per thread for whole-prompt launches, 4 for converting per-layer
-// ones (16-element units of BF16 take two loads each).
+// in flight per thread, but 4 for converting per-layer launches (16-element
+// units of BF16 take two loads each to quantize and two stores to dequantize)
+// except ordered one-wave quantizing ones. Measured with 8 loads: those rose
+// 4351 -> 4592 GB/s (70B layers), while quantizing launches of several waves
+// lost 1-2 % (Qwen 32K and MLA layers, shaped for 4 instead of 6 CTAs per SM),
+// and dequantizing ones (80 registers) gained on 8B layers but not on 70B.
 template <int MODE, bool REP>
 KvrKernel pick_instance(int32_t conv) {
     constexpr bool LAYER = MODE != KVR_MODE_WHOLE;
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
-            return kvr_relayout_kernel<(LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL) / 2,
+            return kvr_relayout_kernel<MODE == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
+                                       : LAYER                        ? KVR_UNROLL_LAYER_QUANT
+                                                                      : KVR_UNROLL / 2,
                                        KVR_CONV_BF16_TO_E4M3, MODE, REP>;
         case KVR_CONV_E4M3_TO_BF16:
             return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL,
@@ -375,7 +381,7 @@ KvrKernel pick_kernel(int32_t conv, int mode, bool rep) {
 }
 
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
-                  bool per_layer, void *stream, bool no_wait = false) {
+                  int32_t mode, void *stream, bool no_wait = false) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
@@ -384,17 +390,14 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     a.no_wait = no_wait ? 1 : 0;
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
-    // Ordered per-layer launches of one wave prefetch their first window's
-    // prefill rows into L2 before the grid-dependency wait: all their CTAs can
-    // be resident while the previous grid drains, so the rows arrive during
-    // its tail. Measured: 70B layers (512 CTAs, one wave) 5292 -> 6205 GB/s;
-    // launches of several waves lost 1.5-3.7 % with the prefetch in their
-    // first wave and up to 0.5 % with it in every CTA, so they go without.
-    // A launch that does not wait first has nothing to overlap.
-    int mode = per_layer ? KVR_MODE_LAYER : KVR_MODE_WHOLE;
-    if (per_layer && !no_wait && p->host.layer_resident > 0 &&
-        grid <= (uint64_t)p->host.sm_count * (uint64_t)p->host.layer_resident)
-        mode = KVR_MODE_LAYER_PREFETCH;
+    // KVR_MODE_LAYER_PREFETCH (kvr_range_launch picks it): ordered per-layer
+    // launches of one wave prefetch their first window's prefill rows into L2
+    // before the grid-dependency wait; all their CTAs can be resident while the
+    // previous grid drains, so the rows arrive during its tail. Measured: 70B
+    // layers (512 CTAs, one wave) 5292 -> 6205 GB/s; launches of several waves
+    // lost 1.5-3.7 % with the prefetch in their first wave and up to 0.5 % with
+    // it in every CTA, so they go without. A launch that does not wait first
+    // has nothing to overlap.
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -514,7 +517,7 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
         // the per-layer instance this plan will launch (desc is validated below)
         const bool rep = desc != nullptr && desc->kv_heads > 0 &&
                          (desc->src_tp > desc->kv_heads || desc->dst_tp > desc->kv_heads);
-        // CTAs per SM of both per-layer instances (with and without the prefetch)
+        // CTAs per SM of both per-layer instances (each shapes its own grids)
         int resident = 0, resident_pf = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &resident, pick_kernel(conv, KVR_MODE_LAYER, rep), KVR_THREADS, 0) !=
@@ -525,9 +528,8 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
             cudaGetLastError();
             resident = resident_pf = 0;
         }
-        resident = std::min(resident, resident_pf);
-        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, resident, &p->host,
-                                 nullptr, nullptr);
+        st = kvr_build_host_plan(desc, src_layout, dst_layout, cv, sms, resident, resident_pf,
+                                 &p->host, nullptr, nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
@@ -588,7 +590,7 @@ extern "C" kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_c
 extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
     if (layer < 0 || layer >= plan->host.num_layers) return KVR_ERR_LAYER_RANGE;
-    return launch(plan, layer, 1, plan->host.slices_layer, true, stream);
+    return kv_relayout_layers_ex(plan, layer, 1, 0u, stream);
 }
 
 extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
@@ -598,7 +600,7 @@ extern "C" kvr_status kv_relayout_all(const kvr_plan *plan, void *stream) {
     const int32_t slices = green > 0 && green < plan->host.sm_count
                                ? kvr_range_slices(plan->host, plan->host.num_layers, green)
                                : plan->host.slices_all;
-    return launch(plan, 0, plan->host.num_layers, slices, false, stream);
+    return launch(plan, 0, plan->host.num_layers, slices, KVR_MODE_WHOLE, stream);
 }
 
 extern "C" kvr_status kv_relayout_layers_ex(const kvr_plan *plan, int32_t first, int32_t count,
@@ -606,12 +608,11 @@ extern "C" kvr_status kv_relayout_layers_ex(const kvr_plan *plan, int32_t first,
     if (plan == nullptr || (flags & ~KVR_LAUNCH_NO_WAIT) != 0) return KVR_ERR_INVALID_ARG;
     const int32_t L = plan->host.num_layers;
     if (first < 0 || count < 1 || first >= L || count > L - first) return KVR_ERR_LAYER_RANGE;
-    int32_t slices = 1;
-    bool per_layer = true;
-    kvr_range_launch(plan->host, count, count > 1 ? kvr_stream_green_sms(stream) : 0, &slices,
-                     &per_layer);
-    return launch(plan, first, count, slices, per_layer, stream,
-                  (flags & KVR_LAUNCH_NO_WAIT) != 0);
+    const bool no_wait = (flags & KVR_LAUNCH_NO_WAIT) != 0;
+    int32_t slices = 1, mode = KVR_MODE_LAYER;
+    kvr_range_launch(plan->host, count, count > 1 ? kvr_stream_green_sms(stream) : 0, no_wait,
+                     &slices, &mode);
+    return launch(plan, first, count, slices, mode, stream, no_wait);
 }
 
 extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,
@@ -632,7 +633,10 @@ extern "C" kvr_status kv_relayout_plan_launch_shape(const kvr_plan *plan, int64_
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
     const int64_t n = (int64_t)plan->host.items.size();
     if (grid_all) *grid_all = n * plan->host.num_layers * plan->host.slices_all;
-    if (grid_layer) *grid_layer = n * plan->host.slices_layer;
+    // an ordered kv_relayout_layer() launch (the prefetching shape when it has one)
+    if (grid_layer)
+        *grid_layer = n * (plan->host.slices_layer_pf > 0 ? plan->host.slices_layer_pf
+                                                          : plan->host.slices_layer);
     if (tile_tokens) *tile_tokens = plan->host.tile;
     return KVR_OK;
 }
@@ -702,7 +706,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
 
     KvrHostPlan hp;
     try {
-        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, 0, &hp, nullptr,
+        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, 0, 0, &hp, nullptr,
                                  nullptr);
     } catch (...) {
         st = KVR_ERR_NOMEM;

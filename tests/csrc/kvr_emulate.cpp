@@ -61,15 +61,16 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
              const Ranges &sr, const Ranges &dr, int sm_count, int first, int count, int copy,
              int64_t *chunks) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 4, &hp, nullptr, nullptr);
+    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, sm_count, 4, 4, &hp, nullptr, nullptr);
     if (st != KVR_OK) return st;
     if (hp.g.conv != KVR_CONV_NONE) copy = 0;   // converted values are checked on the GPU
     const int all = count < 0;
     if (!all && (first < 0 || count < 1 || first + count > hp.num_layers))
         return KVR_ERR_LAYER_RANGE;
     int32_t slices = hp.slices_all;
-    bool per_layer = false;                      // the per-layer kernel instance
-    if (!all) kvr_range_launch(hp, count, 0, &slices, &per_layer);
+    int32_t mode = KVR_MODE_WHOLE;               // the kernel instance (an ordered launch)
+    if (!all) kvr_range_launch(hp, count, 0, false, &slices, &mode);
+    const bool per_layer = mode != KVR_MODE_WHOLE;
     const int32_t layer0 = all ? 0 : first, layers = all ? hp.num_layers : count;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
                                       hp.factors.data(), hp.src_base.data(), hp.dst_base.data(),
@@ -79,8 +80,11 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     // units in flight per thread, as the kernel instance the launch picks
     const uint32_t U = hp.g.conv == KVR_CONV_NONE
                            ? (per_layer ? KVR_UNROLL_LAYER : KVR_UNROLL)
-                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL) /
-                                 (hp.g.conv == KVR_CONV_BF16_TO_E4M3 ? 2 : 1);
+                       : hp.g.conv == KVR_CONV_BF16_TO_E4M3
+                           ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
+                              : per_layer                     ? KVR_UNROLL_LAYER_QUANT
+                                                              : KVR_UNROLL / 2)
+                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
@@ -228,7 +232,7 @@ int64_t emu_relayout_range(const kvr_desc *d, int sm_count, int32_t first, int32
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].
 int32_t emu_plan_info(const kvr_desc *d, int sm_count, int64_t *out) {
     KvrHostPlan hp;
-    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, 4, &hp,
+    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, 4, 4, &hp,
                                         nullptr, nullptr);
     if (st != KVR_OK) return st;
     const int64_t n = (int64_t)hp.items.size();
