@@ -248,9 +248,11 @@ kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count
  *
  * Every launch is ordered after the kernel launched before it on `stream`:
  * the kernel may start early (programmatic dependent launch) and build its
- * work tables, but it waits for that kernel to finish before it touches a
- * pool, which is what orders a hand-off after the kernel that wrote its
- * prefill rows. KVR_LAUNCH_NO_WAIT moves that wait to the end of the launch,
+ * work tables, but it waits for that kernel to finish before it loads from
+ * or stores to a pool, which is what orders a hand-off after the kernel that
+ * wrote its prefill rows. (A per-layer launch may ask L2 to prefetch its
+ * prefill rows before that wait; the prefetch is only a cache hint, and the
+ * loads after the wait see everything the previous kernel wrote.) KVR_LAUNCH_NO_WAIT moves that wait to the end of the launch,
  * after its copies: the launch reads and writes the pools while the kernel
  * before it may still run, and still completes only after that kernel (work
  * queued after it on the stream sees both), so back-to-back hand-off

@@ -88,6 +88,39 @@ def test_layer_launch_ordered_after_the_producer_kernel():
         np.testing.assert_array_equal(b, a)
 
 
+def test_chained_hand_offs_see_the_previous_launchs_writes():
+    """A's decode pools are B's prefill pools; per-layer launches alternate A, B on one
+    stream. Each launch lets the next one start early and prefetch its prefill rows
+    into L2 while the previous launch may still be writing them; B must still read
+    what A wrote (the oracle applied twice), layer after layer."""
+    import dataclasses
+    import torch
+    a = wl.custom("chainA", 21, num_layers=4, num_components=2, kv_heads=8, head_dim=128,
+                  elem_bytes=2, src_tp=2, dst_tp=4, src_block=16, dst_block=32,
+                  seq_lens=[300, 77, 1])
+    # B reads A's decode side: same shards, blocks and tables; writes 1 shard of 64-token blocks
+    b0 = wl.custom("chainB", 22, num_layers=4, num_components=2, kv_heads=8, head_dim=128,
+                   elem_bytes=2, src_tp=4, dst_tp=1, src_block=32, dst_block=64,
+                   seq_lens=[300, 77, 1])
+    b = dataclasses.replace(b0, src_num_blocks=a.dst_num_blocks, src_off=a.dst_off,
+                            src_bt=a.dst_bt)
+    src_np = a.src_pools_numpy()
+    mid_ref = _ref(a, src_np)
+    want = _ref(b, mid_ref)
+    src = to_device(src_np, 2)
+    for _ in range(3):
+        mid = to_device(a.dst_pools_numpy(), 2)
+        dst = to_device(b.dst_pools_numpy(), 2)
+        with RelayoutPlan(src, mid, **a.geometry()) as pa, \
+                RelayoutPlan(mid, dst, **b.geometry()) as pb:
+            for layer in range(a.num_layers):
+                pa.run_layer(layer)
+                pb.run_layer(layer)
+            torch.cuda.synchronize()
+        for x, y in zip(want, to_host(dst, b)):
+            np.testing.assert_array_equal(y, x)
+
+
 def test_captured_in_a_cuda_graph_and_replayed():
     import torch
     w = _small()
