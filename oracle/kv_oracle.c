@@ -22,7 +22,7 @@
  *   - section "传输的代价": KV per token times prompt length is the amount
  *     of data moved.
  *
- * Readings taken where the page is silent (each is listed in the design doc):
+ * Readings taken where the page is silent:
  *   - pool layout, one buffer per TP shard: [L][C][N][B][H_local][D] of
  *     es-byte elements (C = 2 for K and V, C = 1 for an MLA latent);
  *   - TP shard s holds the contiguous head range [s*H/T, (s+1)*H/T) when
