@@ -83,7 +83,8 @@ typedef enum kvr_status {
     KVR_ERR_NOMEM = -9,         /* host or device allocation of the plan failed */
     KVR_ERR_POOL_OVERLAP = -10, /* a decode pool overlaps another decode pool or a prefill pool */
     KVR_ERR_SCRATCH_LIMIT = -11, /* kv_relayout_all_prealloc: work list larger than its scratch */
-    KVR_ERR_POOL_ADDRESS = -12  /* a pool's first or last byte is not memory this GPU can access */
+    KVR_ERR_POOL_ADDRESS = -12, /* a pool's first or last byte is not memory this GPU can access */
+    KVR_ERR_DEVICE_BOUNDS = -13 /* checked builds: a launch computed a row outside its pools */
 } kvr_status;
 
 typedef struct kvr_desc {
@@ -348,6 +349,29 @@ void kv_relayout_sm_stream_destroy(kvr_sm_stream *s);
  *  - The host arrays of *desc may be freed when the call returns.
  */
 kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *stream);
+
+/*
+ * Device-side address checks (test builds). The library can be compiled with
+ * KVR_DEVICE_CHECKS defined (prefill_decode_paged_gb300.build.build_checked()):
+ * its kernels then check, for every row of every launch of a plan made by
+ * kv_relayout_plan*(), that the row's prefill bytes lie inside the prefill
+ * pools (views) and its decode bytes inside the decode pools, as the plan
+ * validated them; a row that does not is counted in an error word and not
+ * read, prefetched or written. The checks catch a disagreement between the
+ * plan's validation and the kernel's address arithmetic on the GPU itself,
+ * without ever touching memory outside the pools. Product builds skip them.
+ *
+ * kv_relayout_debug_status(): waits for the device (cudaDeviceSynchronize),
+ * reads and clears the plan's error word into *flags (may be NULL); returns
+ * KVR_ERR_DEVICE_BOUNDS if a row was dropped since the last call, KVR_OK if
+ * not, KVR_ERR_UNSUPPORTED in a product build.
+ * kv_relayout_debug_narrow(): makes the checks treat the last `bytes` bytes of
+ * every pool region as outside it (to test that the checks fire; those rows
+ * are then dropped, the others still move); KVR_ERR_UNSUPPORTED in a product
+ * build. kv_relayout_all_prealloc() launches are not checked.
+ */
+kvr_status kv_relayout_debug_status(const kvr_plan *plan, uint32_t *flags);
+kvr_status kv_relayout_debug_narrow(kvr_plan *plan, int64_t bytes);
 
 #ifdef __cplusplus
 }

@@ -119,7 +119,22 @@ struct KvrArgs {
                                         // before them (the caller's call)
     uint32_t tasks_per_layer;           // n_items * slices
     KvrDiv div_tasks_per_layer, div_slices;
+#ifdef KVR_DEVICE_CHECKS
+    // Checked builds only: [lo, hi) byte ranges the prefill rows (the first
+    // n_src_regions pairs) and decode rows (the next n_dst_regions) must lie in;
+    // NULL: no check. A row outside them sets *check_error and is dropped.
+    const uint64_t *check_regions;
+    int32_t n_src_regions, n_dst_regions;
+    unsigned int *check_error;
+#endif
 };
+
+// Does [a, a + bytes) lie inside one of the n [lo, hi) pairs of `reg`?
+KVR_HD bool kvr_span_in(const uint64_t *reg, int32_t n, uint64_t a, uint64_t bytes) {
+    for (int32_t k = 0; k < n; ++k)
+        if (a >= reg[2 * k] && a + bytes <= reg[2 * k + 1]) return true;
+    return false;
+}
 
 // Launch modes (kernel instances).
 enum KvrMode : int32_t {

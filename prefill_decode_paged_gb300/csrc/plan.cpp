@@ -551,6 +551,7 @@ extern "C" const char *kv_relayout_strerror(kvr_status s) {
         case KVR_ERR_POOL_OVERLAP: return "decode pool overlaps another pool";
         case KVR_ERR_SCRATCH_LIMIT: return "work list larger than the preallocated scratch";
         case KVR_ERR_POOL_ADDRESS: return "pool is not memory this GPU can access";
+        case KVR_ERR_DEVICE_BOUNDS: return "a row fell outside its pools (checked build)";
     }
     return "unknown status";
 }

@@ -36,6 +36,10 @@ struct kvr_plan {
     const int32_t *dev_dbt = nullptr;
     const float *dev_factors = nullptr;
     int device = 0;
+#ifdef KVR_DEVICE_CHECKS
+    uint64_t *dev_regions = nullptr;      // checked builds: the pool regions, then the error word
+    unsigned int *dev_check_error = nullptr;
+#endif
 };
 
 namespace {
@@ -53,6 +57,29 @@ __device__ __forceinline__ uint4 load_stream(const unsigned char *p) {
 __device__ __forceinline__ void prefetch_l2(uint64_t addr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
+
+#ifdef KVR_DEVICE_CHECKS
+// Checked builds: a row whose prefill or decode bytes leave the plan's pool
+// regions is flagged in *check_error and dropped (both addresses 0: nothing
+// is read, prefetched or written for it).
+__device__ __forceinline__ void kvr_check_row(const KvrArgs &a, uint64_t *sa, uint64_t *da) {
+    if (a.check_regions == nullptr) return;
+    if (!kvr_span_in(a.check_regions, a.n_src_regions, *sa, (uint64_t)a.g.src_row_bytes) ||
+        !kvr_span_in(a.check_regions + 2 * a.n_src_regions, a.n_dst_regions, *da,
+                     (uint64_t)a.g.dst_row_bytes)) {
+        atomicOr(a.check_error, 1u);
+        *sa = 0;
+        *da = 0;
+    }
+}
+#define KVR_CHECK_ROW(a, sa, da) kvr_check_row((a), &(sa), &(da))
+#define KVR_SRC_DROPPED(row) ((row).x == 0)
+#define KVR_DST_DROPPED(row) ((row).y == 0)
+#else
+#define KVR_CHECK_ROW(a, sa, da) ((void)0)
+#define KVR_SRC_DROPPED(row) false
+#define KVR_DST_DROPPED(row) false
+#endif
 
 __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
@@ -199,13 +226,15 @@ __global__ void __launch_bounds__(KVR_THREADS)
                 uint64_t sa, da;
                 kvr_row<true>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base,
                               w0 * dc + t, &sa, &da, &fidx);
+                KVR_CHECK_ROW(a, sa, da);
                 rows[t] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[t] = a.factors[fidx];
             }
             if (PF && !waited) {
                 // the first copy of each row this thread built (see the plain branch)
                 for (uint32_t t = threadIdx.x; t < t_end; t += KVR_THREADS)
-                    if (t - (t / dc) * dc == 0) prefetch_l2(rows[t].x, (uint32_t)a.g.src_row_bytes);
+                    if (t - (t / dc) * dc == 0 && !KVR_SRC_DROPPED(rows[t]))
+                        prefetch_l2(rows[t].x, (uint32_t)a.g.src_row_bytes);
             }
             if (EARLY && !waited) {
                 if (!a.no_wait) {
@@ -227,9 +256,12 @@ __global__ void __launch_bounds__(KVR_THREADS)
                         const uint32_t r = a.g.div_rc.div(q);
                         const uint32_t u = q - r * rc;
                         const ulonglong2 p = rows[(r - w0) * dc];
+                        if (!KVR_SRC_DROPPED(p)) {
 #pragma unroll
-                        for (int j = 0; j < NL; ++j)
-                            v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                            for (int j = 0; j < NL; ++j)
+                                v[k][j] =
+                                    load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                        }
                         if (CONV != KVR_CONV_NONE) f[k] = row_factor[(r - w0) * dc];
                     }
                 }
@@ -242,6 +274,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
                     const uint32_t r = a.g.div_rc.div(q);
                     const uint32_t u = q - r * rc;
                     const uint32_t ti = (r - w0) * dc;
+                    if (KVR_SRC_DROPPED(rows[ti])) continue;
                     uint4 lo, hi;
                     if (CONV == KVR_CONV_NONE) {
                         lo = v[k][0];
@@ -251,6 +284,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
                         dequant16(v[k][0], f[k], &lo, &hi);
                     }
                     for (uint32_t c = 0; c < dc; ++c) {
+                        if (KVR_DST_DROPPED(rows[ti + c])) continue;
                         unsigned char *to = (unsigned char *)rows[ti + c].y + u * DU;
                         store_stream(to, lo);
                         if (CONV == KVR_CONV_E4M3_TO_BF16) store_stream(to + 16, hi);
@@ -272,6 +306,7 @@ __global__ void __launch_bounds__(KVR_THREADS)
                 uint64_t sa, da;
                 kvr_row<false>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa,
                                &da, &fidx);
+                KVR_CHECK_ROW(a, sa, da);
                 rows[r - w0] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
             }
@@ -284,7 +319,8 @@ __global__ void __launch_bounds__(KVR_THREADS)
                 // a producer writes after this prefetch replace the prefetched
                 // lines there, and the loads after the wait see its writes.
                 for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS)
-                    prefetch_l2(rows[r - w0].x, (uint32_t)a.g.src_row_bytes);
+                    if (!KVR_SRC_DROPPED(rows[r - w0]))
+                        prefetch_l2(rows[r - w0].x, (uint32_t)a.g.src_row_bytes);
             }
             if (EARLY && !waited) {
                 if (!a.no_wait) {
@@ -309,10 +345,13 @@ __global__ void __launch_bounds__(KVR_THREADS)
                         const uint32_t r = a.g.div_rc.div(q);
                         const uint32_t u = q - r * rc;
                         const ulonglong2 p = rows[r - w0];
+                        if (!KVR_SRC_DROPPED(p)) {
 #pragma unroll
-                        for (int j = 0; j < NL; ++j)
-                            v[k][j] = load_stream((const unsigned char *)p.x + u * SU + 16u * j);
-                        to[k] = (unsigned char *)p.y + u * DU;
+                            for (int j = 0; j < NL; ++j)
+                                v[k][j] =
+                                    load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                            to[k] = (unsigned char *)p.y + u * DU;
+                        }
                         if (CONV != KVR_CONV_NONE) f[k] = row_factor[r - w0];
                     }
                 }
@@ -388,6 +427,12 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt, p->dev_factors,
                                 p->dev_src_base, p->dev_dst_base, layer0, slices);
     a.no_wait = no_wait ? 1 : 0;
+#ifdef KVR_DEVICE_CHECKS
+    a.check_regions = p->dev_regions;
+    a.n_src_regions = (int32_t)(p->host.src_regions.size() / 2);
+    a.n_dst_regions = (int32_t)(p->host.dst_regions.size() / 2);
+    a.check_error = p->dev_check_error;
+#endif
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
     // KVR_MODE_LAYER_PREFETCH (kvr_range_launch picks it): ordered per-layer
@@ -495,6 +540,29 @@ DevTables place_tables(const KvrHostPlan &hp, unsigned char *base, Piece pieces[
     return t;
 }
 
+#ifdef KVR_DEVICE_CHECKS
+// Checked builds: copy the plan's merged pool regions (prefill, then decode) to
+// the device, followed by a zeroed error word (allocated on the first call).
+kvr_status upload_regions(kvr_plan *p) {
+    const std::vector<uint64_t> &sr = p->host.src_regions, &dr = p->host.dst_regions;
+    const size_t n = sr.size() + dr.size();
+    if (p->dev_regions == nullptr) {
+        if (cudaMalloc(&p->dev_regions, (n + 2) * sizeof(uint64_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return KVR_ERR_CUDA;
+        }
+        p->dev_check_error = (unsigned int *)(p->dev_regions + n);
+    }
+    std::vector<uint64_t> all(sr);
+    all.insert(all.end(), dr.begin(), dr.end());
+    if ((n > 0 && cudaMemcpy(p->dev_regions, all.data(), n * sizeof(uint64_t),
+                             cudaMemcpyHostToDevice) != cudaSuccess) ||
+        cudaMemset(p->dev_check_error, 0, sizeof(unsigned int)) != cudaSuccess)
+        return KVR_ERR_CUDA;
+    return KVR_OK;
+}
+#endif
+
 }  // namespace
 
 static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
@@ -564,6 +632,12 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
         p->dev_dbt = t.dbt;
         p->dev_factors = t.factors;
     }
+#ifdef KVR_DEVICE_CHECKS
+    if (upload_regions(p) != KVR_OK) {
+        kv_relayout_plan_destroy(p);
+        return KVR_ERR_CUDA;
+    }
+#endif
     *out = p;
     return KVR_OK;
 }
@@ -644,7 +718,45 @@ extern "C" kvr_status kv_relayout_plan_launch_shape(const kvr_plan *plan, int64_
 extern "C" void kv_relayout_plan_destroy(kvr_plan *plan) {
     if (plan == nullptr) return;
     if (plan->dev_meta != nullptr) cudaFree(plan->dev_meta);
+#ifdef KVR_DEVICE_CHECKS
+    if (plan->dev_regions != nullptr) cudaFree(plan->dev_regions);
+#endif
     delete plan;
+}
+
+extern "C" kvr_status kv_relayout_debug_status(const kvr_plan *plan, uint32_t *flags) {
+    if (flags != nullptr) *flags = 0;
+#ifdef KVR_DEVICE_CHECKS
+    if (plan == nullptr) return KVR_ERR_INVALID_ARG;
+    unsigned int word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, plan->dev_check_error, sizeof(word), cudaMemcpyDeviceToHost) !=
+            cudaSuccess ||
+        cudaMemset(plan->dev_check_error, 0, sizeof(word)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return KVR_ERR_CUDA;
+    if (flags != nullptr) *flags = word;
+    return word != 0 ? KVR_ERR_DEVICE_BOUNDS : KVR_OK;
+#else
+    (void)plan;
+    return KVR_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" kvr_status kv_relayout_debug_narrow(kvr_plan *plan, int64_t bytes) {
+#ifdef KVR_DEVICE_CHECKS
+    if (plan == nullptr || bytes < 0) return KVR_ERR_INVALID_ARG;
+    for (std::vector<uint64_t> *regs : {&plan->host.src_regions, &plan->host.dst_regions})
+        for (size_t k = 0; k + 1 < regs->size(); k += 2)
+            (*regs)[k + 1] = (*regs)[k + 1] - (*regs)[k] > (uint64_t)bytes
+                                 ? (*regs)[k + 1] - (uint64_t)bytes
+                                 : (*regs)[k];
+    return upload_regions(plan);
+#else
+    (void)plan;
+    (void)bytes;
+    return KVR_ERR_UNSUPPORTED;
+#endif
 }
 
 // ---------------------------------------------------------------------------

@@ -21,7 +21,7 @@ STATUS = {
     -3: "KVR_ERR_ALIGNMENT", -4: "KVR_ERR_BLOCK_RANGE", -5: "KVR_ERR_TABLE_SHORT",
     -6: "KVR_ERR_DST_ALIAS", -7: "KVR_ERR_LAYER_RANGE", -8: "KVR_ERR_CUDA",
     -9: "KVR_ERR_NOMEM", -10: "KVR_ERR_POOL_OVERLAP", -11: "KVR_ERR_SCRATCH_LIMIT",
-    -12: "KVR_ERR_POOL_ADDRESS",
+    -12: "KVR_ERR_POOL_ADDRESS", -13: "KVR_ERR_DEVICE_BOUNDS",
 }
 PREALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
@@ -29,7 +29,8 @@ EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_strerror", "kv_relayout_all_prealloc", "kv_relayout_desc_convert_bytes",
            "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
            "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy",
-           "kv_relayout_plan_launch_shape", "kv_relayout_layers", "kv_relayout_layers_ex")
+           "kv_relayout_plan_launch_shape", "kv_relayout_layers", "kv_relayout_layers_ex",
+           "kv_relayout_debug_status", "kv_relayout_debug_narrow")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 LAUNCH_NO_WAIT = 1
@@ -78,44 +79,61 @@ def library() -> ctypes.CDLL:
             raise RuntimeError(
                 f"CUDA library {LIB_PATH} is missing: build it first "
                 "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(LIB_PATH)
-        i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
-        lib.kv_relayout_desc_bytes.restype = i32
-        lib.kv_relayout_desc_bytes.argtypes = [p, p, p]
-        lib.kv_relayout_plan.restype = i32
-        lib.kv_relayout_plan.argtypes = [p, p]
-        lib.kv_relayout_layer.restype = i32
-        lib.kv_relayout_layer.argtypes = [p, i32, p]
-        lib.kv_relayout_all.restype = i32
-        lib.kv_relayout_all.argtypes = [p, p]
-        lib.kv_relayout_plan_bytes.restype = i32
-        lib.kv_relayout_plan_bytes.argtypes = [p, p, p]
-        lib.kv_relayout_plan_destroy.restype = None
-        lib.kv_relayout_plan_destroy.argtypes = [p]
-        lib.kv_relayout_strerror.restype = ctypes.c_char_p
-        lib.kv_relayout_strerror.argtypes = [i32]
-        lib.kv_relayout_all_prealloc.restype = i32
-        lib.kv_relayout_all_prealloc.argtypes = [p, p]
-        lib.kv_relayout_desc_convert_bytes.restype = i32
-        lib.kv_relayout_desc_convert_bytes.argtypes = [p, p, p, p]
-        lib.kv_relayout_plan_convert.restype = i32
-        lib.kv_relayout_plan_convert.argtypes = [p, p, p]
-        lib.kv_relayout_desc_bytes_ex.restype = i32
-        lib.kv_relayout_desc_bytes_ex.argtypes = [p, p, p, p, p, p]
-        lib.kv_relayout_plan_ex.restype = i32
-        lib.kv_relayout_plan_ex.argtypes = [p, p, p, p, p]
-        lib.kv_relayout_sm_stream_create.restype = i32
-        lib.kv_relayout_sm_stream_create.argtypes = [i32, p, p, p]
-        lib.kv_relayout_sm_stream_destroy.restype = None
-        lib.kv_relayout_sm_stream_destroy.argtypes = [p]
-        lib.kv_relayout_plan_launch_shape.restype = i32
-        lib.kv_relayout_plan_launch_shape.argtypes = [p, p, p, p]
-        lib.kv_relayout_layers.restype = i32
-        lib.kv_relayout_layers.argtypes = [p, i32, i32, p]
-        lib.kv_relayout_layers_ex.restype = i32
-        lib.kv_relayout_layers_ex.argtypes = [p, i32, i32, ctypes.c_uint32, p]
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
     return _lib
+
+
+def checked_library() -> ctypes.CDLL:
+    """The library built with device-side address checks (tests only): the same C ABI,
+    plus working ``kv_relayout_debug_status`` / ``kv_relayout_debug_narrow``. Builds it
+    on first use. Call its functions directly with a ``_Desc``; ``RelayoutPlan`` uses
+    the product library."""
+    from . import build as kbuild
+    return _bind(ctypes.CDLL(kbuild.build_checked()))
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded copy of the library."""
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.kv_relayout_desc_bytes.restype = i32
+    lib.kv_relayout_desc_bytes.argtypes = [p, p, p]
+    lib.kv_relayout_plan.restype = i32
+    lib.kv_relayout_plan.argtypes = [p, p]
+    lib.kv_relayout_layer.restype = i32
+    lib.kv_relayout_layer.argtypes = [p, i32, p]
+    lib.kv_relayout_all.restype = i32
+    lib.kv_relayout_all.argtypes = [p, p]
+    lib.kv_relayout_plan_bytes.restype = i32
+    lib.kv_relayout_plan_bytes.argtypes = [p, p, p]
+    lib.kv_relayout_plan_destroy.restype = None
+    lib.kv_relayout_plan_destroy.argtypes = [p]
+    lib.kv_relayout_strerror.restype = ctypes.c_char_p
+    lib.kv_relayout_strerror.argtypes = [i32]
+    lib.kv_relayout_all_prealloc.restype = i32
+    lib.kv_relayout_all_prealloc.argtypes = [p, p]
+    lib.kv_relayout_desc_convert_bytes.restype = i32
+    lib.kv_relayout_desc_convert_bytes.argtypes = [p, p, p, p]
+    lib.kv_relayout_plan_convert.restype = i32
+    lib.kv_relayout_plan_convert.argtypes = [p, p, p]
+    lib.kv_relayout_desc_bytes_ex.restype = i32
+    lib.kv_relayout_desc_bytes_ex.argtypes = [p, p, p, p, p, p]
+    lib.kv_relayout_plan_ex.restype = i32
+    lib.kv_relayout_plan_ex.argtypes = [p, p, p, p, p]
+    lib.kv_relayout_sm_stream_create.restype = i32
+    lib.kv_relayout_sm_stream_create.argtypes = [i32, p, p, p]
+    lib.kv_relayout_sm_stream_destroy.restype = None
+    lib.kv_relayout_sm_stream_destroy.argtypes = [p]
+    lib.kv_relayout_plan_launch_shape.restype = i32
+    lib.kv_relayout_plan_launch_shape.argtypes = [p, p, p, p]
+    lib.kv_relayout_layers.restype = i32
+    lib.kv_relayout_layers.argtypes = [p, i32, i32, p]
+    lib.kv_relayout_layers_ex.restype = i32
+    lib.kv_relayout_layers_ex.argtypes = [p, i32, i32, ctypes.c_uint32, p]
+    lib.kv_relayout_debug_status.restype = i32
+    lib.kv_relayout_debug_status.argtypes = [p, p]
+    lib.kv_relayout_debug_narrow.restype = i32
+    lib.kv_relayout_debug_narrow.argtypes = [p, i64]
+    return lib
 
 
 def _strerror(status: int) -> str:

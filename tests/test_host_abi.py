@@ -93,6 +93,15 @@ def test_library_exports_every_declared_symbol(cuda_lib):
     assert set(names) <= exported
 
 
+def test_product_library_has_no_device_checks(cuda_lib):
+    """The device-side address checks exist only in the checked test build."""
+    flags = ctypes.c_uint32(7)
+    assert kr.STATUS[cuda_lib.kv_relayout_debug_status(None, ctypes.byref(flags))] == \
+        "KVR_ERR_UNSUPPORTED"
+    assert flags.value == 0
+    assert kr.STATUS[cuda_lib.kv_relayout_debug_narrow(None, 0)] == "KVR_ERR_UNSUPPORTED"
+
+
 def test_strerror_names_every_status(cuda_lib):
     for code in kr.STATUS:
         assert cuda_lib.kv_relayout_strerror(code)
