@@ -4,7 +4,7 @@ In the checked build every row a launch computes is compared, on the GPU, with
 the pool regions the plan validated before anything is read or written; a row
 outside them is counted in an error word and dropped. These tests run that build
 over the parity cases (head splits, odd blocks, replicated heads), every launch
-mode, both conversions and two full-size workloads, and require a clear error
+mode, both conversions and every full-size workload, and require a clear error
 word and the oracle's bytes. Then they narrow the checked regions so that the
 check must fire: the rows it drops stay at their sentinel, every other row still
 moves, and no access ever leaves the pools (a dropped row is simply not touched).
@@ -140,7 +140,8 @@ def test_checked_converting_kernels(clib, direction):
             assert np.array_equal(t.cpu().numpy().view(dnp), a)
 
 
-@pytest.mark.parametrize("name", ["llama70b", "dsv3mla_tp8"])
+@pytest.mark.parametrize("name", ["llama8b", "llama70b", "qwen32k_ragged", "dsv3mla",
+                                  "dsv3mla_tp8"])
 def test_checked_kernels_on_full_size_workloads(clib, name):
     """Every row of the whole-prompt and of every per-layer launch, checked on the GPU."""
     w = wl.get(name)
