@@ -194,3 +194,24 @@ def test_narrowed_regions_make_the_check_fire(clib):
         assert np.all((last == want) | (last == sentinel))
         dropped += int(((last == sentinel) & (want != sentinel)).sum())
     assert dropped > 0
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_checked_kernels_on_fuzzed_geometries(clib, seed):
+    """Random valid geometries (TP splits and replication, block sizes 1-256, element
+    widths, ragged and empty prompts, shared prefixes), every launch mode."""
+    from fuzz_cases import random_workload
+    w = random_workload(seed + 100, max_tokens=400)
+    src_np = w.src_pools_numpy()
+    ref = _oracle(w, src_np)
+    src = to_device(src_np, w.elem_bytes)
+    for mode in ("all", "layer", "ranges"):
+        dst = to_device(w.dst_pools_numpy(), w.elem_bytes)
+        p = _Plan(clib, w, src, dst)
+        try:
+            p.run(mode, w.num_layers)
+            assert p.status() == ("KVR_OK", 0), mode
+        finally:
+            p.close()
+        for s, (a, b) in enumerate(zip(ref, to_host(dst, w))):
+            np.testing.assert_array_equal(b, a, err_msg=f"seed {seed} {mode} shard {s}")
