@@ -586,8 +586,23 @@ def run_ours(args):
                 ext.synchronize()
                 windows.append((th, time.time()))
                 ms = e0.elapsed_time(e1) / steps
+                # the same hand-off layer by layer (L ordered launches per step)
+                for layer in range(L):
+                    plan.run_layer(layer, sms.handle)
+                ext.synchronize()
+                th = time.time()
+                e0.record(ext)
+                for _ in range(steps):
+                    for layer in range(L):
+                        plan.run_layer(layer, sms.handle)
+                e1.record(ext)
+                ext.synchronize()
+                windows.append((th, time.time()))
+                ms_l = e0.elapsed_time(e1) / steps
                 sm_sweep[str(sms.sms)] = {"gbs": round(bytes_step / (ms * 1e-3) / 1e9, 1),
-                                          "ms_per_step": round(ms, 4)}
+                                          "ms_per_step": round(ms, 4),
+                                          "per_layer_gbs": round(
+                                              bytes_step / (ms_l * 1e-3) / 1e9, 1)}
 
     # e2e: the pools live in pinned host memory; every step hands the batch over
     # through the public no-allocation call, whose kernel reads the prefill rows

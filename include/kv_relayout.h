@@ -305,7 +305,9 @@ const char *kv_relayout_strerror(kvr_status status);
  * the device's split granularity (8 SMs on this GPU generation);
  * *sms_granted receives the SMs the stream got. The stream is a cudaStream_t
  * for kv_relayout_layer() / kv_relayout_all() and any other launch; it shares
- * memory with the rest of the process. Errors: KVR_ERR_INVALID_ARG for a
+ * memory with the rest of the process. Relayout launches on such a stream
+ * shape their grids for its SMs (they ask the driver which green context the
+ * stream belongs to at each launch). Errors: KVR_ERR_INVALID_ARG for a
  * count outside [1, SMs], KVR_ERR_UNSUPPORTED when the driver has no green
  * contexts or cannot split, KVR_ERR_CUDA for other driver failures.
  * Destroy it (after its work is done) with kv_relayout_sm_stream_destroy().

@@ -443,19 +443,22 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
 void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, bool no_wait,
                       int32_t *slices, int32_t *mode) {
     const int64_t tasks = (int64_t)count * (int64_t)hp.items.size();
-    const int64_t slots = (int64_t)std::max(hp.sm_count, 1) *
+    const bool limited = stream_sms > 0 && stream_sms < hp.sm_count;
+    const int32_t sms = limited ? stream_sms : hp.sm_count;
+    const int64_t slots = (int64_t)std::max(sms, 1) *
                           (hp.layer_resident > 0 ? hp.layer_resident : KVR_LAYER_CTAS_PER_SM);
-    const int64_t slots_pf = (int64_t)std::max(hp.sm_count, 1) * hp.layer_resident_pf;
+    const int64_t slots_pf = (int64_t)std::max(sms, 1) * hp.layer_resident_pf;
     if (!no_wait && tasks < slots_pf) {
-        *slices = count == 1 ? hp.slices_layer_pf
-                             : choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count,
-                                                   hp.layer_resident_pf);
+        *slices = count == 1 && !limited
+                      ? hp.slices_layer_pf
+                      : choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident_pf);
         *mode = KVR_MODE_LAYER_PREFETCH;
     } else if (count == 1) {
-        *slices = hp.slices_layer;
+        *slices = limited ? choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident)
+                          : hp.slices_layer;
         *mode = KVR_MODE_LAYER;
     } else if (tasks < slots) {
-        *slices = choose_layer_slices(tasks, hp.avg_chunks, hp.sm_count, hp.layer_resident);
+        *slices = choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident);
         *mode = KVR_MODE_LAYER;
     } else {
         *slices = kvr_range_slices(hp, count, stream_sms);

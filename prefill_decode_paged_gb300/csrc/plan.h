@@ -88,13 +88,16 @@ struct KvrHostPlan {
 // prologue, so items are only sliced to fill those SMs.
 int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sms);
 
-// Shape of a kv_relayout_layers() launch over `count` layers: slices per item,
-// and the kernel instance (KvrMode). An ordered launch (no_wait false) whose
-// (layer, item) tasks fit in one wave of the prefetching per-layer instance
-// runs that instance, shaped for it; otherwise one layer, or a range whose
-// tasks fit in one wave of the per-layer instance (short and latency-bound
-// like a single layer), runs the per-layer instance; longer ranges run the
-// whole-prompt one.
+// Shape of a kv_relayout_layers() launch over `count` layers on a stream with
+// `stream_sms` SMs (0 or the device's count: the whole device): slices per
+// item, and the kernel instance (KvrMode). An ordered launch (no_wait false)
+// whose (layer, item) tasks fit in one wave of the prefetching per-layer
+// instance on those SMs runs that instance, shaped for it; otherwise one
+// layer, or a range whose tasks fit in one wave of the per-layer instance
+// (short and latency-bound like a single layer), runs the per-layer instance;
+// longer ranges run the whole-prompt one. Per-layer grids on fewer SMs are
+// shaped for those SMs (on 16-96 of 152 SMs, 80 ordered 70B layers ran 5-29 %
+// faster than with the whole device's shape).
 void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, bool no_wait,
                       int32_t *slices, int32_t *mode);
 
