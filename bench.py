@@ -89,10 +89,11 @@ def parse_args(argv=None):
     p.add_argument("--sm-sweep", default="",
                    help="comma-separated SM counts: also time the whole-prompt relayout on "
                         "streams limited to that many SMs (green contexts)")
-    p.add_argument("--modes", default="all,layer,graph,groups",
+    p.add_argument("--modes", default="all,layer,graph,groups,overlap",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA "
-                        "graph), groups (launches of --groups layers each, from a CUDA graph)")
+                        "graph), groups (launches of --groups layers each, from a CUDA graph), "
+                        "overlap (70B: the hand-off beside a stand-in for the prefill compute)")
     p.add_argument("--groups", default="2,4,8,16",
                    help="layers per launch for the groups measurement")
     return p.parse_args(argv)
@@ -432,6 +433,91 @@ def host_threads():
 
 # -- our arm --------------------------------------------------------------------------
 
+def overlap_measure(plan, w, dev, stream, prompts=9):
+    """The hand-off beside the prefill compute it belongs to. Stand-in for one layer's
+    prefill compute: one bf16 GEMM (cuBLAS) with the FLOPs of a Llama-3-70B layer's
+    linear layers for the prompt, [tokens, 8192] x [8192, 104448] (output columns:
+    QKV 10240, O 8192, MLP gate and up 57344, down 28672; attention left out).
+    Arrangements, per prompt: serial (the L GEMMs, then the whole-prompt hand-off on
+    the same stream); layerwise (each layer handed over on a second stream as soon
+    as its GEMM is done); layerwise_16sm (the same on a stream limited to 16 SMs).
+    Per prompt, events give the span of the GEMMs (first start to last end) and the
+    tail: from the last GEMM's end to the end of the hand-off, the time a decode
+    instance waits once prefill is done. Medians over `prompts` prompts per
+    arrangement, taken in rotation; the GEMM span of each is set beside the GEMMs
+    alone with its spread, which bounds how much the hand-off slows the compute."""
+    import torch
+    from prefill_decode_paged_gb300 import KVRelayoutError, SmStream
+    tokens = int(w.seq_lens.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    a = torch.randn(tokens, 8192, device=dev, dtype=torch.bfloat16, generator=g)
+    b = torch.randn(8192, 104448, device=dev, dtype=torch.bfloat16, generator=g) * 0.01
+    c = torch.empty(tokens, 104448, device=dev, dtype=torch.bfloat16)
+    L = w.num_layers
+    side = torch.cuda.Stream(dev)
+    done = [torch.cuda.Event() for _ in range(L)]
+    try:
+        sms = SmStream(16)
+    except KVRelayoutError:
+        sms = None
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def prompt(kind, handle=None, join=None):
+        """One prompt; returns (start, last GEMM end, hand-off end) events."""
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        for layer in range(L):
+            torch.mm(a, b, out=c)
+            if kind == "layerwise":
+                done[layer].record(stream)
+                join.wait_event(done[layer])
+                plan.run_layer(layer, handle)
+        e1.record(stream)
+        if kind == "serial":
+            plan.run_all(stream)
+        elif kind == "layerwise":
+            stream.wait_stream(join)
+        e2.record(stream)
+        return e0, e1, e2
+
+    arrangements = {"compute": lambda: prompt("compute"), "serial": lambda: prompt("serial"),
+                    "layerwise": lambda: prompt("layerwise", side, side)}
+    if sms is not None:
+        ext = torch.cuda.ExternalStream(sms.handle, device=dev)
+        arrangements["layerwise_16sm"] = lambda: prompt("layerwise", sms.handle, ext)
+    span = {k: [] for k in arrangements}
+    tail = {k: [] for k in arrangements}
+    with torch.cuda.stream(stream):
+        for f in arrangements.values():          # warm-up
+            f()
+        torch.cuda.synchronize(dev)
+        for _ in range(prompts):
+            for k, f in arrangements.items():
+                e0, e1, e2 = f()
+                e2.synchronize()
+                span[k].append(e0.elapsed_time(e1))
+                tail[k].append(e1.elapsed_time(e2) * 1e3)
+    med = statistics.median
+    t_c = med(span["compute"])
+    out = {"compute_ms": round(t_c, 3),
+           "compute_tflops": round(2.0 * tokens * 8192 * 104448 * L / (t_c * 1e-3) / 1e12, 1),
+           "compute_spread_ms": round(max(span["compute"]) - min(span["compute"]), 3),
+           "tail_us": {k: round(med(v), 1) for k, v in tail.items() if k != "compute"},
+           "gemm_span_ms": {k: round(med(v), 3) for k, v in span.items() if k != "compute"},
+           "what": "per prompt: stand-in prefill compute (one bf16 GEMM per layer with the "
+                   "FLOPs of a 70B layer's linear layers for the prompt); tail = last GEMM's "
+                   "end to the hand-off's end; gemm_span = first GEMM's start to last GEMM's "
+                   f"end; medians of {prompts} prompts per arrangement"}
+    if sms is not None:
+        sms.close()
+    del a, b, c
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -558,6 +644,11 @@ def run_ours(args):
                 "us_per_launch": round(ms * 1e3 / K / launches, 3),
                 "launches_per_step": launches}
             del g
+
+    # the per-layer hand-off beside the prefill compute it belongs to (70B workload)
+    overlap = None
+    if "overlap" in modes and args.config == "llama70b" and conv is None and not args.layers:
+        overlap = overlap_measure(plan, w, dev, stream)
 
     # the whole-prompt relayout on streams limited to a number of SMs
     sm_sweep = None
@@ -756,6 +847,7 @@ def run_ours(args):
                         "hand-off launch; every layer is ready before the first)"},
         },
         "layer_groups": layer_groups,
+        "overlap": overlap,
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
