@@ -15,6 +15,8 @@ Public API (see ``include/kv_relayout.h`` for the C ABI it binds):
   the relayout beside other kernels.
 * :func:`relayout_all_prealloc` -- ``run_all`` without any device allocation, for
   callers that cannot allocate (work lists up to 1 MiB).
+* ``kv_relayout.checked_library()`` / ``build.build_checked()`` -- the same C ABI
+  built with device-side address checks (tests).
 """
 from .kv_relayout import (KVRelayoutError, RelayoutPlan, desc_bytes, library,  # noqa: F401
                           LIB_PATH, STATUS, EXPORTS, relayout_all_prealloc, layout_of_views,

@@ -6,17 +6,22 @@
 // shard that holds the head, at the row the prefill block table gives for
 // the token, and written to the decode shard that holds the head, at the row
 // the decode block table gives. There is no intermediate buffer: the gather,
-// the TP re-shard and the scatter are one load and one store per chunk.
+// the TP re-shard and the scatter are one load and one store per chunk. With
+// more TP shards than KV heads, a head is read from the first prefill shard
+// that holds it and stored to every decode shard that holds it; with a dtype
+// change (BF16 <-> FP8 E4M3), each unit of 16 elements is converted between
+// its load and its store.
 //
-// It is pure data movement (no arithmetic on the values, no tensor cores),
-// bound by HBM bandwidth: every chunk is read once and written once, so the
-// DRAM traffic floor is 2 x (KV bytes of the prompts). The kernel keeps
-// KVR_UNROLL independent 16-byte loads in flight per thread before their
-// stores, uses streaming cache hints on both sides (neither the prefill rows
-// nor the decode rows are touched again by this kernel), and opts into
-// programmatic dependent launch so back-to-back per-layer launches overlap
-// their launch latency and their block-table reads with the previous
-// launch's tail.
+// It is data movement bound by HBM bandwidth (no tensor cores): every chunk
+// is read once and written once, so the DRAM traffic floor is the KV bytes of
+// the prompts read plus written. The kernel keeps several independent 16-byte
+// loads in flight per thread before their stores, uses streaming cache hints
+// on both sides (neither the prefill rows nor the decode rows are touched
+// again by this kernel), and opts into programmatic dependent launch so that
+// back-to-back per-layer launches overlap their launch latency, block-table
+// reads and (ordered launches of one wave) an L2 prefetch of their prefill
+// rows with the previous launch's tail. Built with KVR_DEVICE_CHECKS (tests),
+// it also checks every row against the plan's pools before touching it.
 #include <cuda_runtime.h>
 
 #include <algorithm>

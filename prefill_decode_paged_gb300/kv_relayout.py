@@ -367,7 +367,8 @@ class RelayoutPlan:
     """A validated relayout of one batch of prompts, ready to launch.
 
     ``src_pools``/``dst_pools``: one device buffer (torch tensor or address)
-    per TP shard, layout [L][C][N][B][H / tp][D]. Block tables are CSR:
+    per TP shard, layout [L][C][N][B][H / tp][D] (a TP degree above H, a multiple
+    of it: [L][C][N][B][1][D], tp / H shards per head). Block tables are CSR:
     ``src_off``/``dst_off`` (R + 1 offsets) into ``src_bt``/``dst_bt``.
     ``convert``: None (bit copy) or dict(src_dtype=..., dst_dtype=..., scales=...,
     per_head=False) for a BF16 <-> FP8 E4M3 relayout (``kv_relayout_plan_convert``).
