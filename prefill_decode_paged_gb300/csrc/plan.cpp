@@ -471,12 +471,14 @@ int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sm
     const bool limited = stream_sms > 0 && stream_sms < hp.sm_count;
     int32_t s = choose_slices(tasks, hp.avg_chunks, limited ? stream_sms : hp.sm_count,
                               KVR_TARGET_CTAS_PER_SM);
-    // large items (decode blocks of many tokens) of a bit copy on the whole
-    // device are cut until a CTA reads at most KVR_MAX_CTA_BYTES, so the grid
-    // does not end in a long partial wave; the converting kernels (more
-    // registers, fewer resident CTAs) measured faster with the larger CTAs,
-    // and so did every launch on an SM-limited stream, so those stay whole
-    if (!limited && hp.g.conv == KVR_CONV_NONE) {
+    // large items (decode blocks of many tokens) of a bit copy or a dequantizing
+    // relayout on the whole device are cut until a CTA moves at most
+    // KVR_MAX_CTA_BYTES, so the grid does not end in a long partial wave; the
+    // quantizing kernel measured faster with the larger CTAs, and so did every
+    // launch on an SM-limited stream, so those stay whole (dequantizing: the cap
+    // on bytes written with 4 units in flight per thread, 70B 6574 -> 6731,
+    // Qwen 32K 6763 -> 6780 GB/s; either change alone lost)
+    if (!limited && (hp.g.conv == KVR_CONV_NONE || hp.g.conv == KVR_CONV_E4M3_TO_BF16)) {
         // bytes written (a replicated head's unit is stored to every copy)
         const int64_t item_bytes = hp.avg_chunks * hp.g.dst_unit_bytes * hp.g.dcopies;
         const int64_t most = std::max<int64_t>(1, hp.avg_chunks / KVR_MIN_SLICE_CHUNKS);

@@ -386,12 +386,14 @@ __global__ void __launch_bounds__(KVR_THREADS)
 using KvrKernel = void (*)(KvrArgs);
 
 // Kernel instance for a conversion, launch mode and head replication: 8 loads
-// in flight per thread, but 4 for converting per-layer launches (16-element
-// units of BF16 take two loads each to quantize and two stores to dequantize)
-// except ordered one-wave quantizing ones. Measured with 8 loads: those rose
-// 4351 -> 4592 GB/s (70B layers), while quantizing launches of several waves
-// lost 1-2 % (Qwen 32K and MLA layers, shaped for 4 instead of 6 CTAs per SM),
-// and dequantizing ones (80 registers) gained on 8B layers but not on 70B.
+// in flight per thread, but 4 for dequantizing launches and converting
+// per-layer ones (16-element units of BF16 take two loads each to quantize and
+// two stores to dequantize) except ordered one-wave quantizing ones. Measured
+// with 8 loads: those rose 4351 -> 4592 GB/s (70B layers), while quantizing
+// launches of several waves lost 1-2 % (Qwen 32K and MLA layers, shaped for 4
+// instead of 6 CTAs per SM); dequantizing ones with 8 units (80 registers, 3
+// CTAs per SM) ran slower than with 4 (48 registers, 5 CTAs per SM) once
+// whole-prompt items were capped like a bit copy's.
 template <int MODE, bool REP>
 KvrKernel pick_instance(int32_t conv) {
     constexpr bool LAYER = MODE != KVR_MODE_WHOLE;
@@ -402,7 +404,7 @@ KvrKernel pick_instance(int32_t conv) {
                                                                       : KVR_UNROLL / 2,
                                        KVR_CONV_BF16_TO_E4M3, MODE, REP>;
         case KVR_CONV_E4M3_TO_BF16:
-            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL,
+            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL / 2,
                                        KVR_CONV_E4M3_TO_BF16, MODE, REP>;
         default:
             return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER : KVR_UNROLL, KVR_CONV_NONE, MODE,

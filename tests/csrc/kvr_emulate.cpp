@@ -84,7 +84,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                            ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
                               : per_layer                     ? KVR_UNROLL_LAYER_QUANT
                                                               : KVR_UNROLL / 2)
-                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL);
+                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL / 2);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
