@@ -280,3 +280,24 @@ int64_t emu_fastdiv_check(uint32_t d_max, uint32_t stride) {
     return bad;
 }
 }
+
+extern "C" {
+
+// kvr_range_launch() for a plan built with the given residencies: out = [slices,
+// mode, grid (CTAs), items].
+int32_t emu_range_launch(const kvr_desc *d, int sm_count, int resident, int resident_pf,
+                         int32_t count, int32_t stream_sms, int32_t no_wait, int64_t *out) {
+    KvrHostPlan hp;
+    kvr_status st = kvr_build_host_plan(d, nullptr, nullptr, nullptr, sm_count, resident,
+                                        resident_pf, &hp, nullptr, nullptr);
+    if (st != KVR_OK) return st;
+    int32_t slices = 0, mode = -1;
+    kvr_range_launch(hp, count, stream_sms, no_wait != 0, &slices, &mode);
+    out[0] = slices;
+    out[1] = mode;
+    out[2] = (int64_t)count * (int64_t)hp.items.size() * slices;
+    out[3] = (int64_t)hp.items.size();
+    return 0;
+}
+
+}  // extern "C"

@@ -49,6 +49,9 @@ def emu():
     lib.emu_plan_info.argtypes = [p, ctypes.c_int, p]
     lib.emu_fastdiv_check.restype = i64
     lib.emu_fastdiv_check.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    lib.emu_range_launch.restype = i32
+    lib.emu_range_launch.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, i32,
+                                     i32, p]
     lib.emu_fastdiv_check_one.restype = i64
     lib.emu_fastdiv_check_one.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
     return lib
@@ -342,6 +345,47 @@ def test_launch_shapes(emu):
     assert emu.emu_plan_info(ctypes.byref(desc.desc), SMS, info) == 0
     assert info[5] == 48
     assert info[0] == sum(-(-int(n) // 48) for n in w.seq_lens)
+
+
+def test_launch_modes_and_grids_per_stream(emu):
+    """Which kernel instance a kv_relayout_layers() launch runs, and its grid: an ordered
+    launch whose tasks fit one wave of the prefetching instance on the stream's SMs runs
+    it with a grid inside that wave; no-wait launches never prefetch; a stream with
+    fewer SMs gets a grid shaped for them; long ranges run the whole-prompt instance."""
+    WHOLE, LAYER, PREFETCH = 0, 1, 2
+    out = (ctypes.c_int64 * 4)()
+
+    def shape(name, count, stream_sms=0, no_wait=False, res=4, res_pf=4):
+        w = wl.get(name)
+        s, d = fake_pools(w)
+        desc = kr._Desc(s, d, **w.geometry())
+        assert emu.emu_range_launch(ctypes.byref(desc.desc), SMS, res, res_pf, count,
+                                    stream_sms, int(no_wait), out) == 0
+        return out[0], out[1], out[2], out[3]
+
+    # 70B: 128 items per layer
+    sl, mode, grid, items = shape("llama70b", 1)
+    assert items == 128 and mode == PREFETCH and grid == 512 and grid <= SMS * 4
+    sl, mode, grid, _ = shape("llama70b", 1, no_wait=True)
+    assert mode == LAYER and grid <= SMS * 4
+    for sms in (8, 16, 32, 64, 96):
+        sl, mode, grid, _ = shape("llama70b", 1, stream_sms=sms)
+        if 128 < sms * 4:                     # fits one wave of the prefetching instance
+            assert mode == PREFETCH and sms * 4 - 128 < grid <= sms * 4
+        else:                                 # about three waves of the per-layer one
+            assert mode == LAYER and grid >= 128
+    # a prefetching instance with fewer resident CTAs gets its own shape
+    sl, mode, grid, _ = shape("llama70b", 1, res=6, res_pf=4)
+    assert mode == PREFETCH and grid <= SMS * 4
+    # no residency known for the prefetching instance: never prefetch
+    assert shape("llama70b", 1, res_pf=0)[1] == LAYER
+    # ranges: two 70B layers still fit one wave, eight do not
+    sl, mode, grid, _ = shape("llama70b", 2)
+    assert mode == PREFETCH and grid <= SMS * 4
+    assert shape("llama70b", 8)[1] == WHOLE
+    # Qwen 32K layers hold 2048 items: several waves, no prefetch
+    sl, mode, grid, items = shape("qwen32k", 1)
+    assert items == 2048 and mode == LAYER and grid >= SMS * 4
 
 
 # -- converting relayout (host side) -------------------------------------------------
