@@ -268,3 +268,19 @@ def test_binding_refuses_tensors_smaller_than_the_geometry(emu):
         kr.pack_plan(src, stage, **g)
     with pytest.raises(ValueError, match="staging buffer"):
         kr.pack_plan(src, stage[0], **g)
+
+
+def test_binding_checks_replicated_pool_extents(emu):
+    """With more TP shards than KV heads a shard pool holds one head row per token:
+    [L][C][N][B][1][D]; the binding accepts exactly that extent and refuses less."""
+    w = _w(7, kv_heads=2, src_tp=4, dst_tp=8, src_block=5, dst_block=16)
+    g = w.geometry()
+    assert w.src_shape()[4] == 1 and w.dst_shape()[4] == 1
+    src = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
+    dst = [_aligned(w.dst_shape(), np.uint16) for _ in range(w.dst_tp)]
+    r, wr = kr.desc_bytes(src, dst, **g)
+    assert wr == 4 * r                                 # every head written to 8 / 2 shards
+    short = _aligned((int(np.prod(w.dst_shape())) - 8,), np.uint16)
+    with pytest.raises(ValueError, match="dst pool 3"):
+        kr.desc_bytes(src, dst[:3] + [short] + dst[4:], **g)
+
