@@ -89,11 +89,12 @@ def parse_args(argv=None):
     p.add_argument("--sm-sweep", default="",
                    help="comma-separated SM counts: also time the whole-prompt relayout on "
                         "streams limited to that many SMs (green contexts)")
-    p.add_argument("--modes", default="all,layer,graph,groups,overlap",
+    p.add_argument("--modes", default="all,layer,graph,groups,overlap,formats",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA "
                         "graph), groups (launches of --groups layers each, from a CUDA graph), "
-                        "overlap (70B: the hand-off beside a stand-in for the prefill compute)")
+                        "overlap (70B: the hand-off beside a stand-in for the prefill compute), "
+                        "formats (other decode layouts and the staging-buffer route)")
     p.add_argument("--groups", default="2,4,8,16",
                    help="layers per launch for the groups measurement")
     return p.parse_args(argv)
@@ -433,6 +434,54 @@ def host_threads():
 
 # -- our arm --------------------------------------------------------------------------
 
+def formats_measure(w, src, dev, stream, timed, bytes_step, K, world):
+    """The whole-prompt hand-off into other decode layouts, and through a staging
+    buffer: head-major decode blocks ([N][H][B][D] per layer and component),
+    K and V interleaved per block ([L][N][C][B][H][D] per shard), and the two
+    passes of the staging route (pack the prefill pools into [L][C][tokens][H][D],
+    pd.py's gathered shape; unpack it into the decode pools), each timed like the
+    step. GB/s counts each launch's own bytes read + written."""
+    import torch
+    from prefill_decode_paged_gb300 import (RelayoutPlan, layout_of_views, pack_plan,
+                                            unpack_plan)
+    L, C, Nd, Bd, Hd, D = w.dst_shape()
+    tdt = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[w.elem_bytes]
+
+    def gbs(ms):
+        return round(whole_job_gbs(bytes_step, K, world, ms * 1e-3), 2)
+
+    out = {}
+    for name, shape, view in (
+            ("head_major", (L, C, Nd, Hd, Bd, D), lambda b, l, c: b[l, c].permute(0, 2, 1, 3)),
+            ("kv_interleaved", (L, Nd, C, Bd, Hd, D), lambda b, l, c: b[l, :, c])):
+        bufs = [torch.full(shape, -1, dtype=tdt, device=dev) for _ in range(w.dst_tp)]
+        views = [[[view(b, l, c) for c in range(C)] for l in range(L)] for b in bufs]
+        with RelayoutPlan(src, None, dst_layout=layout_of_views(views), **w.geometry()) as p:
+            ms = timed(lambda: p.run_all(stream), K)
+        out[name] = {"gbs": gbs(ms), "ms_per_step": round(ms / K, 5)}
+        del bufs, views
+    total = int(w.seq_lens.sum())
+    stage = torch.empty((L, C, total, w.kv_heads, D), dtype=tdt, device=dev)
+    dst = w.dst_pools_torch(dev)
+    with pack_plan(src, stage, **w.geometry()) as pk, \
+            unpack_plan(stage, dst, **w.geometry()) as up:
+        ms_p = timed(lambda: pk.run_all(stream), K)
+        ms_u = timed(lambda: up.run_all(stream), K)
+
+        def both():
+            pk.run_all(stream)
+            up.run_all(stream)
+        ms_b = timed(both, K)
+    out["staging"] = {"pack_gbs": gbs(ms_p), "unpack_gbs": gbs(ms_u),
+                      "pack_then_unpack_ms_per_step": round(ms_b / K, 5),
+                      "what": "pack: prefill pools -> [L][C][tokens][H][D] staging buffer; "
+                              "unpack: staging buffer -> decode pools; each moves the "
+                              "prompt's KV once (read + write)"}
+    del stage, dst
+    torch.cuda.empty_cache()
+    return out
+
+
 def overlap_measure(plan, w, dev, stream, prompts=9):
     """The hand-off beside the prefill compute it belongs to. Stand-in for one layer's
     prefill compute: one bf16 GEMM (cuBLAS) with the FLOPs of a Llama-3-70B layer's
@@ -645,6 +694,11 @@ def run_ours(args):
                 "launches_per_step": launches}
             del g
 
+    # other decode layouts and the staging-buffer route (70B workload, bit copy)
+    formats = None
+    if "formats" in modes and args.config == "llama70b" and conv is None and not args.layers:
+        formats = formats_measure(w, src, dev, stream, timed, bytes_step, K, world)
+
     # the whole-prompt relayout on streams limited to a number of SMs
     sm_sweep = None
     if args.sm_sweep:
@@ -850,6 +904,7 @@ def run_ours(args):
         },
         "layer_groups": layer_groups,
         "overlap": overlap,
+        "formats": formats,
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
