@@ -89,12 +89,15 @@ def parse_args(argv=None):
     p.add_argument("--sm-sweep", default="",
                    help="comma-separated SM counts: also time the whole-prompt relayout on "
                         "streams limited to that many SMs (green contexts)")
-    p.add_argument("--modes", default="all,layer,graph,groups,overlap,formats",
+    p.add_argument("--modes", default="all,layer,graph,groups,formats,targets",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA "
                         "graph), groups (launches of --groups layers each, from a CUDA graph), "
-                        "overlap (70B: the hand-off beside a stand-in for the prefill compute), "
-                        "formats (other decode layouts and the staging-buffer route)")
+                        "formats (other decode layouts and the staging-buffer route), "
+                        "targets (70B default run: the Qwen3-32B 4 x 32K batch and the 70B "
+                        "per-layer conversions, timed like the step), "
+                        "overlap (70B, not in the default: the hand-off beside a stand-in for "
+                        "the prefill compute; its GEMMs run the GPU at its power limit)")
     p.add_argument("--groups", default="2,4,8,16",
                    help="layers per launch for the groups measurement")
     return p.parse_args(argv)
@@ -320,16 +323,24 @@ BF16, E4M3 = 1, 2
 
 def conversion(args, w):
     """(prefill workload, decode workload, convert dict or None) for --convert."""
+    return conversion_for(args.convert, w)
+
+
+def conversion_for(kind, w):
+    """(prefill workload, decode workload, convert dict or None) for a conversion kind
+    ("none", "bf16_to_fp8", "fp8_to_bf16"): FP8 prefill pools hold seeded byte patterns
+    spread over every finite E4M3 code (FP8 KV written by a quantizer holds no NaN code),
+    scales are seeded per (layer, component, head)."""
     import dataclasses
 
     import numpy as np
-    if args.convert == "none":
+    if kind == "none":
         return w, w, None
     rng = np.random.default_rng(w.seed + 100)
     scales = rng.uniform(0.01, 0.05, w.num_layers * w.num_components * w.kv_heads)
     scales = scales.astype(np.float32)
-    fp8 = dataclasses.replace(w, elem_bytes=1, values="bits")
-    if args.convert == "bf16_to_fp8":
+    fp8 = dataclasses.replace(w, elem_bytes=1, values="e4m3")
+    if kind == "bf16_to_fp8":
         return w, fp8, dict(src_dtype=BF16, dst_dtype=E4M3, per_head=True, scales=scales)
     return fp8, w, dict(src_dtype=E4M3, dst_dtype=BF16, per_head=True, scales=scales)
 
@@ -567,6 +578,85 @@ def overlap_measure(plan, w, dev, stream, prompts=9):
     return out
 
 
+def layer_graph(plan, num_layers, dev, stream, no_wait_after_first=False):
+    """The per-layer hand-off of one prompt batch captured once in a CUDA graph:
+    ``num_layers`` ordered launches (kv_relayout_layer), or with
+    ``no_wait_after_first`` launches 2.. passing KVR_LAUNCH_NO_WAIT (each follows
+    another hand-off launch, and every layer is ready before the first)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cap):
+        for layer in range(num_layers):
+            plan.run_layers(layer, 1, wait_for_previous=not no_wait_after_first or layer == 0)
+    stream.wait_stream(cap)
+    return g
+
+
+def _figures(bytes_step, ms, steps, world, peak, launches=1):
+    """GB/s (whole job), fraction of the copy peak, ms per step and us per launch."""
+    gbs = whole_job_gbs(bytes_step, steps, world, ms * 1e-3)
+    out = {"gbs": round(gbs, 1), "frac": round(gbs / world / peak, 4),
+           "ms": round(ms / steps, 4)}
+    if launches > 1:
+        out["us_per_launch"] = round(ms * 1e3 / steps / launches, 3)
+    return out
+
+
+def targets_measure(timed, dev, stream, K, world, peak, main_per_layer=None):
+    """Both >= 80 % targets, and the per-layer hand-off, each timed like the step
+    (same warm-up, K steps, CUDA events on the launching stream):
+
+    - qwen32k: Qwen3-32B KV shape, 4 x 32768 tokens, prefill TP4 block 16 -> decode
+      TP2 block 64 (86 GB of pools): one whole-prompt launch per step, and the same
+      batch in 64 ordered per-layer launches per step (CUDA graph);
+    - llama70b per layer with a dtype change on the way (BF16 -> FP8 E4M3 and
+      FP8 E4M3 -> BF16, per-head scales): whole prompt, and 80 ordered per-layer
+      launches per step (CUDA graph).
+
+    ``target_ms`` is the time at 80 % of the measured copy peak; ``frac`` is of that
+    peak."""
+    import torch
+
+    import workloads as wl
+    from prefill_decode_paged_gb300 import RelayoutPlan
+
+    out = {"peak_gbs": peak}
+    if main_per_layer is not None:
+        out["llama70b"] = main_per_layer
+    k_big = max(3, min(K, 30))
+    w = wl.get("qwen32k")
+    src, dst = w.src_pools_torch(dev), w.dst_pools_torch(dev)
+    with RelayoutPlan(src, dst, **w.geometry()) as plan:
+        b = plan.bytes_read + plan.bytes_written
+        whole = _figures(b, timed(lambda: plan.run_all(stream), k_big), k_big, world, peak)
+        g = layer_graph(plan, w.num_layers, dev, stream)
+        layer = _figures(b, timed(g.replay, k_big), k_big, world, peak, w.num_layers)
+        del g
+    target_ms = b / (0.8 * peak * 1e9) * 1e3
+    out["qwen32k"] = {"whole": whole, "per_layer": layer, "target_ms": round(target_ms, 3),
+                      "met": whole["ms"] <= target_ms and layer["ms"] <= target_ms}
+    del src, dst
+    torch.cuda.empty_cache()
+
+    w70 = wl.get("llama70b")
+    for kind in ("bf16_to_fp8", "fp8_to_bf16"):
+        ws, wd, conv = conversion_for(kind, w70)
+        src, dst = ws.src_pools_torch(dev), wd.dst_pools_torch(dev)
+        with RelayoutPlan(src, dst, convert=conv, **ws.geometry()) as plan:
+            b = plan.bytes_read + plan.bytes_written
+            whole = _figures(b, timed(lambda: plan.run_all(stream), K), K, world, peak)
+            g = layer_graph(plan, ws.num_layers, dev, stream)
+            layer = _figures(b, timed(g.replay, K), K, world, peak, ws.num_layers)
+            del g
+        out[f"llama70b_{kind}"] = {"whole": whole, "per_layer": layer,
+                                   "met": layer["frac"] >= 0.8}
+        del src, dst
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -649,24 +739,12 @@ def run_ours(args):
         ms_layer = timed(per_layer, k_layer)
     if "graph" in modes:
         # per-layer, the L launches captured once in a CUDA graph and replayed
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            for layer in range(L):
-                plan.run_layer(layer)
-        stream.wait_stream(cap)
+        g = layer_graph(plan, L, dev, stream)
         ms_graph = timed(g.replay, K)
         del g
         # the same launches where each but the first passes KVR_LAUNCH_NO_WAIT: they
         # follow another hand-off launch and their layers are ready before it (all are)
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            for layer in range(L):
-                plan.run_layers(layer, 1, wait_for_previous=layer == 0)
-        stream.wait_stream(cap)
+        g = layer_graph(plan, L, dev, stream, no_wait_after_first=True)
         ms_graph_nw = timed(g.replay, K)
         del g
     layer_groups = None
@@ -744,6 +822,19 @@ def run_ours(args):
                                           "per_layer_gbs": round(
                                               bytes_step / (ms_l * 1e-3) / 1e9, 1)}
 
+    hbm_peak, peak_src = measured_hbm_peak()
+
+    # both >= 80 % targets and the per-layer conversions (the default 70B run only)
+    targets = None
+    if "targets" in modes and args.config == "llama70b" and conv is None and not args.layers:
+        main = None
+        if ms_graph is not None:
+            main = {"whole": _figures(bytes_step, ms_all, K, world, hbm_peak),
+                    "per_layer": _figures(bytes_step, ms_graph, K, world, hbm_peak, L),
+                    "target_ms": round(bytes_step / (0.8 * hbm_peak * 1e9) * 1e3, 4)}
+            main["met"] = max(main["whole"]["ms"], main["per_layer"]["ms"]) <= main["target_ms"]
+        targets = targets_measure(timed, dev, stream, K, world, hbm_peak, main)
+
     # e2e: the pools live in pinned host memory; every step hands the batch over
     # through the public no-allocation call, whose kernel reads the prefill rows
     # from host memory and writes the decode rows to host memory over
@@ -761,7 +852,11 @@ def run_ours(args):
             h.copy_(t)
         for h in h_dst:
             h.fill_(-1)
+        # the work list the call copies to the device: 16 B per token tile (here one
+        # decode block), 8 B per (shard, layer, component) view base of each side, 4 B
+        # per used prefill and decode block id
         meta_bytes = 16 * sum(-(-int(n) // w.dst_block) for n in w.seq_lens) + \
+            8 * (w.src_tp + w.dst_tp) * w.num_layers * w.num_components + \
             4 * sum(-(-int(n) // w.src_block) + -(-int(n) // w.dst_block) for n in w.seq_lens)
 
         def run_e2e(step, steps, what, h2d, d2h):
@@ -789,9 +884,8 @@ def run_ours(args):
 
         e2e = run_e2e(zero_copy_step, args.e2e_steps,
                       "per step: kv_relayout_all_prealloc on pools in pinned host memory "
-                      "(validate, upload the work list, one kernel that reads the prefill "
-                      "rows from host memory and writes the decode rows to host memory "
-                      "over NVLink-C2C), synchronize; wall clock",
+                      "(the kernel reads and writes them over NVLink-C2C), synchronize; "
+                      "wall clock",
                       plan.bytes_read + meta_bytes, plan.bytes_written)
         for h, t in zip(h_dst, dst):
             if not torch.equal(h.to(dev), t):
@@ -855,13 +949,23 @@ def run_ours(args):
                                            f"({moved1} bytes in {sec1:.1f} s)"},
                "host_cpus": os.cpu_count(), "host_cpu": host_cpu_model()}
 
-    hbm_peak, peak_src = measured_hbm_peak()
     avg_launch_ms = ms_all / K
     achieved = bytes_step / (avg_launch_ms * 1e-3) / 1e9
     traffic, _ = profiled_traffic(args.config, w.num_layers,
                                   "" if conv is None else f"_{args.convert}")
     prompts = w.num_requests
     value = whole_job_gbs(bytes_step, K, world, ms_all * 1e-3)
+
+    def per_layer_entry(ms, steps, extra=None):
+        if ms is None:
+            return None
+        e = {"gbs": round(whole_job_gbs(bytes_step, steps, world, ms * 1e-3), 2),
+             "ms_per_prompt": round(ms / steps / prompts, 5),
+             "us_per_launch": round(ms * 1e3 / steps / L, 3)}
+        return {**e, **(extra or {})}
+
+    # key order: the driver keeps the end of stdout, so the per-layer figures and the
+    # targets come last
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -875,47 +979,37 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": dtype_label(w, args, conv),
         "data": data_label(w),
-        "config": {**workload_config(args, w, conv),
-                   "l2": "inputs larger than L2 (no flush)" if bytes_step > 2 * 129e6 else
-                         "working set fits in L2 (launch-bound case)",
-                   "parallelism": f"replica per GPU x{world}"},
+        "config": workload_config(args, w, conv),
+        "run": {"l2": "inputs larger than L2 (no flush)" if bytes_step > 2 * 129e6 else
+                      "working set fits in L2 (launch-bound case)",
+                "parallelism": f"replica per GPU x{world}", "impl": "CUDA kernel via the C ABI"},
         "ms_per_prompt": round(ms_all / K / prompts, 5),
         "launch_ms": launch_ms,
         "pct_of_hbm_peak": round(100 * achieved / hbm_peak, 2),
         "pct_of_nominal_hbm": round(100 * achieved / NOMINAL_HBM_GBS, 2),
-        "per_layer": {
-            "eager": None if ms_layer is None else {
-                "gbs": round(whole_job_gbs(bytes_step, k_layer, world, ms_layer * 1e-3), 2),
-                "ms_per_prompt": round(ms_layer / k_layer / prompts, 5),
-                "us_per_launch": round(ms_layer * 1e3 / k_layer / L, 3),
-                "launches_per_step": L, "steps": k_layer},
-            "cuda_graph": None if ms_graph is None else {
-                "gbs": round(whole_job_gbs(bytes_step, K, world, ms_graph * 1e-3), 2),
-                "ms_per_prompt": round(ms_graph / K / prompts, 5),
-                "us_per_launch": round(ms_graph * 1e3 / K / L, 3),
-                "launches_per_step": L, "steps": K},
-            "cuda_graph_no_wait": None if ms_graph_nw is None else {
-                "gbs": round(whole_job_gbs(bytes_step, K, world, ms_graph_nw * 1e-3), 2),
-                "ms_per_prompt": round(ms_graph_nw / K / prompts, 5),
-                "us_per_launch": round(ms_graph_nw * 1e3 / K / L, 3),
-                "launches_per_step": L, "steps": K,
-                "what": "launches 2..L pass KVR_LAUNCH_NO_WAIT (each follows another "
-                        "hand-off launch; every layer is ready before the first)"},
-        },
-        "layer_groups": layer_groups,
-        "overlap": overlap,
-        "formats": formats,
         "gpu_launches": K,
+        "formats": formats,
+        "overlap": overlap,
+        "layer_groups": layer_groups,
+        "sm_sweep": sm_sweep,
+        "e2e_staged": e2e_staged,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_src} (copy, read+write)",
                      "kernel": "kvr_relayout_kernel",
                      "algorithmic_bytes_per_launch": bytes_step},
-        "e2e": e2e,
-        "e2e_staged": e2e_staged,
-        "sm_sweep": sm_sweep,
-        "cpu_baseline": cpu,
         "clocks": clock,
+        "per_layer": {
+            "launches_per_step": L,
+            "eager": per_layer_entry(ms_layer, k_layer),
+            "cuda_graph": per_layer_entry(ms_graph, K),
+            "cuda_graph_no_wait": per_layer_entry(ms_graph_nw, K,
+                                                  {"what": "launches 2..L pass "
+                                                           "KVR_LAUNCH_NO_WAIT"}),
+        },
+        "targets": targets,
     }
     plan.close()
     if rank == 0:
@@ -969,8 +1063,9 @@ def run_reference(args):
            "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": dtype_label(w, args, conv),
            "data": data_label(w),
-           "config": {**workload_config(args, w, conv), "sample_layers_per_step": n,
-                      "parallelism": f"CPU oracle, {used} host threads"},
+           "config": workload_config(args, w, conv),
+           "run": {"sample_layers_per_step": n,
+                   "parallelism": f"CPU oracle, {used} host threads", "impl": "CPU oracle"},
            "cpu_baseline": cpu,
            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}

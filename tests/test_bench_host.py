@@ -45,6 +45,7 @@ def test_two_gloo_ranks_take_the_slowest_time(tmp_path):
 
 
 def test_reference_arm_prints_the_contract_line():
+    sys.path.insert(0, ROOT)
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--config", "tiny", "--steps", "3", "--warmup", "1"],
                          capture_output=True, text=True, timeout=300, cwd=ROOT)
@@ -58,6 +59,12 @@ def test_reference_arm_prints_the_contract_line():
         assert k in d, k
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
+    # the workload's config only; how the arm ran goes under "run"
+    import bench
+    import workloads as wl
+    args = bench.parse_args(["--impl", "reference", "--config", "tiny"])
+    assert d["config"] == bench.workload_config(args, wl.get("tiny"), None)
+    assert "sample_layers_per_step" in d["run"]
 
 
 def test_reference_arm_other_ranks_exit_quietly():

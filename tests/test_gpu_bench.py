@@ -38,4 +38,14 @@ def test_bench_line_keeps_the_contract():
     # tiny has 2 layers: at most 2 threads, each on its own layer; and the one-core figure
     assert c["cores"] <= 2 and c["single_thread"]["cores"] == 1
     assert c["single_thread"]["value"] > 0
-    assert d["per_layer"]["eager"]["launches_per_step"] == 2
+    assert d["per_layer"]["launches_per_step"] == 2
+    assert d["per_layer"]["eager"]["gbs"] > 0 and d["per_layer"]["cuda_graph"]["gbs"] > 0
+    # the reference arm reports the identical config for the same workload
+    ref = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--steps", "3", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert ref.returncode == 0, ref.stderr[-3000:]
+    assert json.loads(ref.stdout.strip().splitlines()[-1])["config"] == d["config"]
+    # the per-layer figures and the targets close the line (the end of stdout is what
+    # a log tail keeps)
+    assert list(d)[-2:] == ["per_layer", "targets"]

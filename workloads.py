@@ -77,7 +77,8 @@ class Workload:
     src_bt: np.ndarray            # int32, prefill block ids
     dst_off: np.ndarray           # int64 [R + 1], CSR into dst_bt
     dst_bt: np.ndarray            # int32, decode block ids
-    values: str                   # "bits" (uniform bit patterns) or "randn" (bf16 N(0,1))
+    values: str                   # "bits" (uniform bit patterns), "randn" (bf16 N(0,1)) or
+                                  # "e4m3" (uniform over the 254 non-NaN E4M3 byte patterns)
 
     # -- shapes ---------------------------------------------------------
     @property
@@ -127,6 +128,9 @@ class Workload:
                 f = rng.standard_normal(self.src_shape(), dtype=np.float32).view(np.uint32)
                 rounded = f + 0x7FFF + ((f >> 16) & 1)
                 out.append((rounded >> 16).astype(np.uint16))
+            elif self.values == "e4m3":
+                out.append(_finite_e4m3_codes(rng.integers(0, 254, size=self.src_shape(),
+                                                            dtype=np.uint8)))
             else:
                 info = np.iinfo(self.int_dtype())
                 out.append(rng.integers(0, int(info.max) + 1, size=self.src_shape(),
@@ -156,6 +160,11 @@ class Workload:
                 t = torch.randn(self.src_shape(), generator=g, device=device,
                                 dtype=torch.bfloat16)
                 out.append(t.view(torch.int16))
+            elif self.values == "e4m3":
+                assert self.elem_bytes == 1
+                r = torch.randint(0, 254, self.src_shape(), generator=g, device=device,
+                                  dtype=torch.uint8)
+                out.append(r + (r >= 0x7F).to(torch.uint8))
             else:
                 lo, hi = {1: (0, 256), 2: (-32768, 32768), 4: (-2**31, 2**31)}[self.elem_bytes]
                 out.append(torch.randint(lo, hi, self.src_shape(), generator=g, device=device,
@@ -171,6 +180,12 @@ class Workload:
             tdt = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[self.elem_bytes]
             out.append(t.view(tdt).view(self.dst_shape()))
         return out
+
+
+def _finite_e4m3_codes(r):
+    """Byte patterns 0..253 spread over the 254 bytes other than 0x7F and 0xFF (the
+    two NaN patterns of an E4M3 element): r -> r, or r + 1 from 0x7F on."""
+    return (r + (r >= 0x7F)).astype(np.uint8)
 
 
 # -- block allocation -------------------------------------------------------
