@@ -616,23 +616,25 @@ def targets_measure(timed, dev, stream, K, world, peak, main_per_layer=None):
       launches per step (CUDA graph).
 
     ``target_ms`` is the time at 80 % of the measured copy peak; ``frac`` is of that
-    peak."""
+    peak. Each is timed over max(K, 200) steps, at most 2000 (max(K, 30), at most 100,
+    for the Qwen batch), after 20 warm-up steps on its freshly allocated pools."""
     import torch
 
     import workloads as wl
     from prefill_decode_paged_gb300 import RelayoutPlan
 
-    out = {"peak_gbs": peak}
+    k_big, W = min(max(K, 30), 100), 20
+    K = min(max(K, 200), 2000)
+    out = {"peak_gbs": peak, "steps": K, "steps_qwen32k": k_big}
     if main_per_layer is not None:
         out["llama70b"] = main_per_layer
-    k_big = max(3, min(K, 30))
     w = wl.get("qwen32k")
     src, dst = w.src_pools_torch(dev), w.dst_pools_torch(dev)
     with RelayoutPlan(src, dst, **w.geometry()) as plan:
         b = plan.bytes_read + plan.bytes_written
-        whole = _figures(b, timed(lambda: plan.run_all(stream), k_big), k_big, world, peak)
+        whole = _figures(b, timed(lambda: plan.run_all(stream), k_big, W), k_big, world, peak)
         g = layer_graph(plan, w.num_layers, dev, stream)
-        layer = _figures(b, timed(g.replay, k_big), k_big, world, peak, w.num_layers)
+        layer = _figures(b, timed(g.replay, k_big, W), k_big, world, peak, w.num_layers)
         del g
     target_ms = b / (0.8 * peak * 1e9) * 1e3
     out["qwen32k"] = {"whole": whole, "per_layer": layer, "target_ms": round(target_ms, 3),
@@ -646,9 +648,9 @@ def targets_measure(timed, dev, stream, K, world, peak, main_per_layer=None):
         src, dst = ws.src_pools_torch(dev), wd.dst_pools_torch(dev)
         with RelayoutPlan(src, dst, convert=conv, **ws.geometry()) as plan:
             b = plan.bytes_read + plan.bytes_written
-            whole = _figures(b, timed(lambda: plan.run_all(stream), K), K, world, peak)
+            whole = _figures(b, timed(lambda: plan.run_all(stream), K, W), K, world, peak)
             g = layer_graph(plan, ws.num_layers, dev, stream)
-            layer = _figures(b, timed(g.replay, K), K, world, peak, ws.num_layers)
+            layer = _figures(b, timed(g.replay, K, W), K, world, peak, ws.num_layers)
             del g
         out[f"llama70b_{kind}"] = {"whole": whole, "per_layer": layer,
                                    "met": layer["frac"] >= 0.8}
@@ -694,8 +696,8 @@ def run_ours(args):
         time.sleep(0.3)
     windows = []
 
-    def timed(fn, steps):
-        for _ in range(args.warmup):
+    def timed(fn, steps, warmup=None):
+        for _ in range(args.warmup if warmup is None else warmup):
             fn()
         torch.cuda.synchronize(dev)
         barrier(world)

@@ -216,6 +216,47 @@ kvr_status kv_relayout_plan_ex(const kvr_desc *desc, const kvr_layout *src_layou
                                kvr_plan **out);
 
 /*
+ * The two halves of the hand-off through a contiguous staging buffer (page
+ * "PD 分离与 KV 传输", section "实现": pd.py's prefill() gathers each layer's K
+ * and V of a prompt into a contiguous [seq, kv_heads, head_dim] array, and
+ * admit() writes that array through the decode block table; the page
+ * "推理 INFRA 方法论（6）", section "KV-Cache 传输:方案与时延", stages the KV
+ * this way when the two sides' TP degrees differ and a link sits between them).
+ *
+ * The staging buffer is ONE contiguous buffer of
+ *   [num_layers][num_components][sum of n_r][kv_heads][head_dim]
+ * elements: every global head side by side (the prefill shards' head ranges
+ * merged, a replicated head once), request r's tokens at rows
+ * sum(n[:r]) .. sum(n[:r + 1]) - 1. It must be 16-byte aligned, memory the
+ * current device can access, and hold kv_relayout_staging_bytes() bytes.
+ *
+ * kv_relayout_plan_pack(): a plan that gathers the prefill pools of *desc into
+ * `staging` (the desc's decode-side fields dst_tp, dst_block_size,
+ * dst_num_blocks, dst_pools, dst_bt_offsets and dst_bt are ignored). With a
+ * conversion `cv`, the staging buffer holds cv->dst_dtype elements.
+ * kv_relayout_plan_unpack(): a plan that writes `staging` into the decode
+ * pools of *desc (its prefill-side fields src_tp, src_block_size,
+ * src_num_blocks, src_pools, src_bt_offsets and src_bt are ignored); the
+ * staging buffer holds desc->elem_bytes elements (cv->src_dtype with a
+ * conversion). Either plan is launched with kv_relayout_all() /
+ * kv_relayout_layer() / kv_relayout_layers() like any plan; packing and then
+ * unpacking gives the same decode bytes as one kv_relayout_plan() relayout.
+ * Errors: those of kv_relayout_plan_ex() (the staging buffer is one side's
+ * view: KVR_ERR_POOL_OVERLAP if it meets the other side's pools), and
+ * KVR_ERR_INVALID_ARG for a NULL staging buffer or a batch of zero tokens.
+ *
+ * kv_relayout_staging_bytes(): the staging buffer's size for elements of
+ * `elem_bytes` bytes (1, 2 or 4): L * C * (sum of n_r) * H * D * elem_bytes.
+ * Host only (no CUDA call); reads num_layers, num_components, kv_heads,
+ * head_dim, num_requests and seq_lens of *desc.
+ */
+kvr_status kv_relayout_staging_bytes(const kvr_desc *desc, int32_t elem_bytes, int64_t *bytes);
+kvr_status kv_relayout_plan_pack(const kvr_desc *desc, void *staging, const kvr_convert *cv,
+                                 kvr_plan **out);
+kvr_status kv_relayout_plan_unpack(const kvr_desc *desc, const void *staging,
+                                   const kvr_convert *cv, kvr_plan **out);
+
+/*
  * Move layer `layer` of every request: one kernel launch on `stream`
  * (a cudaStream_t; NULL = the legacy default stream). Asynchronous. Calling
  * it for every layer gives the same bytes as kv_relayout_all(). The current
@@ -332,11 +373,12 @@ void kv_relayout_sm_stream_destroy(kvr_sm_stream *s);
  * for the work list; this call allocates nothing: it validates *desc exactly
  * like kv_relayout_plan(), copies the work list (16 bytes per token tile of
  * a request, 8 bytes per (shard, layer, component) view of each side, 4 bytes
- * per used prefill and decode block id) into a
+ * per used prefill and decode block id) with one cudaMemcpyAsync into a
  * fixed device array of KVR_PREALLOC_SCRATCH_BYTES (1 MiB) that the library
  * reserves on every GPU that loads it, until the process exits, and launches
- * the same kernel as kv_relayout_all() on `stream` (asynchronous). The pool
- * memory checks of kv_relayout_plan() apply.
+ * the same kernel as kv_relayout_all() on `stream`, with the grid shaped for
+ * the stream's green context as kv_relayout_all() does. The pool memory
+ * checks of kv_relayout_plan() apply.
  *
  *  - A work list larger than the array is rejected with
  *    KVR_ERR_SCRATCH_LIMIT before anything is copied or launched; use
@@ -344,9 +386,16 @@ void kv_relayout_sm_stream_destroy(kvr_sm_stream *s);
  *  - The first call on a device looks up the array's device address on that
  *    device (with the device current) and caches it; make that first call
  *    before any stream capture begins.
- *  - Every call on a device shares the one array. Calls whose copies and
- *    kernels overlap on the GPU (different streams, not ordered by the
- *    caller) race on it and may move the wrong rows: issue them on one stream
+ *  - The work list is copied from pageable host memory that the call frees
+ *    before it returns: the call returns once the CUDA runtime has taken the
+ *    copy, which may wait for work already queued on `stream`. While `stream`
+ *    is being captured, the call returns KVR_ERR_UNSUPPORTED and enqueues
+ *    nothing.
+ *  - Every call on a device shares the one array. Calls from several host
+ *    threads enqueue their copy and their kernel under one lock per device,
+ *    so calls on one stream run one after another. Calls whose copies and
+ *    kernels overlap on the GPU (different streams not ordered by the caller)
+ *    race on the array and may move the wrong rows: issue them on one stream
  *    or order them with events.
  *  - The host arrays of *desc may be freed when the call returns.
  */

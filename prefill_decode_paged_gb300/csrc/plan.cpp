@@ -510,6 +510,82 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const i
     return a;
 }
 
+kvr_status kvr_staging_extent(const kvr_desc *d, int64_t es, int64_t *total, int64_t *bytes) {
+    if (d == nullptr || d->num_requests < 0 || (d->num_requests > 0 && d->seq_lens == nullptr) ||
+        d->num_layers < 1 || (d->num_components != 1 && d->num_components != 2) ||
+        d->kv_heads < 1 || d->head_dim < 1 || (es != 1 && es != 2 && es != 4))
+        return KVR_ERR_INVALID_ARG;
+    int64_t t = 0;
+    for (int32_t r = 0; r < d->num_requests; ++r) {
+        if (d->seq_lens[r] < 0) return KVR_ERR_INVALID_ARG;
+        t += d->seq_lens[r];                 // at most 2^31 requests of < 2^31 tokens
+    }
+    int64_t b = 0;
+    if (t > INT32_MAX ||
+        !mul_fits({t, (int64_t)d->num_layers, d->num_components, d->kv_heads, d->head_dim, es},
+                  &b))
+        return KVR_ERR_UNSUPPORTED;
+    *total = t;
+    *bytes = b;
+    return KVR_OK;
+}
+
+kvr_status kvr_staging_desc(const kvr_desc *desc, const void *staging, const kvr_convert *cv,
+                            bool pack, KvrStaging *st, kvr_desc *out) {
+    if (desc == nullptr || st == nullptr || out == nullptr) return KVR_ERR_INVALID_ARG;
+    // element bytes of the buffer: the conversion (if any) happens on the way in
+    int64_t es = desc->elem_bytes;
+    if (pack && cv != nullptr) {
+        if (cv->dst_dtype == KVR_DTYPE_BF16) es = 2;
+        else if (cv->dst_dtype == KVR_DTYPE_FP8_E4M3) es = 1;
+        else return KVR_ERR_UNSUPPORTED;
+    }
+    int64_t bytes = 0;
+    const kvr_status s = kvr_staging_extent(desc, es, &st->total, &bytes);
+    if (s != KVR_OK) return s;
+    if (st->total == 0 || staging == nullptr) return KVR_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)desc->head_dim * es, tok = row * desc->kv_heads;
+    const int64_t plane = st->total * tok;
+    const int64_t views = (int64_t)desc->num_layers * desc->num_components;
+    st->bases.resize((size_t)views);
+    for (int64_t v = 0; v < views; ++v)
+        st->bases[(size_t)v] = (const unsigned char *)staging + v * plane;
+    st->off.assign((size_t)desc->num_requests + 1, 0);
+    for (int32_t r = 0; r < desc->num_requests; ++r)
+        st->off[(size_t)r + 1] = st->off[(size_t)r] + desc->seq_lens[r];
+    st->ids.resize((size_t)st->total);
+    for (int64_t k = 0; k < st->total; ++k) st->ids[(size_t)k] = (int32_t)k;
+    st->layout.bases = st->bases.data();
+    st->layout.block_stride = tok;
+    st->layout.token_stride = tok;
+    st->layout.head_stride = row;
+    *out = *desc;
+    if (pack) {
+        out->dst_tp = 1;
+        out->dst_block_size = 1;
+        out->dst_num_blocks = st->total;
+        out->dst_pools = nullptr;
+        out->dst_bt_offsets = st->off.data();
+        out->dst_bt = st->ids.data();
+    } else {
+        out->src_tp = 1;
+        out->src_block_size = 1;
+        out->src_num_blocks = st->total;
+        out->src_pools = nullptr;
+        out->src_bt_offsets = st->off.data();
+        out->src_bt = st->ids.data();
+    }
+    return KVR_OK;
+}
+
+extern "C" kvr_status kv_relayout_staging_bytes(const kvr_desc *desc, int32_t elem_bytes,
+                                                int64_t *bytes) {
+    int64_t total = 0, b = 0;
+    const kvr_status st = kvr_staging_extent(desc, elem_bytes, &total, &b);
+    if (st == KVR_OK && bytes != nullptr) *bytes = b;
+    return st;
+}
+
 extern "C" kvr_status kv_relayout_desc_bytes_ex(const kvr_desc *desc,
                                                 const kvr_layout *src_layout,
                                                 const kvr_layout *dst_layout,

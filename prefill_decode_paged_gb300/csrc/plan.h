@@ -122,3 +122,26 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,
                         const int32_t *dev_sbt, const int32_t *dev_dbt,
                         const float *dev_factors, const uint64_t *dev_src_base,
                         const uint64_t *dev_dst_base, int32_t layer0, int32_t slices);
+
+// The staging side of a pack or unpack plan (kv_relayout_plan_pack/_unpack): a
+// contiguous [L][C][sum n][H][D] buffer seen as a single shard of one-token
+// blocks, request r's tokens from sum(n[:r]) on, so a block id is the token's
+// row in the buffer. `layout` points into `bases`.
+struct KvrStaging {
+    std::vector<const void *> bases;   // [L][C] view bases
+    std::vector<int64_t> off;          // CSR offsets: prefix sums of the prompt lengths
+    std::vector<int32_t> ids;          // 0 .. sum n - 1
+    kvr_layout layout;
+    int64_t total = 0;                 // tokens in the batch
+};
+
+// Tokens of d's batch and the bytes of its staging buffer for `es`-byte elements
+// (host only; validates the fields it reads).
+kvr_status kvr_staging_extent(const kvr_desc *d, int64_t es, int64_t *total, int64_t *bytes);
+
+// *out = *desc with its decode side (pack) or prefill side (unpack) replaced by
+// the staging buffer `staging`, whose layout *st receives (pass it as that side's
+// kvr_layout). The staging buffer holds the decode dtype when packing, the
+// prefill dtype (desc->elem_bytes) when unpacking.
+kvr_status kvr_staging_desc(const kvr_desc *desc, const void *staging, const kvr_convert *cv,
+                            bool pack, KvrStaging *st, kvr_desc *out);

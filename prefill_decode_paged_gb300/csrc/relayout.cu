@@ -23,11 +23,13 @@
 // rows with the previous launch's tail. Built with KVR_DEVICE_CHECKS (tests),
 // it also checks every row against the plan's pools before touching it.
 #include <cuda_runtime.h>
+#include <string.h>
 
 #include <algorithm>
 #include <new>
 
 #include "kv_relayout.h"
+#include "kvr_convert.cuh"
 #include "kvr_index.h"
 #include "plan.h"
 
@@ -92,97 +94,24 @@ __device__ __forceinline__ void store_stream(unsigned char *p, const uint4 &v) {
                  : "memory");
 }
 
-// -- element conversion (BF16 <-> FP8 E4M3) ------------------------------------
-//
-// Definitions (kv_relayout.h): quantize q = E4M3(x * (1/s)), nearest-even,
-// saturating at +-448, NaN kept with its sign; dequantize y = BF16(q * s),
-// nearest-even, a NaN code -> sign | 0x7FC0. The hardware conversion to E4M3
-// is applied to |y| and the input's sign is put back explicitly, so signed
-// zeros and NaN signs are exact; NaN codes are patched explicitly after the
-// hardware conversions to BF16.
-
-// E4M3 codes of two non-negative fp32 values: `hi` in bits 15..8, `lo` in 7..0.
-__device__ __forceinline__ uint32_t e4m3x2_rn_satfinite(float hi, float lo) {
-    unsigned short d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-    return d;
+// CTAs per SM each converting instance is compiled for (caps its registers:
+// 256 threads x 64 registers fill an SM's register file 4 times); 0 leaves the
+// bit copy's registers to the compiler. The dequantizer measured faster at 4
+// CTAs (64 registers) than at 5 (48 registers, which spills); a minimum of 4
+// for the bit copy (the 64 registers it takes anyway) cost 2-7 % (70B: 6945 ->
+// 6814 GB/s whole-prompt, 6193 -> 6000 per layer).
+#ifndef KVR_MIN_CTAS_DEQUANT
+#define KVR_MIN_CTAS_DEQUANT 4
+#endif
+constexpr int kvr_min_ctas(int U, int CONV) {
+    return CONV == KVR_CONV_E4M3_TO_BF16            ? KVR_MIN_CTAS_DEQUANT
+           : CONV == KVR_CONV_BF16_TO_E4M3 && U <= 2 ? 5
+           : CONV == KVR_CONV_BF16_TO_E4M3           ? 4
+                                                     : 0;
 }
 
-// Two BF16 elements (element 0 in the low half of `w`) -> two E4M3 codes
-// (element 0 in bits 7..0). The signs come from the inputs: since 1/s > 0 they
-// are the products' signs, and they also give a NaN input's sign (a NaN
-// product's sign is not fixed by IEEE 754; the GPU returns a positive one).
-__device__ __forceinline__ uint32_t quant2(uint32_t w, float inv) {
-    const float y0 = __fmul_rn(__uint_as_float(w << 16), inv);
-    const float y1 = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv);
-    const uint32_t sign = ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
-    return e4m3x2_rn_satfinite(fabsf(y1), fabsf(y0)) | sign;
-}
-
-// 16 BF16 (two 16-byte pieces) -> 16 E4M3 codes (one 16-byte piece).
-__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float inv) {
-    uint4 o;
-    o.x = quant2(a.x, inv) | (quant2(a.y, inv) << 16);
-    o.y = quant2(a.z, inv) | (quant2(a.w, inv) << 16);
-    o.z = quant2(b.x, inv) | (quant2(b.y, inv) << 16);
-    o.w = quant2(b.z, inv) | (quant2(b.w, inv) << 16);
-    return o;
-}
-
-__device__ __forceinline__ float f16_to_f32(unsigned short h) {
-    float f;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
-    return f;
-}
-
-// Two non-NaN E4M3 codes (element 0 in bits 7..0) -> two BF16 (element 0 in
-// the low half): exact decode to f16x2, exact widening, fp32 products,
-// nearest-even rounding to BF16 (overflow to infinity) by the hardware.
-__device__ __forceinline__ uint32_t dequant2(uint32_t codes, float s) {
-    uint32_t h2, out;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)codes));
-    const float y0 = __fmul_rn(f16_to_f32((unsigned short)(h2 & 0xFFFFu)), s);
-    const float y1 = __fmul_rn(f16_to_f32((unsigned short)(h2 >> 16)), s);
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(y1), "f"(y0));
-    return out;
-}
-
-// Four E4M3 codes (one word) -> four BF16 (two words). A NaN code (x.1111.111)
-// gives sign | 0x7FC0 with the code's sign; the packed test finds such codes
-// four at a time, so the patch-up runs only for words that hold one.
-__device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t *lo, uint32_t *hi) {
-    uint32_t a = dequant2(w & 0xFFFFu, s), b = dequant2(w >> 16, s);
-    const uint32_t nan = ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
-    if (nan != 0u) {
-        const uint32_t n0 = ((w & 0x80u) << 8) | 0x7FC0u, n1 = ((w & 0x8000u)) | 0x7FC0u;
-        const uint32_t n2 = ((w >> 8) & 0x8000u) | 0x7FC0u, n3 = ((w >> 16) & 0x8000u) | 0x7FC0u;
-        if (nan & 0x80u) a = (a & 0xFFFF0000u) | n0;
-        if (nan & 0x8000u) a = (a & 0x0000FFFFu) | (n1 << 16);
-        if (nan & 0x800000u) b = (b & 0xFFFF0000u) | n2;
-        if (nan & 0x80000000u) b = (b & 0x0000FFFFu) | (n3 << 16);
-    }
-    *lo = a;
-    *hi = b;
-}
-
-// 16 E4M3 codes (one 16-byte piece) -> 16 BF16 (two 16-byte pieces).
-__device__ __forceinline__ void dequant16(const uint4 &c, float s, uint4 *lo, uint4 *hi) {
-    dequant4(c.x, s, &lo->x, &lo->y);
-    dequant4(c.y, s, &lo->z, &lo->w);
-    dequant4(c.z, s, &hi->x, &hi->y);
-    dequant4(c.w, s, &hi->z, &hi->w);
-}
-
-// U: units each thread keeps in flight before its stores. CONV: KvrConv.
-// MODE: KVR_MODE_WHOLE, KVR_MODE_LAYER or KVR_MODE_LAYER_PREFETCH. Per-layer
-// modes build the first row window before waiting for the previous grid
-// (hides the block-table reads in the previous launch's tail; whole-prompt
-// launches wait first, which measured 1.7 % faster there); the prefetching
-// one also pulls those rows into L2 before the wait.
-// A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
-// REP: the plan replicates heads (a TP degree above H; see kvr_row).
 template <int U, int CONV, int MODE, bool REP>
-__global__ void __launch_bounds__(KVR_THREADS)
+__global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
     constexpr bool EARLY = MODE != KVR_MODE_WHOLE;
     constexpr bool PF = MODE == KVR_MODE_LAYER_PREFETCH;
@@ -668,6 +597,34 @@ extern "C" kvr_status kv_relayout_plan_convert(const kvr_desc *desc, const kvr_c
     return make_plan(desc, nullptr, nullptr, cv, out);
 }
 
+// -- pack / unpack: one side is a contiguous staging buffer ---------------------
+
+static kvr_status make_staging_plan(const kvr_desc *desc, const void *staging,
+                                    const kvr_convert *cv, bool pack, kvr_plan **out) {
+    if (out == nullptr) return KVR_ERR_INVALID_ARG;
+    *out = nullptr;
+    KvrStaging sd;
+    kvr_desc d;
+    kvr_status st;
+    try {
+        st = kvr_staging_desc(desc, staging, cv, pack, &sd, &d);
+    } catch (...) {
+        return KVR_ERR_NOMEM;
+    }
+    if (st != KVR_OK) return st;
+    return make_plan(&d, pack ? nullptr : &sd.layout, pack ? &sd.layout : nullptr, cv, out);
+}
+
+extern "C" kvr_status kv_relayout_plan_pack(const kvr_desc *desc, void *staging,
+                                            const kvr_convert *cv, kvr_plan **out) {
+    return make_staging_plan(desc, staging, cv, true, out);
+}
+
+extern "C" kvr_status kv_relayout_plan_unpack(const kvr_desc *desc, const void *staging,
+                                              const kvr_convert *cv, kvr_plan **out) {
+    return make_staging_plan(desc, staging, cv, false, out);
+}
+
 extern "C" kvr_status kv_relayout_layer(const kvr_plan *plan, int32_t layer, void *stream) {
     if (plan == nullptr) return KVR_ERR_INVALID_ARG;
     if (layer < 0 || layer >= plan->host.num_layers) return KVR_ERR_LAYER_RANGE;
@@ -769,10 +726,10 @@ extern "C" kvr_status kv_relayout_debug_narrow(kvr_plan *plan, int64_t bytes) {
 
 // ---------------------------------------------------------------------------
 // kv_relayout_all_prealloc: the whole-prompt relayout without any device
-// allocation. The kernel's scratch (the work list and the used prefill block
-// ids, normally in the plan's cudaMalloc'd buffer) lives in the file-scope
-// array below instead. Every GPU that loads this library holds the array
-// until the process exits.
+// allocation. The kernel's scratch (the work list, the view bases and the used
+// block ids, normally in the plan's cudaMalloc'd buffer) lives in the
+// file-scope array below instead. Every GPU that loads this library holds the
+// array until the process exits.
 // ---------------------------------------------------------------------------
 #include <mutex>
 
@@ -786,16 +743,17 @@ struct PreallocScratch {
     bool ready = false;
     unsigned char *addr = nullptr;   // device address of g_kvr_prealloc_scratch
     int sms = 0;
+    std::mutex use;                  // held from a call's copy to its launch
 };
 
 PreallocScratch g_prealloc[KVR_PREALLOC_MAX_DEVICES];
-std::mutex g_prealloc_mu;
+std::mutex g_prealloc_setup_mu;
 
 // Once per device, with that device current: the array's device address. In
 // host code the array's name is only a host-side stand-in, so the kernel must
 // be given this address, never the name.
-kvr_status prealloc_setup(int dev, PreallocScratch *out) {
-    std::lock_guard<std::mutex> lock(g_prealloc_mu);
+kvr_status prealloc_setup(int dev, PreallocScratch **out) {
+    std::lock_guard<std::mutex> lock(g_prealloc_setup_mu);
     PreallocScratch &s = g_prealloc[dev];
     if (!s.ready) {
         void *p = nullptr;
@@ -810,7 +768,7 @@ kvr_status prealloc_setup(int dev, PreallocScratch *out) {
         s.sms = sms;
         s.ready = true;
     }
-    *out = s;
+    *out = &s;
     return KVR_OK;
 }
 
@@ -820,51 +778,72 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev < 0 || dev >= KVR_PREALLOC_MAX_DEVICES) return KVR_ERR_UNSUPPORTED;
-    PreallocScratch sc;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The tables are copied from host memory that is gone when this call
+    // returns, so the call enqueues nothing on a stream that is being captured.
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capturing) != cudaSuccess) {
+        cudaGetLastError();
+        return KVR_ERR_UNSUPPORTED;
+    }
+    if (capturing != cudaStreamCaptureStatusNone) return KVR_ERR_UNSUPPORTED;
+    PreallocScratch *sc = nullptr;
     kvr_status st = prealloc_setup(dev, &sc);
     if (st != KVR_OK) return st;
 
     KvrHostPlan hp;
+    std::vector<unsigned char> staged;
+    Piece pieces[6];
+    DevTables t = {};
     try {
-        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc.sms, 0, 0, &hp, nullptr,
+        st = kvr_build_host_plan(desc, nullptr, nullptr, nullptr, sc->sms, 0, 0, &hp, nullptr,
                                  nullptr);
+        if (st == KVR_OK) st = check_pools(hp, dev);
+        if (st == KVR_OK && tables_bytes(hp) > KVR_PREALLOC_SCRATCH_BYTES)
+            st = KVR_ERR_SCRATCH_LIMIT;
+        if (st == KVR_OK && !hp.items.empty()) {
+            // every table in one host buffer laid out like the scratch: one copy
+            t = place_tables(hp, sc->addr, pieces);
+            staged.resize(tables_bytes(hp));
+            size_t off = 0;
+            for (const Piece &pc : pieces) {
+                if (pc.bytes > 0) memcpy(staged.data() + off, pc.host, pc.bytes);
+                off += pc.bytes;
+            }
+        }
     } catch (...) {
         st = KVR_ERR_NOMEM;
     }
-    if (st == KVR_OK) st = check_pools(hp, dev);
     if (st != KVR_OK) return st;
-    if (tables_bytes(hp) > KVR_PREALLOC_SCRATCH_BYTES) return KVR_ERR_SCRATCH_LIMIT;
     if (hp.items.empty()) return KVR_OK;
 
-    // The array is overwritten up to what this call reads, so nothing needs
-    // clearing; the copies are ordered before the launch on `stream`.
-    cudaStream_t s = (cudaStream_t)stream;
-    Piece pieces[6];
-    const DevTables t = place_tables(hp, sc.addr, pieces);
-    unsigned char *to = sc.addr;
-    for (const Piece &pc : pieces) {
-        if (pc.bytes > 0 &&
-            cudaMemcpyAsync(to, pc.host, pc.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return KVR_ERR_CUDA;
-        to += pc.bytes;
-    }
-
+    // a stream on a green context with fewer SMs gets a grid shaped for them
+    const int32_t green = kvr_stream_green_sms(stream);
+    const int32_t slices = green > 0 && green < hp.sm_count
+                               ? kvr_range_slices(hp, hp.num_layers, green)
+                               : hp.slices_all;
     const KvrArgs a = kvr_launch_args(hp, t.items, t.sbt, t.dbt, nullptr, t.src_base,
-                                      t.dst_base, 0, hp.slices_all);
-    const uint64_t grid = (uint64_t)hp.num_layers * a.tasks_per_layer;
+                                      t.dst_base, 0, slices);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.gridDim = dim3((unsigned)((uint64_t)hp.num_layers * a.tasks_per_layer), 1, 1);
     cfg.blockDim = dim3(KVR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    // No programmatic dependent launch here: the kernel reads its tables before
-    // its grid-dependency wait, and these tables were just copied on `stream`,
-    // so the launch must be fully ordered after the copies.
+    // No programmatic dependent launch: the kernel follows this call's copy of
+    // its tables on `stream` and must start only after it.
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, pick_kernel(KVR_CONV_NONE, KVR_MODE_WHOLE, kvr_replicated(hp.g)),
-                              a) ==
-                   cudaSuccess
+    // The copy and the launch go onto the stream back to back under the
+    // device's lock, so calls from several host threads on one stream cannot
+    // interleave one call's copy with another call's kernel. The array is
+    // overwritten up to what this call reads, so nothing needs clearing.
+    std::lock_guard<std::mutex> lock(sc->use);
+    if (cudaMemcpyAsync(sc->addr, staged.data(), staged.size(), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return KVR_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg,
+                              pick_kernel(KVR_CONV_NONE, KVR_MODE_WHOLE, kvr_replicated(hp.g)),
+                              a) == cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
 }

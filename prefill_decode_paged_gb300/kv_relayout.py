@@ -30,7 +30,8 @@ EXPORTS = ("kv_relayout_desc_bytes", "kv_relayout_plan", "kv_relayout_layer",
            "kv_relayout_plan_convert", "kv_relayout_desc_bytes_ex", "kv_relayout_plan_ex",
            "kv_relayout_sm_stream_create", "kv_relayout_sm_stream_destroy",
            "kv_relayout_plan_launch_shape", "kv_relayout_layers", "kv_relayout_layers_ex",
-           "kv_relayout_debug_status", "kv_relayout_debug_narrow")
+           "kv_relayout_debug_status", "kv_relayout_debug_narrow",
+           "kv_relayout_staging_bytes", "kv_relayout_plan_pack", "kv_relayout_plan_unpack")
 DTYPE_BF16 = 1
 DTYPE_FP8_E4M3 = 2
 LAUNCH_NO_WAIT = 1
@@ -133,6 +134,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kv_relayout_debug_status.argtypes = [p, p]
     lib.kv_relayout_debug_narrow.restype = i32
     lib.kv_relayout_debug_narrow.argtypes = [p, i64]
+    lib.kv_relayout_staging_bytes.restype = i32
+    lib.kv_relayout_staging_bytes.argtypes = [p, i32, p]
+    lib.kv_relayout_plan_pack.restype = i32
+    lib.kv_relayout_plan_pack.argtypes = [p, p, p, p]
+    lib.kv_relayout_plan_unpack.restype = i32
+    lib.kv_relayout_plan_unpack.argtypes = [p, p, p, p]
     return lib
 
 
@@ -344,8 +351,10 @@ def relayout_all_prealloc(src_pools, dst_pools, stream=None, **geometry):
     into a fixed 1 MiB device array the library keeps on every GPU it runs on;
     larger work lists raise ``KVR_ERR_SCRATCH_LIMIT`` (use :class:`RelayoutPlan`).
     The first call on a device sets the array up and should come before any
-    stream capture. Calls share the array: calls that overlap on the GPU (on
-    different, unordered streams) race.
+    stream capture; on a stream under capture the call raises
+    ``KVR_ERR_UNSUPPORTED`` and enqueues nothing. Calls share the array: calls from
+    several threads on one stream run one after another, calls that overlap on the
+    GPU (on different, unordered streams) race.
     """
     _check_extents(src_pools, dst_pools, None, None, None, geometry)
     d = _Desc(src_pools, dst_pools, **geometry)
@@ -407,6 +416,20 @@ class RelayoutPlan:
         if st != 0:
             raise KVRelayoutError(st, "kv_relayout_plan_bytes")
         self.bytes_read, self.bytes_written = r.value, w.value
+
+    @classmethod
+    def _adopt(cls, handle, num_layers, keep):
+        """Wrap a plan the library already made (``keep``: the host objects its
+        descriptor pointed to, held for the plan's lifetime)."""
+        self = cls.__new__(cls)
+        self._h, self._keep, self.num_layers = handle, keep, num_layers
+        r, w = ctypes.c_int64(), ctypes.c_int64()
+        st = library().kv_relayout_plan_bytes(self._h, ctypes.byref(r), ctypes.byref(w))
+        if st != 0:
+            self.close()
+            raise KVRelayoutError(st, "kv_relayout_plan_bytes")
+        self.bytes_read, self.bytes_written = r.value, w.value
+        return self
 
     @property
     def launch_shape(self):
@@ -505,43 +528,65 @@ class SmStream:
 
 # -- staging buffer: pd.py's gathered [seq, kv_heads, head_dim] per layer ---------------
 
-def staging_geometry(geometry, side):
-    """Geometry with one side replaced by a staging buffer [L][C][sum n][H][D]: a single
-    shard of one-token blocks, request r's tokens at offset sum(n[:r])."""
-    lens = np.asarray(geometry["seq_lens"], dtype=np.int64)
-    total = int(lens.sum())
-    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    ids = np.arange(total, dtype=np.int32)
-    g = dict(geometry)
-    g.update({f"{side}_tp": 1, f"{side}_block": 1, f"{side}_num_blocks": max(total, 1),
-              f"{side}_off": off, f"{side}_bt": ids})
-    return g
+def staging_bytes(staging_elem_bytes, **geometry):
+    """Bytes of the staging buffer [L][C][sum n][H][D] of ``staging_elem_bytes``-byte
+    elements for this batch (``kv_relayout_staging_bytes``)."""
+    d = _Desc(None, None, **geometry)
+    out = ctypes.c_int64()
+    st = library().kv_relayout_staging_bytes(ctypes.byref(d.desc), int(staging_elem_bytes),
+                                             ctypes.byref(out))
+    if st != 0:
+        raise KVRelayoutError(st, "kv_relayout_staging_bytes")
+    return out.value
 
 
-def staging_layout(buf, num_layers, num_components):
-    """Layout of a staging tensor shaped [L][C][tokens][H][D] (one shard)."""
-    if len(buf.shape) != 5 or tuple(buf.shape[:2]) != (num_layers, num_components):
+def _check_staging(buf, convert, pack, geometry):
+    """The staging tensor must be [L][C][sum n][H][D], contiguous, of the staging dtype."""
+    L, C = geometry["num_layers"], geometry["num_components"]
+    total = int(np.asarray(geometry["seq_lens"], dtype=np.int64).sum())
+    want = (L, C, total, geometry["kv_heads"], geometry["head_dim"])
+    if tuple(int(x) for x in buf.shape) != want:
         raise ValueError(f"staging buffer is {list(buf.shape)}; expected "
-                         f"[{num_layers}][{num_components}][tokens][heads][head_dim]")
-    L, C, T, H, D = buf.shape
-    return layout_of_views([[[buf[l, c].reshape(T, 1, H, D) for c in range(C)]
-                             for l in range(L)]])
+                         f"[{L}][{C}][{total}][heads][head_dim] = {list(want)}")
+    if not _contiguous(buf):
+        raise ValueError("staging buffer must be contiguous")
+    es = geometry["elem_bytes"]
+    if pack and convert is not None:
+        es = _DTYPE_BYTES.get(int(convert["dst_dtype"]), es)
+    have = _nbytes(buf)
+    if have is not None and have != staging_bytes(es, **geometry):
+        raise ValueError(f"staging buffer holds {have} bytes of "
+                         f"{have // max(1, int(np.prod(want)))}-byte elements; the staging "
+                         f"side holds {es}-byte elements")
+
+
+def _staging_plan(pools, staging, convert, pack, geometry):
+    if pack:
+        _check_extents(pools, None, convert, None, {}, geometry)
+    else:
+        _check_extents(None, pools, convert, {}, None, geometry)
+    _check_staging(staging, convert, pack, geometry)
+    d = _Desc(pools if pack else None, None if pack else pools, **geometry)
+    cv = _Convert(**convert) if convert is not None else None
+    h = ctypes.c_void_p()
+    fn = library().kv_relayout_plan_pack if pack else library().kv_relayout_plan_unpack
+    st = fn(ctypes.byref(d.desc), _ptr(staging), ctypes.byref(cv.conv) if cv else None,
+            ctypes.byref(h))
+    if st != 0:
+        raise KVRelayoutError(st, "kv_relayout_plan_pack" if pack else "kv_relayout_plan_unpack")
+    return RelayoutPlan._adopt(h, geometry["num_layers"], keep=(d, cv, staging, pools))
 
 
 def pack_plan(src_pools, staging, convert=None, **geometry):
     """Plan that gathers every request's KV out of the prefill pools into ``staging``
     ([L][C][sum n][H][D]: pd.py's per-layer [seq, kv_heads, head_dim], requests one
-    after another), merging the prefill TP shards' heads."""
-    g = staging_geometry(geometry, "dst")
-    return RelayoutPlan(src_pools, None, convert=convert,
-                        dst_layout=staging_layout(staging, g["num_layers"], g["num_components"]),
-                        **g)
+    after another), merging the prefill TP shards' heads (``kv_relayout_plan_pack``;
+    the geometry's decode-side entries are not used)."""
+    return _staging_plan(src_pools, staging, convert, True, geometry)
 
 
 def unpack_plan(staging, dst_pools, convert=None, **geometry):
     """Plan that writes a staging buffer filled by :func:`pack_plan` into the decode
-    pools through the decode block table, splitting heads over the decode TP shards."""
-    g = staging_geometry(geometry, "src")
-    return RelayoutPlan(None, dst_pools, convert=convert,
-                        src_layout=staging_layout(staging, g["num_layers"], g["num_components"]),
-                        **g)
+    pools through the decode block table, splitting heads over the decode TP shards
+    (``kv_relayout_plan_unpack``; the geometry's prefill-side entries are not used)."""
+    return _staging_plan(dst_pools, staging, convert, False, geometry)

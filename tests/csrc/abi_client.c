@@ -5,7 +5,10 @@
  *
  *   abi_client host   validation and byte counts on fake pool addresses (no GPU)
  *   abi_client gpu    pools from cudaMalloc; whole-prompt, per-layer and layer
- *                     range launches checked byte for byte against the C oracle
+ *                     range launches checked byte for byte against the C oracle;
+ *                     pack into a staging buffer (checked against the oracle's
+ *                     gather into [L][C][sum n][H][D]) and unpack from it (checked
+ *                     against the oracle's direct relayout)
  *
  * Exit status 0 on success; a message on stderr otherwise.
  */
@@ -24,6 +27,18 @@ int kvo_relayout(int32_t layer_begin, int32_t layer_end, int32_t num_layers,
                  const uint8_t *const *src_pools, uint8_t *const *dst_pools,
                  int32_t num_requests, const int32_t *seq_lens, const int64_t *src_off,
                  const int32_t *src_bt, const int64_t *dst_off, const int32_t *dst_bt);
+
+/* The oracle on any layout (per-(shard, layer, component) view bases and strides). */
+int kvo_relayout_general(int32_t layer_begin, int32_t layer_end, int32_t num_layers,
+                         int32_t num_components, int32_t kv_heads, int32_t head_dim,
+                         int32_t src_dtype, int32_t dst_dtype, int32_t elem_bytes,
+                         int32_t per_head, const float *scales, int32_t src_tp, int32_t dst_tp,
+                         int32_t src_block, int32_t dst_block, const uint64_t *src_base,
+                         int64_t s_block_stride, int64_t s_token_stride, int64_t s_head_stride,
+                         const uint64_t *dst_base, int64_t d_block_stride,
+                         int64_t d_token_stride, int64_t d_head_stride, int32_t num_requests,
+                         const int32_t *seq_lens, const int64_t *src_off, const int32_t *src_bt,
+                         const int64_t *dst_off, const int32_t *dst_bt);
 
 #include <cuda_runtime_api.h>
 #define H2D cudaMemcpyHostToDevice
@@ -137,6 +152,11 @@ static int host_mode(void) {
     if (kv_relayout_desc_bytes(NULL, &r, &w) != KVR_ERR_INVALID_ARG) FAIL("NULL accepted");
     if (strcmp(kv_relayout_strerror((kvr_status)12345), "unknown status") != 0)
         FAIL("strerror of an unknown status");
+    describe(&d, src, dst);
+    if (kv_relayout_staging_bytes(&d, ES, &r) != KVR_OK ||
+        r != (int64_t)(300 + 77) * L * C * H * D * ES)
+        FAIL("staging bytes %lld", (long long)r);
+    if (kv_relayout_staging_bytes(&d, 3, &r) != KVR_ERR_INVALID_ARG) FAIL("3-byte staging");
     printf("abi_client host: ok\n");
     return 0;
 }
@@ -181,6 +201,74 @@ static int gpu_run(int mode, uint8_t *const *h_src, uint8_t *const *h_ref, void 
     return 0;
 }
 
+/* pack into a staging buffer [L][C][sum n][H][D], then unpack it into fresh decode
+ * pools layer by layer: the staging bytes against the oracle's gather into that
+ * buffer, the decode bytes against the oracle's direct relayout */
+#define TOTAL (300 + 0 + 77)
+static int gpu_staging(uint8_t *const *h_src, uint8_t *const *h_ref, void *const *d_src) {
+    const int64_t row = (int64_t)D * ES, tok = row * H, plane = tok * TOTAL;
+    const int64_t stage_bytes = plane * L * C;
+    const int64_t hs = (H / TP_S) * row, sblk = BP * hs;          /* standard prefill strides */
+    int64_t stage_off[R + 1], got_bytes = -1;
+    int32_t stage_ids[TOTAL];
+    uint64_t sbase[TP_S * L * C], dbase[L * C];
+    uint8_t *want, *got;
+    void *d_stage, *d_dst[TP_D];
+    kvr_desc d;
+    kvr_plan *plan = NULL;
+    kvr_status st = KVR_OK;
+    const float one = 1.0f;
+    int r, s, v, l;
+    stage_off[0] = 0;
+    for (r = 0; r < R; ++r) stage_off[r + 1] = stage_off[r] + lens[r];
+    for (v = 0; v < TOTAL; ++v) stage_ids[v] = v;
+    want = (uint8_t *)calloc((size_t)stage_bytes, 1);
+    got = (uint8_t *)malloc((size_t)(stage_bytes > dst_pool_bytes ? stage_bytes : dst_pool_bytes));
+    if (want == NULL || got == NULL) FAIL("host allocation");
+    for (s = 0; s < TP_S; ++s)
+        for (v = 0; v < L * C; ++v)
+            sbase[s * L * C + v] = (uint64_t)(uintptr_t)(h_src[s] + (int64_t)v * NP * sblk);
+    for (v = 0; v < L * C; ++v) dbase[v] = (uint64_t)(uintptr_t)(want + (int64_t)v * plane);
+    if (kvo_relayout_general(0, L, L, C, H, D, 0, 0, ES, 0, &one, TP_S, 1, BP, 1, sbase, sblk,
+                             hs, row, dbase, tok, tok, row, R, lens, src_off, src_bt,
+                             stage_off, stage_ids) != 0)
+        FAIL("oracle (staging)");
+    describe(&d, d_src, NULL);
+    if (kv_relayout_staging_bytes(&d, ES, &got_bytes) != KVR_OK || got_bytes != stage_bytes)
+        FAIL("staging bytes %lld", (long long)got_bytes);
+    if (cudaMalloc(&d_stage, (size_t)stage_bytes) != 0) FAIL("cudaMalloc");
+    cudaMemset(d_stage, 0, (size_t)stage_bytes);
+    st = kv_relayout_plan_pack(&d, d_stage, NULL, &plan);
+    if (st != KVR_OK) FAIL("plan_pack: %s", kv_relayout_strerror(st));
+    st = kv_relayout_all(plan, NULL);
+    if (st != KVR_OK) FAIL("pack launch: %s", kv_relayout_strerror(st));
+    if (cudaDeviceSynchronize() != 0) FAIL("synchronize");
+    kv_relayout_plan_destroy(plan);
+    cudaMemcpy(got, d_stage, (size_t)stage_bytes, D2H);
+    if (memcmp(got, want, (size_t)stage_bytes) != 0) FAIL("packed staging differs from the oracle");
+    for (s = 0; s < TP_D; ++s) {
+        if (cudaMalloc(&d_dst[s], (size_t)dst_pool_bytes) != 0) FAIL("cudaMalloc");
+        cudaMemset(d_dst[s], 0xEE, (size_t)dst_pool_bytes);
+    }
+    describe(&d, NULL, d_dst);
+    st = kv_relayout_plan_unpack(&d, d_stage, NULL, &plan);
+    if (st != KVR_OK) FAIL("plan_unpack: %s", kv_relayout_strerror(st));
+    for (l = 0; l < L && st == KVR_OK; ++l) st = kv_relayout_layer(plan, l, NULL);
+    if (st != KVR_OK) FAIL("unpack launch: %s", kv_relayout_strerror(st));
+    if (cudaDeviceSynchronize() != 0) FAIL("synchronize");
+    kv_relayout_plan_destroy(plan);
+    for (s = 0; s < TP_D; ++s) {
+        cudaMemcpy(got, d_dst[s], (size_t)dst_pool_bytes, D2H);
+        if (memcmp(got, h_ref[s], (size_t)dst_pool_bytes) != 0)
+            FAIL("unpacked decode shard %d differs from the oracle", s);
+        cudaFree(d_dst[s]);
+    }
+    cudaFree(d_stage);
+    free(want);
+    free(got);
+    return 0;
+}
+
 static int gpu_mode(void) {
     uint8_t *h_src[TP_S], *h_ref[TP_D];
     void *d_src[TP_S];
@@ -205,12 +293,13 @@ static int gpu_mode(void) {
         FAIL("oracle");
     for (mode = 0; mode < 3; ++mode)
         if (gpu_run(mode, h_src, h_ref, d_src) != 0) return 1;
+    if (gpu_staging(h_src, h_ref, d_src) != 0) return 1;
     for (s = 0; s < TP_S; ++s) {
         cudaFree(d_src[s]);
         free(h_src[s]);
     }
     for (s = 0; s < TP_D; ++s) free(h_ref[s]);
-    printf("abi_client gpu: ok (whole-prompt, per-layer, layer ranges)\n");
+    printf("abi_client gpu: ok (whole-prompt, per-layer, layer ranges, pack, unpack)\n");
     return 0;
 }
 

@@ -217,6 +217,22 @@ int64_t emu_walk_ex(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *d
                 sm_count, layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, copy, chunks);
 }
 
+// kv_relayout_plan_pack (pack != 0) / _unpack on host buffers: *d with one side
+// replaced by the library's own staging side over `staging`
+// (kvr_staging_desc), walked like emu_walk_ex; the other side is d's pools in
+// the standard layout. Every row must fall inside the given ranges.
+int64_t emu_staging(const kvr_desc *d, void *staging, int32_t pack, const uint64_t *src_ranges,
+                    int64_t n_src, const uint64_t *dst_ranges, int64_t n_dst, int sm_count,
+                    int32_t layer, int32_t copy, int64_t *chunks) {
+    KvrStaging st;
+    kvr_desc d2;
+    const kvr_status s = kvr_staging_desc(d, staging, nullptr, pack != 0, &st, &d2);
+    if (s != KVR_OK) return s;
+    return walk(&d2, pack ? nullptr : &st.layout, pack ? &st.layout : nullptr, nullptr,
+                given_ranges(src_ranges, n_src), given_ranges(dst_ranges, n_dst), sm_count,
+                layer < 0 ? 0 : layer, layer < 0 ? -1 : 1, copy, chunks);
+}
+
 // kv_relayout_layers(first, count) on host pools through the kernel's
 // decomposition (copy != 0: move the bytes; 0: bounds check only).
 int64_t emu_relayout_range(const kvr_desc *d, int sm_count, int32_t first, int32_t count,

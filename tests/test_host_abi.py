@@ -589,3 +589,39 @@ def test_plain_c_client_validates_on_the_host():
     out = subprocess.run([exe, "host"], capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
     assert "host: ok" in out.stdout
+
+
+# -- pack / unpack through a staging buffer ---------------------------------------------
+
+def test_staging_bytes_and_pack_unpack_statuses(cuda_lib):
+    """kv_relayout_staging_bytes is L * C * (sum of n) * H * D * element bytes (host
+    only); pack and unpack plans refuse what they cannot describe before any CUDA call,
+    and otherwise need the GPU."""
+    import ctypes
+    import torch
+    w = wl.llama70b()
+    g = w.geometry()
+    assert kr.staging_bytes(2, **g) == 4096 * 80 * 2 * 8 * 128 * 2 == 1_342_177_280
+    assert kr.staging_bytes(1, **g) == 671_088_640
+    q = wl.qwen32k()
+    assert kr.staging_bytes(2, **q.geometry()) == 4 * 32768 * 262_144      # 256 KB per token
+    assert status_of(lambda: kr.staging_bytes(3, **g)) == "KVR_ERR_INVALID_ARG"
+    assert status_of(lambda: kr.staging_bytes(2, **dict(g, seq_lens=[-1], src_off=[0, 0],
+                                                        dst_off=[0, 0]))) == \
+        "KVR_ERR_INVALID_ARG"
+    s, _ = fake_pools(w)
+    lib = kr.library()
+
+    def plan(fn, desc, staging):
+        h = ctypes.c_void_p(12345)
+        st = fn(ctypes.byref(desc.desc), staging, None, ctypes.byref(h))
+        assert h.value is None                     # *out is NULL on every failure
+        return kr.STATUS[st]
+    d = kr._Desc(s, None, **g)
+    assert plan(lib.kv_relayout_plan_pack, d, None) == "KVR_ERR_INVALID_ARG"
+    assert plan(lib.kv_relayout_plan_unpack, kr._Desc(None, None, **g), None) == \
+        "KVR_ERR_INVALID_ARG"
+    empty = kr._Desc(s, None, **dict(g, seq_lens=[0], src_off=[0, 0], dst_off=[0, 0]))
+    assert plan(lib.kv_relayout_plan_pack, empty, 1 << 45) == "KVR_ERR_INVALID_ARG"
+    if not torch.cuda.is_available():
+        assert plan(lib.kv_relayout_plan_pack, d, 1 << 45) == "KVR_ERR_CUDA"

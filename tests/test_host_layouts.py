@@ -133,8 +133,38 @@ def test_emulated_kernel_head_major_prefill(emu, geo):
         np.testing.assert_array_equal(a, b)
 
 
+def _staging_tables(g, side):
+    """The staging buffer's documented indexing as one side's tables: one-token blocks,
+    request r's tokens at rows sum(n[:r]) .. sum(n[:r + 1]) - 1 (block id = row)."""
+    lens = np.asarray(g["seq_lens"], dtype=np.int64)
+    total = int(lens.sum())
+    t = dict(g)
+    t.update({f"{side}_tp": 1, f"{side}_block": 1,
+              f"{side}_off": np.concatenate([[0], np.cumsum(lens)]).astype(np.int64),
+              f"{side}_bt": np.arange(total, dtype=np.int32)})
+    return t
+
+
+def _emu_staging(emu, w, stage, pack, pools):
+    emu.emu_staging.restype = ctypes.c_int64
+    emu.emu_staging.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                ctypes.c_int64, ctypes.c_int, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_void_p]
+    d = kr._Desc(pools if pack else None, None if pack else pools, **w.geometry())
+    sr, dr = (_ranges(pools), _ranges([stage])) if pack else (_ranges([stage]), _ranges(pools))
+    n = ctypes.c_int64()
+    bad = emu.emu_staging(ctypes.byref(d.desc), stage.ctypes.data, int(pack), sr.ctypes.data,
+                          len(sr) // 2, dr.ctypes.data, len(dr) // 2, SMS, -1, 1,
+                          ctypes.byref(n))
+    assert bad == 0, f"{bad} rows or units outside their buffers / misaligned"
+
+
 @pytest.mark.parametrize("geo", sorted(GEOS))
 def test_emulated_pack_and_unpack_through_a_staging_buffer(emu, geo):
+    """The library's own staging side (kvr_staging_desc, as kv_relayout_plan_pack and
+    _unpack build it), walked by the emulated kernel: pack equals the oracle's gather
+    into [L][C][sum n][H][D], pack then unpack equals the direct relayout."""
     w = _w(3, **GEOS[geo])
     src_bufs = [_aligned(w.src_shape(), np.uint16) for _ in range(w.src_tp)]
     for a, b in zip(src_bufs, w.src_pools_numpy()):
@@ -142,19 +172,15 @@ def test_emulated_pack_and_unpack_through_a_staging_buffer(emu, geo):
     total = int(w.seq_lens.sum())
     stage = _aligned((L_, C_, total, w.kv_heads, w.head_dim), np.uint16)
     stage[...] = 0
-    sviews = [[[stage[l, c].reshape(total, 1, w.kv_heads, w.head_dim) for c in range(C_)]
-               for l in range(L_)]]
-    g_pack = kr.staging_geometry(w.geometry(), "dst")
-    _walk(emu, w, _std(w, src_bufs, "src"), src_bufs, sviews, [stage], geometry=g_pack)
+    _emu_staging(emu, w, stage, True, src_bufs)
     want = np.zeros_like(stage)
     oracle.relayout_general(_std(w, src_bufs, "src"),
                             [[[want[l, c].reshape(total, 1, w.kv_heads, w.head_dim)
                                for c in range(C_)] for l in range(L_)]],
-                            **_tables(g_pack))
+                            **_tables(_staging_tables(w.geometry(), "dst")))
     np.testing.assert_array_equal(stage, want)
-    got_bufs, got_views = dst_family(w, "standard")
-    g_unpack = kr.staging_geometry(w.geometry(), "src")
-    _walk(emu, w, sviews, [stage], got_views, got_bufs, geometry=g_unpack)
+    got_bufs, _ = dst_family(w, "standard")
+    _emu_staging(emu, w, stage, False, got_bufs)
     ref = w.dst_pools_numpy()
     oracle.relayout(src_bufs, ref, **w.geometry())
     for a, b in zip(ref, got_bufs):
@@ -264,7 +290,7 @@ def test_binding_refuses_tensors_smaller_than_the_geometry(emu):
     # staging buffers: the batch's token count, all heads
     total = int(w.seq_lens.sum())
     stage = _aligned((L_, C_, total - 1, w.kv_heads, w.head_dim), np.uint16)
-    with pytest.raises(ValueError, match="dst views"):
+    with pytest.raises(ValueError, match="staging buffer"):
         kr.pack_plan(src, stage, **g)
     with pytest.raises(ValueError, match="staging buffer"):
         kr.pack_plan(src, stage[0], **g)
