@@ -19,7 +19,7 @@
 #define KVR_UNROLL_LAYER 8       // the same for per-layer bit-copy launches
 #endif
 #ifndef KVR_UNROLL_LAYER_CONVERT
-#define KVR_UNROLL_LAYER_CONVERT 4  // per-layer FP8 -> BF16 launches (two stores per unit)
+#define KVR_UNROLL_LAYER_CONVERT 2  // per-layer FP8 -> BF16 launches (two stores per unit)
 #endif
 #ifndef KVR_UNROLL_LAYER_QUANT
 #define KVR_UNROLL_LAYER_QUANT 2    // per-layer BF16 -> FP8 launches: units (two loads each)

@@ -59,10 +59,24 @@ __device__ __forceinline__ uint4 load_stream(const unsigned char *p) {
     return v;
 }
 
-// Fetch [addr, addr + bytes) into L2 (no completion to wait for; bytes a
-// multiple of 16, addr 16-byte aligned).
+// Fetch [addr, addr + bytes) into L2 (a hint: no completion to wait for, no
+// register written; bytes a multiple of 16, addr 16-byte aligned). The SM's
+// bulk copy unit takes these requests one at a time.
 __device__ __forceinline__ void prefetch_l2(uint64_t addr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
+// The same hint as one prefetch.global.L2 per 128-byte line of [addr, addr +
+// bytes), from the thread that computed the row: no bulk copy unit in the way,
+// so a per-layer CTA is ready to run sooner (256 bulk requests per CTA took ~1
+// us to issue), but the rows reach L2 later. Measured on ordered 70B layers:
+// the converting launches gain (BF16 -> FP8 5236 -> 5302, FP8 -> BF16 4295 ->
+// 4591 GB/s), the bit copy loses (6204 -> 6035), so it keeps the bulk form.
+// The lines hold bytes of the row, so they lie in its pages: nothing is touched
+// outside the pools.
+__device__ __forceinline__ void prefetch_l2_lines(uint64_t addr, uint32_t bytes) {
+    for (uint64_t p = addr & ~(uint64_t)127; p < addr + bytes; p += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 #ifdef KVR_DEVICE_CHECKS
@@ -161,10 +175,15 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                 kvr_row<true>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base,
                               w0 * dc + t, &sa, &da, &fidx);
                 KVR_CHECK_ROW(a, sa, da);
+                // the first decode copy of each prefill row asks for it (converting
+                // instances here; see the plain branch)
+                if (PF && CONV != KVR_CONV_NONE && !waited && t - (t / dc) * dc == 0 &&
+                    !KVR_SRC_DROPPED(make_ulonglong2(sa, da)))
+                    prefetch_l2_lines(sa, (uint32_t)a.g.src_row_bytes);
                 rows[t] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[t] = a.factors[fidx];
             }
-            if (PF && !waited) {
+            if (PF && CONV == KVR_CONV_NONE && !waited) {
                 // the first copy of each row this thread built (see the plain branch)
                 for (uint32_t t = threadIdx.x; t < t_end; t += KVR_THREADS)
                     if (t - (t / dc) * dc == 0 && !KVR_SRC_DROPPED(rows[t]))
@@ -241,10 +260,14 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                 kvr_row<false>(a.g, layer, it, a.sbt, a.dbt, a.src_base, a.dst_base, r, &sa,
                                &da, &fidx);
                 KVR_CHECK_ROW(a, sa, da);
+                // converting instances ask L2 for the row here (see prefetch_l2_lines)
+                if (PF && CONV != KVR_CONV_NONE && !waited &&
+                    !KVR_SRC_DROPPED(make_ulonglong2(sa, da)))
+                    prefetch_l2_lines(sa, (uint32_t)a.g.src_row_bytes);
                 rows[r - w0] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
             }
-            if (PF && !waited) {
+            if (PF && CONV == KVR_CONV_NONE && !waited) {
                 // Before the grid-dependency wait, pull the prefill rows this
                 // thread just entered into L2, so the loads after the wait hit
                 // L2 instead of starting cold: the wait drains the previous
@@ -314,15 +337,15 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
 
 using KvrKernel = void (*)(KvrArgs);
 
-// Kernel instance for a conversion, launch mode and head replication: 8 loads
-// in flight per thread, but 4 for dequantizing launches and converting
-// per-layer ones (16-element units of BF16 take two loads each to quantize and
-// two stores to dequantize) except ordered one-wave quantizing ones. Measured
-// with 8 loads: those rose 4351 -> 4592 GB/s (70B layers), while quantizing
-// launches of several waves lost 1-2 % (Qwen 32K and MLA layers, shaped for 4
-// instead of 6 CTAs per SM); dequantizing ones with 8 units (80 registers, 3
-// CTAs per SM) ran slower than with 4 (48 registers, 5 CTAs per SM) once
-// whole-prompt items were capped like a bit copy's.
+// Kernel instance for a conversion, launch mode and head replication (units
+// in flight per thread; a quantizing unit takes two loads, a dequantizing one
+// two stores): the bit copy 8; quantizing 4 whole-prompt and in ordered
+// one-wave per-layer launches (the prefetching instance), 2 in other per-layer
+// launches; dequantizing 4 whole-prompt, 2 per layer. Measured on 70B layers
+// (one GB300, GB/s): the prefetching quantizer with 4 units 5239, with 2 5075;
+// the per-layer dequantizer with 2 units 4307 (ordered) / 5620 (no wait), with
+// 4 4163 / 5245, with 1 3755 / 4891, with 8 (80 registers) 3805 / 4702; 2 units
+// also won on the multi-wave MLA, Qwen 32K and 8B layers.
 template <int MODE, bool REP>
 KvrKernel pick_instance(int32_t conv) {
     constexpr bool LAYER = MODE != KVR_MODE_WHOLE;
