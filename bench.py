@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 METRIC = "KV relayout GB/s (read+write) and % of GB300 HBM peak; ms per 4K-token 70B prompt"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("relayout.cu", "kvr_index.h", "plan.h", "plan.cpp")
+KERNEL_SOURCES = ("relayout.cu", "kvr_convert.cuh", "kvr_index.h", "plan.h", "plan.cpp")
 WORKLOAD_TEXT = {
     "llama70b": ("Llama-3-70B KV shape: 80 layers, 8 KV heads, head_dim 128, bf16 K/V; "
                  "1 x 4096-token prompt; prefill TP4 (2 heads/shard, block 16) -> decode TP8 "
