@@ -179,3 +179,61 @@ def test_pack_gives_pd_py_gather_and_unpack_gives_the_direct_relayout(geo):
     oracle.relayout(src_np, ref, **w.geometry())
     for a, t in zip(ref, dst):
         assert np.array_equal(t.cpu().numpy().view(np.uint16), a)
+
+
+def _staging_tables(w):
+    """The staging buffer's documented indexing as the decode side's tables (one shard of
+    one-token blocks, request r's tokens at rows sum(n[:r]) ..., block id = row)."""
+    t = _tables(w)
+    lens = np.asarray(w.seq_lens, dtype=np.int64)
+    t.update(dst_tp=1, dst_block=1, dst_off=np.concatenate([[0], np.cumsum(lens)]),
+             dst_bt=np.arange(int(lens.sum()), dtype=np.int32))
+    return t
+
+
+@pytest.mark.parametrize("geo", sorted(GEOS))
+def test_pack_and_unpack_with_conversion(geo):
+    """kv_relayout_plan_pack with a BF16 -> FP8 conversion fills the staging buffer with
+    the converting oracle's gather; a bit-copy pack followed by a quantizing unpack gives
+    the decode pools of one direct quantizing relayout (each element is rounded once on
+    either route), bit for bit."""
+    import torch
+    w = _w(7, **GEOS[geo])
+    rng = np.random.default_rng(17)
+    src_np = [rng.integers(0, 1 << 16, w.src_shape(), dtype=np.uint16) for _ in range(w.src_tp)]
+    scales = rng.uniform(0.01, 2.0, w.num_layers * 2 * w.kv_heads).astype(np.float32)
+    conv = dict(src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3, per_head=True, scales=scales)
+    src = [_np_t(a) for a in src_np]
+    L, C, total = w.num_layers, 2, int(w.seq_lens.sum())
+    # 1. a quantizing pack
+    stage8 = torch.full((L, C, total, w.kv_heads, w.head_dim), 0xEE, dtype=torch.uint8,
+                        device="cuda")
+    with pack_plan(src, stage8, convert=conv, **w.geometry()) as plan:
+        plan.run_all()
+        torch.cuda.synchronize()
+    want = np.full(tuple(stage8.shape), 0xEE, np.uint8)
+    sv = oracle.standard_views(src_np, L, C, w.src_num_blocks, w.src_block,
+                               max(w.kv_heads // w.src_tp, 1), w.head_dim)
+    oracle.relayout_general(sv, [[[want[l, c].reshape(total, 1, w.kv_heads, w.head_dim)
+                                   for c in range(C)] for l in range(L)]],
+                            src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3, per_head=1,
+                            scales=scales, **_staging_tables(w))
+    assert np.array_equal(stage8.cpu().numpy(), want)
+    # 2. a bit-copy pack, then a quantizing unpack into FP8 decode pools, layer by layer
+    stage = torch.zeros((L, C, total, w.kv_heads, w.head_dim), dtype=torch.int16,
+                        device="cuda")
+    with pack_plan(src, stage, **w.geometry()) as plan:
+        plan.run_all()
+    dst = [torch.full(w.dst_shape(), 0xFF, dtype=torch.uint8, device="cuda")
+           for _ in range(w.dst_tp)]
+    with unpack_plan(stage, dst, convert=conv, **w.geometry()) as plan:
+        for layer in range(L):
+            plan.run_layer(layer)
+        torch.cuda.synchronize()
+    ref = [np.full(w.dst_shape(), 0xFF, np.uint8) for _ in range(w.dst_tp)]
+    g = w.geometry()
+    g.pop("elem_bytes")
+    oracle.relayout_convert(src_np, ref, src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3,
+                            per_head=1, scales=scales, **g)
+    for a, t in zip(ref, dst):
+        assert np.array_equal(t.cpu().numpy(), a)
