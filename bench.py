@@ -86,9 +86,11 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--convert", default="none", choices=["none", "bf16_to_fp8", "fp8_to_bf16"],
                    help="change the KV dtype on the way (FP8 = E4M3, per-head scales)")
-    p.add_argument("--sm-sweep", default="",
-                   help="comma-separated SM counts: also time the whole-prompt relayout on "
-                        "streams limited to that many SMs (green contexts)")
+    p.add_argument("--sm-sweep", default=None,
+                   help="comma-separated SM counts: also time the whole-prompt relayout and "
+                        "the ordered per-layer launches on streams limited to that many SMs "
+                        "(green contexts); default 16,48,96 for the 70B default run, none "
+                        "otherwise; '' for none")
     p.add_argument("--modes", default="all,layer,graph,groups,formats,targets",
                    help="measurements to run: all (whole-prompt, the step), layer (per-layer "
                         "eager launches), graph (per-layer launches replayed from a CUDA "
@@ -780,10 +782,14 @@ def run_ours(args):
 
     # the whole-prompt relayout on streams limited to a number of SMs
     sm_sweep = None
-    if args.sm_sweep:
+    sweep_spec = args.sm_sweep
+    if sweep_spec is None:
+        sweep_spec = "16,48,96" if (args.config == "llama70b" and conv is None and
+                                    not args.layers) else ""
+    if sweep_spec:
         from prefill_decode_paged_gb300 import KVRelayoutError, SmStream
         sm_sweep = {}
-        for want in [int(x) for x in args.sm_sweep.split(",") if x]:
+        for want in [int(x) for x in sweep_spec.split(",") if x]:
             try:
                 sms = SmStream(want)
             except KVRelayoutError as e:      # no green contexts here: say so, go on

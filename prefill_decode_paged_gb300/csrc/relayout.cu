@@ -124,6 +124,14 @@ constexpr int kvr_min_ctas(int U, int CONV) {
                                                      : 0;
 }
 
+// U: units each thread keeps in flight before its stores. CONV: KvrConv.
+// MODE: KVR_MODE_WHOLE, KVR_MODE_LAYER or KVR_MODE_LAYER_PREFETCH. Per-layer
+// modes build the first row window before waiting for the previous grid
+// (hides the block-table reads in the previous launch's tail; whole-prompt
+// launches wait first, which measured 1.7 % faster there); the prefetching
+// one also asks L2 for those rows before the wait.
+// A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
+// REP: the plan replicates heads (a TP degree above H; see kvr_row).
 template <int U, int CONV, int MODE, bool REP>
 __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
