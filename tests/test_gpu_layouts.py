@@ -237,3 +237,46 @@ def test_pack_and_unpack_with_conversion(geo):
                             per_head=1, scales=scales, **g)
     for a, t in zip(ref, dst):
         assert np.array_equal(t.cpu().numpy(), a)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzzed_pack_then_unpack_equals_the_direct_relayout(seed):
+    """Random valid geometries (replicated heads included) through the C pack and
+    unpack plans: the staging buffer holds the oracle's gather, and unpacking it gives
+    the oracle's direct relayout, bit for bit (whole prompt and layer by layer)."""
+    import torch
+    from fuzz_cases import random_workload
+    w = random_workload(seed, max_tokens=300)
+    if int(w.seq_lens.sum()) == 0:
+        pytest.skip("empty batch: no staging buffer")
+    dt = {1: np.uint8, 2: np.uint16, 4: np.uint32}[w.elem_bytes]
+    tdt = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[w.elem_bytes]
+    src_np = w.src_pools_numpy()
+    src = [torch.from_numpy(a.view({1: np.uint8, 2: np.int16, 4: np.int32}[w.elem_bytes])).cuda()
+           for a in src_np]
+    L, C, total = w.num_layers, w.num_components, int(w.seq_lens.sum())
+    stage = torch.zeros((L, C, total, w.kv_heads, w.head_dim), dtype=tdt, device="cuda")
+    with pack_plan(src, stage, **w.geometry()) as plan:
+        plan.run_all()
+        torch.cuda.synchronize()
+    want = np.zeros(tuple(stage.shape), dt)
+    sv = oracle.standard_views(src_np, L, C, w.src_num_blocks, w.src_block,
+                               max(w.kv_heads // w.src_tp, 1), w.head_dim)
+    oracle.relayout_general(sv, [[[want[l, c].reshape(total, 1, w.kv_heads, w.head_dim)
+                                   for c in range(C)] for l in range(L)]],
+                            **_staging_tables(w))
+    assert np.array_equal(stage.cpu().numpy().view(dt), want)
+    ref = w.dst_pools_numpy()
+    oracle.relayout(src_np, ref, **w.geometry())
+    for mode in ("all", "layer"):
+        dst = [torch.from_numpy(a.view({1: np.uint8, 2: np.int16, 4: np.int32}[w.elem_bytes]))
+               .cuda() for a in w.dst_pools_numpy()]
+        with unpack_plan(stage, dst, **w.geometry()) as plan:
+            if mode == "all":
+                plan.run_all()
+            else:
+                for layer in range(L):
+                    plan.run_layer(layer)
+            torch.cuda.synchronize()
+        for a, t in zip(ref, dst):
+            assert np.array_equal(t.cpu().numpy().view(dt), a), mode

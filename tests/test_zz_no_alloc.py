@@ -147,3 +147,23 @@ def test_work_list_beyond_the_scratch_is_rejected_before_any_work():
         plan.run_all()
         torch.cuda.synchronize()
     assert int((dst[0] != -1).sum()) == n * 8
+
+
+def test_call_on_an_sm_limited_stream_matches_the_oracle():
+    """On a stream limited to a few SMs (a green context) the call shapes its grid for
+    that stream's SMs, as the allocating path does; the bytes are the oracle's."""
+    import torch
+    from prefill_decode_paged_gb300 import SmStream
+    w = BIG()
+    src_np = w.src_pools_numpy()
+    src = to_device(src_np, w.elem_bytes)
+    dst = w.dst_pools_torch("cuda")
+    try:
+        s = SmStream(16)
+    except KVRelayoutError as e:
+        pytest.skip(f"no green contexts here: {e.name}")
+    with s:
+        relayout_all_prealloc(src, dst, s.handle, **w.geometry())
+        torch.cuda.ExternalStream(s.handle).synchronize()
+    for k, (a, b) in enumerate(zip(_oracle(w, src_np), to_host(dst, w))):
+        assert np.array_equal(a, b), f"shard {k} differs from the oracle"
