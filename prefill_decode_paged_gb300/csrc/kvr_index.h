@@ -145,6 +145,9 @@ enum KvrMode : int32_t {
 
 // Task -> (layer, item, chunk range [q0, q1) of the item). Chunks are units of
 // the prefill rows: with replicated decode heads each is stored to every copy.
+// W = 2 (threads move pairs of adjacent units; rows hold an even number of
+// units): the slices split the item's pairs, so q0 and q1 are even.
+template <int W = 1>
 KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int32_t *layer,
                      KvrItem *item, uint32_t *q0, uint32_t *q1) {
     const uint32_t lt = a.div_tasks_per_layer.div(task);
@@ -155,8 +158,13 @@ KVR_HD void kvr_task(const KvrArgs &a, uint32_t task, const KvrItem *items, int3
     const uint64_t total = (uint64_t)it.ntok * a.g.C * a.g.H * a.g.row_chunks;
     *layer = a.layer0 + (int32_t)lt;
     *item = it;
-    *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);
-    *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
+    if (W == 1) {
+        *q0 = (uint32_t)(total * slice / (uint32_t)a.slices);
+        *q1 = (uint32_t)(total * (slice + 1) / (uint32_t)a.slices);
+    } else {
+        *q0 = 2u * (uint32_t)((total / 2) * slice / (uint32_t)a.slices);
+        *q1 = 2u * (uint32_t)((total / 2) * (slice + 1) / (uint32_t)a.slices);
+    }
 }
 
 // Row r of an item -> address of its prefill row, address of its decode row,

@@ -424,20 +424,41 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     }
 
     // units of the prefill rows (each stored to all dcopies decode copies)
-    const int64_t avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
-    hp->avg_chunks = avg_chunks;
+    hp->avg_chunks = n_items ? tokens * C * H * row_units / n_items : 0;
     hp->sm_count = sm_count;
-    hp->layer_resident = layer_resident;
-    hp->layer_resident_pf = layer_resident_pf;
-    hp->slices_layer = choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident);
+
+    // Pairs of adjacent units per access (one 32-byte load or store where a unit
+    // has 16 bytes): no replicated heads, an even number of units per row, and
+    // every row of both sides 32-byte aligned (view bases, and the strides of
+    // dimensions with more than one position).
+    auto aligned32 = [](const std::vector<uint64_t> &bases) {
+        for (uint64_t b : bases)
+            if (b % 32 != 0) return false;
+        return true;
+    };
+    hp->pairs = !kvr_replicated(g) && row_units % 2 == 0 && aligned32(hp->src_base) &&
+                aligned32(hp->dst_base) && (Np <= 1 || g.s_block_stride % 32 == 0) &&
+                (Bp <= 1 || g.s_token_stride % 32 == 0) &&
+                (Hp <= 1 || g.s_head_stride % 32 == 0) &&
+                (Nd <= 1 || g.d_block_stride % 32 == 0) &&
+                (Bd <= 1 || g.d_token_stride % 32 == 0) &&
+                (Hd <= 1 || g.d_head_stride % 32 == 0);
+    kvr_shape_launches(*hp, layer_resident, layer_resident_pf);
+    return KVR_OK;
+}
+
+void kvr_shape_launches(KvrHostPlan &hp, int layer_resident, int layer_resident_pf) {
+    const int64_t n_items = (int64_t)hp.items.size();
+    hp.layer_resident = layer_resident;
+    hp.layer_resident_pf = layer_resident_pf;
+    hp.slices_layer = choose_layer_slices(n_items, hp.avg_chunks, hp.sm_count, layer_resident);
     // a layer whose items fit in one wave of the prefetching instance: its grid,
     // sized to fill that wave, stays within it (choose_layer_slices)
-    hp->slices_layer_pf =
-        layer_resident_pf > 0 && n_items < (int64_t)std::max(sm_count, 1) * layer_resident_pf
-            ? choose_layer_slices(n_items, avg_chunks, sm_count, layer_resident_pf)
+    hp.slices_layer_pf =
+        layer_resident_pf > 0 && n_items < (int64_t)std::max(hp.sm_count, 1) * layer_resident_pf
+            ? choose_layer_slices(n_items, hp.avg_chunks, hp.sm_count, layer_resident_pf)
             : 0;
-    hp->slices_all = kvr_range_slices(*hp, L, 0);
-    return KVR_OK;
+    hp.slices_all = kvr_range_slices(hp, hp.num_layers, 0);
 }
 
 void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, bool no_wait,

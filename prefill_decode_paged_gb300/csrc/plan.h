@@ -77,7 +77,17 @@ struct KvrHostPlan {
     int32_t sm_count = 0;              // SMs of the device the plan was built for
     int32_t layer_resident = 0;        // CTAs of the per-layer kernel an SM holds (0: unknown)
     int32_t layer_resident_pf = 0;     // the same for its prefetching instance
+    bool pairs = false;                // rows allow pairs of adjacent units per access
+                                       // (32-byte accesses): see kvr_build_host_plan
 };
+
+// Whether a launch of mode `mode` (KvrMode) of a plan moves pairs of units: every
+// instance where the plan's rows allow it, except the bit copy's prefetching
+// per-layer one (its loads mostly hit L2, and single units measured 0.7 %
+// faster there on the 70B workload).
+inline bool kvr_launch_pairs(bool plan_pairs, int32_t conv, int32_t mode) {
+    return plan_pairs && !(conv == KVR_CONV_NONE && mode == KVR_MODE_LAYER_PREFETCH);
+}
 
 // Slices per item of a launch over `count` (>= 2) layers, shaped like a
 // whole-prompt launch (count == num_layers gives slices_all). `stream_sms`:
@@ -116,6 +126,12 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
                                const kvr_layout *dst_layout, const kvr_convert *cv,
                                int sm_count, int layer_resident, int layer_resident_pf,
                                KvrHostPlan *hp, int64_t *bytes_read, int64_t *bytes_written);
+
+// Per-layer and whole-prompt grid shapes of `hp` for per-layer kernel instances
+// that hold `layer_resident` (and, prefetching, `layer_resident_pf`) CTAs per
+// SM (kvr_build_host_plan calls it; a plan may reshape with the occupancy of
+// the instances it will run).
+void kvr_shape_launches(KvrHostPlan &hp, int layer_resident, int layer_resident_pf);
 
 // Kernel arguments of one launch starting at layer `layer0`.
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items,

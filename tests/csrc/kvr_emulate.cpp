@@ -85,6 +85,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                               : per_layer                     ? KVR_UNROLL_LAYER_QUANT
                                                               : KVR_UNROLL / 2)
                            : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL / 2);
+    const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
@@ -100,8 +101,11 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
         int32_t l;
         KvrItem it;
         uint32_t q0, q1;
-        kvr_task(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
-        if (q0 > q1 || l < layer0 || l >= layer0 + layers) {
+        if (pairs)
+            kvr_task<2>(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
+        else
+            kvr_task<1>(a, (uint32_t)task, a.items, &l, &it, &q0, &q1);
+        if (q0 > q1 || l < layer0 || l >= layer0 + layers || (pairs && (q0 | q1) % 2 != 0)) {
             ++bad;
             continue;
         }
@@ -129,6 +133,38 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                 }
             const uint32_t qa = q0 > w0 * rc ? q0 : w0 * rc;
             const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
+            if (pairs) {
+                // pairs of adjacent units (q, q + 1), U / 2 in flight, one 32-byte
+                // access each: both units in one row, both addresses 32-byte aligned
+                const uint32_t up = U > 1 ? U / 2 : 1, pa = qa / 2, pb = qb / 2;
+                if (rep || qa % 2 != 0 || qb % 2 != 0) ++bad;
+                for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
+                    for (uint32_t base = pa + tid; base < pb; base += up * KVR_THREADS)
+                        for (uint32_t k = 0; k < up; ++k) {
+                            const uint32_t pq = base + k * KVR_THREADS;
+                            if (pq >= pb) continue;
+                            const uint32_t q = 2 * pq;
+                            const uint32_t r = a.g.div_rc.div(q);
+                            const uint32_t u = q - r * rc;
+                            visited += 2;
+                            if (r < w0 || r >= w1 || a.g.div_rc.div(q + 1) != r ||
+                                rows_src[r - w0] == UINT64_MAX) {
+                                ++bad;
+                                continue;
+                            }
+                            const uint64_t from = rows_src[r - w0] + (uint64_t)u * su;
+                            const uint64_t to = rows_dst[r - w0] + (uint64_t)u * du;
+                            if (from % 32 != 0 || to % 32 != 0 ||
+                                (u + 2) * su > (uint32_t)a.g.src_row_bytes ||
+                                (u + 2) * du > (uint32_t)a.g.dst_row_bytes) {
+                                ++bad;
+                                continue;
+                            }
+                            if (copy)
+                                memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from, 32);
+                        }
+                continue;
+            }
             for (uint32_t tid = 0; tid < KVR_THREADS; ++tid) {
                 for (uint32_t base = qa + tid; base < qb; base += U * KVR_THREADS) {
                     for (uint32_t k = 0; k < U; ++k) {
@@ -243,6 +279,16 @@ int64_t emu_relayout_range(const kvr_desc *d, int sm_count, int32_t first, int32
                 pool_ranges((const void *const *)d->dst_pools, d->dst_tp, d, d->dst_num_blocks,
                             d->dst_block_size, d->elem_bytes),
                 sm_count, first, count, copy, chunks);
+}
+
+// Whether the plan's rows allow pairs of units per access (KvrHostPlan::pairs):
+// 1 or 0, or a negative kvr_status.
+int32_t emu_plan_pairs(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl,
+                       const kvr_convert *cv) {
+    KvrHostPlan hp;
+    kvr_status st = kvr_build_host_plan(d, sl, dl, cv, 152, 4, 4, &hp, nullptr, nullptr);
+    if (st != KVR_OK) return st;
+    return hp.pairs ? 1 : 0;
 }
 
 // Work-list facts of a plan: [n_items, slices_all, slices_layer, grid_all, grid_layer, tile].

@@ -250,18 +250,19 @@ def _emu_run(emu, w, src, dst, layer=-1, sms=SMS):
     return n.value
 
 
-def _aligned(shape, dtype):
-    """Host array whose data starts on a 16-byte boundary (as device pools do)."""
+def _aligned(shape, dtype, align=256, skew=0):
+    """Host array whose data starts `skew` bytes past an `align`-byte boundary (the
+    CUDA allocator's pools start on 256-byte boundaries)."""
     nbytes = int(np.prod(shape)) * np.dtype(dtype).itemsize
-    raw = np.empty(nbytes + 16, dtype=np.uint8)
-    off = (-raw.ctypes.data) % 16
+    raw = np.empty(nbytes + align + skew, dtype=np.uint8)
+    off = (-raw.ctypes.data) % align + skew
     return raw[off:off + nbytes].view(dtype).reshape(shape)
 
 
-def _pools(w, filled):
+def _pools(w, filled, skew=0):
     out = []
     for a in filled:
-        b = _aligned(a.shape, a.dtype)
+        b = _aligned(a.shape, a.dtype, skew=skew)
         b[...] = a
         out.append(b)
     return out
@@ -532,7 +533,9 @@ def test_fuzzed_geometries_on_the_emulated_kernel(emu, seed):
     on the CPU with bounds checks, equals the oracle."""
     from fuzz_cases import random_workload
     w = random_workload(seed)
-    src = _pools(w, w.src_pools_numpy())
+    # every fourth seed: prefill pools 16 bytes past a 32-byte boundary (rows
+    # taken one unit per access instead of in pairs)
+    src = _pools(w, w.src_pools_numpy(), skew=16 if seed % 4 == 3 else 0)
     ref = w.dst_pools_numpy()
     oracle.relayout(src, ref, **w.geometry())
     sms = [1, 7, SMS][seed % 3]
@@ -553,6 +556,58 @@ def test_fuzzed_geometries_on_the_emulated_kernel(emu, seed):
         assert bad == 0
         for a, b in zip(ref, rng_):
             np.testing.assert_array_equal(a, b)
+
+
+def _pairs(emu, w, src, dst, convert=None):
+    d = kr._Desc(src, dst, **w.geometry())
+    cv = kr._Convert(**convert) if convert else None
+    return emu.emu_plan_pairs(ctypes.byref(d.desc), None, None,
+                              ctypes.byref(cv.conv) if cv else None)
+
+
+def test_pairs_of_units_only_where_every_row_allows_them(emu):
+    """Threads move pairs of adjacent units (32-byte accesses) exactly when no head is
+    replicated, rows hold an even number of units, and every row of both sides
+    starts on a 32-byte boundary."""
+    emu.emu_plan_pairs.restype = ctypes.c_int32
+    emu.emu_plan_pairs.argtypes = [ctypes.c_void_p] * 4
+
+    def case(**kw):
+        base = dict(num_layers=2, num_components=2, kv_heads=8, head_dim=128, elem_bytes=2,
+                    src_tp=4, dst_tp=8, src_block=16, dst_block=32, seq_lens=[40, 7])
+        base.update(kw)
+        return wl.custom("pairs", 0, **base)
+
+    w = case()
+    s, d = fake_pools(w)
+    assert _pairs(emu, w, s, d) == 1                              # 16 units a row
+    assert _pairs(emu, w, s[:1] + [s[1] + 16] + s[2:], d) == 0    # one shard 16 B off
+    assert _pairs(emu, w, s, d[:-1] + [d[-1] + 32]) == 1          # 32 B off is fine
+    w = case(head_dim=8)                                          # one unit a row
+    assert _pairs(emu, w, *fake_pools(w)) == 0
+    w = case(head_dim=24)                                         # three units, odd
+    assert _pairs(emu, w, *fake_pools(w)) == 0
+    w = case(head_dim=16, elem_bytes=1)                           # 16 B rows: one unit
+    assert _pairs(emu, w, *fake_pools(w)) == 0
+    w = case(kv_heads=2, src_tp=4)                                # replicated heads
+    assert _pairs(emu, w, *fake_pools(w)) == 0
+    # conversions: a unit is 16 elements (32 BF16 bytes, 16 FP8 bytes)
+    w = case(head_dim=32)
+    q = dict(src_dtype=1, dst_dtype=2, scales=np.ones(2 * 2, np.float32))
+    assert _pairs(emu, w, *fake_pools(w), convert=q) == 1
+    w = case(head_dim=16)
+    assert _pairs(emu, w, *fake_pools(w), convert=q) == 0
+    # rows of 32 bytes (two units) 48 bytes apart on the decode side: not aligned
+    w = case(head_dim=16)
+    s, d = fake_pools(w)
+    L, C, N, B, Hl, D = w.dst_shape()
+    for pad, want in ((24, 0), (32, 1)):
+        bufs = [_aligned((L, C, N, B, Hl, pad), np.uint16) for _ in range(w.dst_tp)]
+        lay = kr._Layout(**kr.layout_of_views(
+            [[[b[l, c, ..., :D] for c in range(C)] for l in range(L)] for b in bufs]))
+        dd = kr._Desc(s, d, **w.geometry())
+        assert emu.emu_plan_pairs(ctypes.byref(dd.desc), None, ctypes.byref(lay.layout),
+                                  None) == want, pad
 
 
 ABI_CLIENT_SRC = os.path.join(ROOT, "tests", "csrc", "abi_client.c")
