@@ -123,3 +123,38 @@ def test_bench_bytes_equal_the_librarys_count(name, convert):
                     scales=np.ones(w.num_layers * w.num_components, np.float32))
     r, wr = kr.desc_bytes(s, d, convert=conv, **w.geometry())
     assert r + wr == bench.algorithmic_bytes(w, conv)
+
+
+def test_conversion_targets_run_in_a_fresh_single_gpu_process(monkeypatch):
+    """The targets' conversion runs are bench.py children on this rank's GPU alone:
+    no rank variables, the rank's device as the only visible one, and their whole,
+    per-layer and timed-window figures read back from the child's line."""
+    sys.path.insert(0, ROOT)
+    import bench
+    seen = {}
+
+    def fake_run(cmd, env, capture_output, text, timeout):
+        seen.update(cmd=cmd, env=env)
+        line = {"value": 7000.0, "per_layer": {"cuda_graph": {"gbs": 5600.0,
+                                                              "us_per_launch": 4.5}},
+                "run": {"timed_windows": [[1.0, 2.0], [3.0, 4.0]]}}
+        return subprocess.CompletedProcess(cmd, 0, stdout="noise\n" + json.dumps(line) + "\n",
+                                           stderr="")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+    for k, v in dict(RANK="1", LOCAL_RANK="1", WORLD_SIZE="2", MASTER_ADDR="127.0.0.1",
+                     MASTER_PORT="29500", CUDA_VISIBLE_DEVICES="4,5").items():
+        monkeypatch.setenv(k, v)
+    whole, layer, us, windows = bench.conversion_child("bf16_to_fp8", 200, 20, 1)
+    assert (whole, layer, us, windows) == (7000.0, 5600.0, 4.5, [[1.0, 2.0], [3.0, 4.0]])
+    env, cmd = seen["env"], seen["cmd"]
+    assert not {"RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT"} & set(env)
+    assert env["CUDA_VISIBLE_DEVICES"] == "5"
+    assert cmd[cmd.index("--convert") + 1] == "bf16_to_fp8"
+    assert cmd[cmd.index("--steps") + 1] == "200" and cmd[cmd.index("--warmup") + 1] == "20"
+    assert "--report-windows" in cmd and cmd[cmd.index("--modes") + 1] == "all,graph"
+    # a failed child ends the run loudly
+    monkeypatch.setattr(bench.subprocess, "run", lambda cmd, **kw: subprocess.CompletedProcess(
+        cmd, 1, stdout="", stderr="boom"))
+    with pytest.raises(SystemExit, match="boom"):
+        bench.conversion_child("fp8_to_bf16", 200, 20, 0)
