@@ -280,3 +280,51 @@ def test_fuzzed_pack_then_unpack_equals_the_direct_relayout(seed):
             torch.cuda.synchronize()
         for a, t in zip(ref, dst):
             assert np.array_equal(t.cpu().numpy().view(dt), a), mode
+
+
+@pytest.mark.parametrize("skew", [0, 16])
+@pytest.mark.parametrize("direction", ["copy", "quant", "dequant"])
+@pytest.mark.parametrize("mode", ["all", "layer"])
+def test_pairs_and_single_units_match_the_oracle(skew, direction, mode):
+    """Prefill pools on a 32-byte boundary (threads move pairs of adjacent units) and
+    16 bytes past one (single units): both equal the oracle, in every conversion."""
+    import torch
+    rng = np.random.default_rng(11)
+    w = _w(5, elem_bytes=1 if direction == "dequant" else 2)
+    shape = w.src_shape()
+    if direction == "dequant":
+        src_np = [rng.integers(0, 256, shape, dtype=np.uint8) for _ in range(w.src_tp)]
+    else:
+        src_np = [rng.integers(0, 1 << 16, shape, dtype=np.uint16) for _ in range(w.src_tp)]
+    conv = {"copy": None,
+            "quant": dict(src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3),
+            "dequant": dict(src_dtype=DTYPE_FP8_E4M3, dst_dtype=DTYPE_BF16)}[direction]
+    dt, fill = (np.uint8, 0xFF) if direction == "quant" else (np.uint16, 0xFFFF)
+    scales = rng.uniform(0.01, 2.0, w.num_layers * 2 * 8).astype(np.float32)
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block, 2,
+                               w.head_dim)
+    ref_bufs, ref_views, _, _ = decode_family(w, "standard", dt, fill)
+    extra = dict(per_head=1, scales=scales, **conv) if conv else {}
+    oracle.relayout_general(sv, ref_views, **extra, **_tables(w))
+
+    def skewed(a):
+        raw = torch.empty(a.nbytes + 256, dtype=torch.uint8, device="cuda")
+        t = raw[skew:skew + a.nbytes]
+        t.copy_(torch.from_numpy(a.reshape(-1).view(np.uint8)).cuda())
+        return t.view(torch.int16 if a.dtype == np.uint16 else torch.uint8).view(shape)
+
+    src_t = [skewed(a) for a in src_np]
+    assert all(t.data_ptr() % 32 == skew for t in src_t)
+    views = [[[t[l, c] for c in range(2)] for l in range(w.num_layers)] for t in src_t]
+    _, _, tbufs, _ = decode_family(w, "standard", dt, fill)
+    cv = dict(per_head=True, scales=scales, **conv) if conv else None
+    with RelayoutPlan(None, tbufs, src_layout=layout_of_views(views), convert=cv,
+                      **w.geometry()) as plan:
+        if mode == "all":
+            plan.run_all()
+        else:
+            for l in range(w.num_layers):
+                plan.run_layer(l)
+        torch.cuda.synchronize()
+    for ref, got in zip(ref_bufs, tbufs):
+        assert np.array_equal(got.cpu().numpy().view(dt), ref)
