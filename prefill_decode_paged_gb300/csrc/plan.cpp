@@ -469,16 +469,25 @@ void kvr_range_launch(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, 
     const int64_t slots = (int64_t)std::max(sms, 1) *
                           (hp.layer_resident > 0 ? hp.layer_resident : KVR_LAYER_CTAS_PER_SM);
     const int64_t slots_pf = (int64_t)std::max(sms, 1) * hp.layer_resident_pf;
-    if (!no_wait && tasks < slots_pf) {
-        *slices = count == 1 && !limited
-                      ? hp.slices_layer_pf
-                      : choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident_pf);
+    // A range of several layers takes the prefetching instance only if its grid
+    // fills at least 3/4 of that wave; below that it runs the whole-prompt grid
+    // (70B, 3 layers = 384 one-item CTAs on 608 slots: bit copy 5526 -> 5794,
+    // BF16 -> FP8 4840 -> 5216, FP8 -> BF16 4565 -> 5335 GB/s; 2 and 4 layers,
+    // 512 CTAs, keep it).
+    const bool pf = !no_wait && tasks < slots_pf;
+    const int32_t slices_pf =
+        !pf ? 0
+        : count == 1 && !limited
+            ? hp.slices_layer_pf
+            : choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident_pf);
+    if (pf && (count == 1 || 4 * tasks * slices_pf >= 3 * slots_pf)) {
+        *slices = slices_pf;
         *mode = KVR_MODE_LAYER_PREFETCH;
     } else if (count == 1) {
         *slices = limited ? choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident)
                           : hp.slices_layer;
         *mode = KVR_MODE_LAYER;
-    } else if (tasks < slots) {
+    } else if (!pf && tasks < slots) {
         *slices = choose_layer_slices(tasks, hp.avg_chunks, sms, hp.layer_resident);
         *mode = KVR_MODE_LAYER;
     } else {

@@ -380,9 +380,12 @@ def test_launch_modes_and_grids_per_stream(emu):
     assert mode == PREFETCH and grid <= SMS * 4
     # no residency known for the prefetching instance: never prefetch
     assert shape("llama70b", 1, res_pf=0)[1] == LAYER
-    # ranges: two 70B layers still fit one wave, eight do not
-    sl, mode, grid, _ = shape("llama70b", 2)
-    assert mode == PREFETCH and grid <= SMS * 4
+    # ranges: two and four 70B layers fill most of one wave, eight do not fit it;
+    # three (384 one-item CTAs on 608 slots) would leave too much of it idle
+    for count in (2, 4):
+        sl, mode, grid, _ = shape("llama70b", count)
+        assert mode == PREFETCH and 3 * SMS < grid <= SMS * 4, count
+    assert shape("llama70b", 3)[1] == WHOLE
     assert shape("llama70b", 8)[1] == WHOLE
     # Qwen 32K layers hold 2048 items: several waves, no prefetch
     sl, mode, grid, items = shape("qwen32k", 1)
