@@ -21,6 +21,11 @@
 #ifndef KVR_UNROLL_LAYER_CONVERT
 #define KVR_UNROLL_LAYER_CONVERT 2  // per-layer FP8 -> BF16 launches (two stores per unit)
 #endif
+#ifndef KVR_UNROLL_LAYER_CONVERT_PAIRS
+#define KVR_UNROLL_LAYER_CONVERT_PAIRS 4  // the same, pairs of units per access (2 pairs;
+                                          // 70B ordered 5539 -> 5669, no wait 5746 -> 6198,
+                                          // 8B / Qwen 32K / MLA layers +6 / +6 / +3 %)
+#endif
 #ifndef KVR_UNROLL_LAYER_QUANT
 #define KVR_UNROLL_LAYER_QUANT 2    // per-layer BF16 -> FP8 launches: units (two loads each)
 #endif

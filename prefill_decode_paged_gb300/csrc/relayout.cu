@@ -453,7 +453,9 @@ KvrKernel pick_instance(int32_t conv) {
                                                                       : KVR_UNROLL / 2,
                                        KVR_CONV_BF16_TO_E4M3, MODE, REP, W>;
         case KVR_CONV_E4M3_TO_BF16:
-            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL / 2,
+            return kvr_relayout_kernel<!LAYER  ? KVR_UNROLL / 2
+                                       : W == 2 ? KVR_UNROLL_LAYER_CONVERT_PAIRS
+                                                : KVR_UNROLL_LAYER_CONVERT,
                                        KVR_CONV_E4M3_TO_BF16, MODE, REP, W>;
         default:
             return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER : KVR_UNROLL, KVR_CONV_NONE, MODE,

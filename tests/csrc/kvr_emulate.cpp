@@ -78,14 +78,16 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     // units in flight per thread, as the kernel instance the launch picks
+    const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode);
     const uint32_t U = hp.g.conv == KVR_CONV_NONE
                            ? (per_layer ? KVR_UNROLL_LAYER : KVR_UNROLL)
                        : hp.g.conv == KVR_CONV_BF16_TO_E4M3
                            ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
                               : per_layer                     ? KVR_UNROLL_LAYER_QUANT
                                                               : KVR_UNROLL / 2)
-                           : (per_layer ? KVR_UNROLL_LAYER_CONVERT : KVR_UNROLL / 2);
-    const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode);
+                       : !per_layer ? KVR_UNROLL / 2
+                       : pairs      ? KVR_UNROLL_LAYER_CONVERT_PAIRS
+                                    : KVR_UNROLL_LAYER_CONVERT;
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
