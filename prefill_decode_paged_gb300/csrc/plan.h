@@ -29,6 +29,11 @@
 #ifndef KVR_UNROLL_LAYER_QUANT
 #define KVR_UNROLL_LAYER_QUANT 2    // per-layer BF16 -> FP8 launches: units (two loads each)
 #endif
+#ifndef KVR_UNROLL_LAYER_QUANT_PAIRS
+#define KVR_UNROLL_LAYER_QUANT_PAIRS 4  // the same, pairs of units per access (2 pairs; 70B
+                                        // with KVR_LAUNCH_NO_WAIT 5828 -> 6132, 8B layers
+                                        // 6279 -> 6470, MLA 6618 -> 6726, Qwen 32K 6795 -> 6775)
+#endif
 #ifndef KVR_UNROLL_LAYER_QUANT_PF
 #define KVR_UNROLL_LAYER_QUANT_PF 4 // the same, ordered one-wave launches (L2 prefetch)
 #endif

@@ -449,8 +449,9 @@ KvrKernel pick_instance(int32_t conv) {
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
             return kvr_relayout_kernel<MODE == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
-                                       : LAYER                        ? KVR_UNROLL_LAYER_QUANT
-                                                                      : KVR_UNROLL / 2,
+                                       : !LAYER                       ? KVR_UNROLL / 2
+                                       : W == 2                       ? KVR_UNROLL_LAYER_QUANT_PAIRS
+                                                                      : KVR_UNROLL_LAYER_QUANT,
                                        KVR_CONV_BF16_TO_E4M3, MODE, REP, W>;
         case KVR_CONV_E4M3_TO_BF16:
             return kvr_relayout_kernel<!LAYER  ? KVR_UNROLL / 2

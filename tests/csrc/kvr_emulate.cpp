@@ -83,8 +83,9 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                            ? (per_layer ? KVR_UNROLL_LAYER : KVR_UNROLL)
                        : hp.g.conv == KVR_CONV_BF16_TO_E4M3
                            ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
-                              : per_layer                     ? KVR_UNROLL_LAYER_QUANT
-                                                              : KVR_UNROLL / 2)
+                              : !per_layer                    ? KVR_UNROLL / 2
+                              : pairs                         ? KVR_UNROLL_LAYER_QUANT_PAIRS
+                                                              : KVR_UNROLL_LAYER_QUANT)
                        : !per_layer ? KVR_UNROLL / 2
                        : pairs      ? KVR_UNROLL_LAYER_CONVERT_PAIRS
                                     : KVR_UNROLL_LAYER_CONVERT;
