@@ -40,6 +40,30 @@
 #ifndef KVR_ROW_WINDOW
 #define KVR_ROW_WINDOW 1024      // rows whose pointers a CTA keeps in shared memory at once
 #endif
+
+// Units in flight per thread of the kernel instance for a conversion (KvrConv),
+// a launch mode (KvrMode) and the access width (pairs: two units per access);
+// a quantizing unit takes two loads, a dequantizing one two stores. The kernel's
+// instances and the CPU emulation of its launches both read it. Measured on
+// 70B layers (one GB300, GB/s), one unit per access: the prefetching quantizer
+// with 4 units 5239, with 2 5075; the per-layer dequantizer with 2 units 4307
+// (ordered) / 5620 (no wait), with 4 4163 / 5245, with 1 3755 / 4891, with 8
+// (80 registers) 3805 / 4702, and 2 units also won on the multi-wave MLA, Qwen
+// 32K and 8B layers; with pairs, 4 units (2 pairs) won in every per-layer
+// instance (see the _PAIRS values above).
+constexpr int kvr_units(int32_t conv, int32_t mode, bool pairs) {
+    return conv == KVR_CONV_BF16_TO_E4M3
+               ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
+                  : mode == KVR_MODE_WHOLE        ? KVR_UNROLL / 2
+                  : pairs                         ? KVR_UNROLL_LAYER_QUANT_PAIRS
+                                                  : KVR_UNROLL_LAYER_QUANT)
+           : conv == KVR_CONV_E4M3_TO_BF16
+               ? (mode == KVR_MODE_WHOLE ? KVR_UNROLL / 2
+                  : pairs                ? KVR_UNROLL_LAYER_CONVERT_PAIRS
+                                         : KVR_UNROLL_LAYER_CONVERT)
+               : (mode == KVR_MODE_WHOLE ? KVR_UNROLL : KVR_UNROLL_LAYER);
+}
+
 // A whole-prompt launch aims at this many CTAs per SM; items are sliced until
 // it does, but no slice gets fewer than KVR_MIN_SLICE_CHUNKS units. Per-layer
 // launches are shaped by the kernel's occupancy (see choose_layer_slices);

@@ -434,33 +434,20 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
 
 using KvrKernel = void (*)(KvrArgs);
 
-// Kernel instance for a conversion, launch mode and head replication (units
-// in flight per thread; a quantizing unit takes two loads, a dequantizing one
-// two stores): the bit copy 8; quantizing 4 whole-prompt and in ordered
-// one-wave per-layer launches (the prefetching instance), 2 in other per-layer
-// launches; dequantizing 4 whole-prompt, 2 per layer. Measured on 70B layers
-// (one GB300, GB/s): the prefetching quantizer with 4 units 5239, with 2 5075;
-// the per-layer dequantizer with 2 units 4307 (ordered) / 5620 (no wait), with
-// 4 4163 / 5245, with 1 3755 / 4891, with 8 (80 registers) 3805 / 4702; 2 units
-// also won on the multi-wave MLA, Qwen 32K and 8B layers.
+// Kernel instance for a conversion, launch mode, head replication and access
+// width (units in flight per thread: kvr_units).
 template <int MODE, bool REP, int W>
 KvrKernel pick_instance(int32_t conv) {
-    constexpr bool LAYER = MODE != KVR_MODE_WHOLE;
     switch (conv) {
         case KVR_CONV_BF16_TO_E4M3:
-            return kvr_relayout_kernel<MODE == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
-                                       : !LAYER                       ? KVR_UNROLL / 2
-                                       : W == 2                       ? KVR_UNROLL_LAYER_QUANT_PAIRS
-                                                                      : KVR_UNROLL_LAYER_QUANT,
+            return kvr_relayout_kernel<kvr_units(KVR_CONV_BF16_TO_E4M3, MODE, W == 2),
                                        KVR_CONV_BF16_TO_E4M3, MODE, REP, W>;
         case KVR_CONV_E4M3_TO_BF16:
-            return kvr_relayout_kernel<!LAYER  ? KVR_UNROLL / 2
-                                       : W == 2 ? KVR_UNROLL_LAYER_CONVERT_PAIRS
-                                                : KVR_UNROLL_LAYER_CONVERT,
+            return kvr_relayout_kernel<kvr_units(KVR_CONV_E4M3_TO_BF16, MODE, W == 2),
                                        KVR_CONV_E4M3_TO_BF16, MODE, REP, W>;
         default:
-            return kvr_relayout_kernel<LAYER ? KVR_UNROLL_LAYER : KVR_UNROLL, KVR_CONV_NONE, MODE,
-                                       REP, W>;
+            return kvr_relayout_kernel<kvr_units(KVR_CONV_NONE, MODE, W == 2), KVR_CONV_NONE,
+                                       MODE, REP, W>;
     }
 }
 

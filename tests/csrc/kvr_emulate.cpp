@@ -70,7 +70,6 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     int32_t slices = hp.slices_all;
     int32_t mode = KVR_MODE_WHOLE;               // the kernel instance (an ordered launch)
     if (!all) kvr_range_launch(hp, count, 0, false, &slices, &mode);
-    const bool per_layer = mode != KVR_MODE_WHOLE;
     const int32_t layer0 = all ? 0 : first, layers = all ? hp.num_layers : count;
     const KvrArgs a = kvr_launch_args(hp, hp.items.data(), hp.sbt.data(), hp.dbt.data(),
                                       hp.factors.data(), hp.src_base.data(), hp.dst_base.data(),
@@ -79,16 +78,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     // units in flight per thread, as the kernel instance the launch picks
     const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode);
-    const uint32_t U = hp.g.conv == KVR_CONV_NONE
-                           ? (per_layer ? KVR_UNROLL_LAYER : KVR_UNROLL)
-                       : hp.g.conv == KVR_CONV_BF16_TO_E4M3
-                           ? (mode == KVR_MODE_LAYER_PREFETCH ? KVR_UNROLL_LAYER_QUANT_PF
-                              : !per_layer                    ? KVR_UNROLL / 2
-                              : pairs                         ? KVR_UNROLL_LAYER_QUANT_PAIRS
-                                                              : KVR_UNROLL_LAYER_QUANT)
-                       : !per_layer ? KVR_UNROLL / 2
-                       : pairs      ? KVR_UNROLL_LAYER_CONVERT_PAIRS
-                                    : KVR_UNROLL_LAYER_CONVERT;
+    const uint32_t U = (uint32_t)kvr_units(hp.g.conv, mode, pairs);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
     static uint64_t rows_src[KVR_ROW_WINDOW], rows_dst[KVR_ROW_WINDOW];
