@@ -169,7 +169,13 @@ kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
  * ([N][C][B][H][D]); head-major blocks ([N][H][B][D]); a contiguous
  * [tokens][heads][dim] staging buffer seen as blocks of one token.
  * Requirements: every base 16-byte aligned and non-NULL; strides >= 0 and
- * multiples of 16 (a stride whose dimension has extent 1 is ignored). On the
+ * multiples of 16 (a stride whose dimension has extent 1 is ignored).
+ * Performance (not a requirement): when every base and stride of both sides is
+ * a multiple of 32 bytes, the row moves an even number of 16-byte units (16
+ * elements each when converting) and no head is replicated, the kernel moves
+ * 32 bytes per access, which is the faster path; pools from the CUDA
+ * allocator (256-byte aligned) in the standard layout take it whenever the row
+ * allows. On the
  * decode side the views must not alias: sorted by stride, each dimension
  * (of extent > 1) must step over the whole extent of the smaller ones, the
  * smallest over one head row; no two decode views may share a byte (views
