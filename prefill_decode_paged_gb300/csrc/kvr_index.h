@@ -119,6 +119,9 @@ struct KvrArgs {
                                         // before them (the caller's call)
     uint32_t tasks_per_layer;           // n_items * slices
     KvrDiv div_tasks_per_layer, div_slices;
+    uint32_t prefetch_ctas;             // bit copy, prefetching instance, no replicated
+                                        // heads: CTAs below this index prefetch their rows
+                                        // (all: 0xFFFFFFFF)
 #ifdef KVR_DEVICE_CHECKS
     // Checked builds only: [lo, hi) byte ranges the prefill rows (the first
     // n_src_regions pairs) and decode rows (the next n_dst_regions) must lie in;

@@ -519,6 +519,14 @@ int32_t kvr_range_slices(const KvrHostPlan &hp, int32_t count, int32_t stream_sm
     return s;
 }
 
+uint32_t kvr_prefetch_ctas(const KvrHostPlan &hp, int32_t count, int32_t stream_sms, int32_t mode,
+                           int32_t slices) {
+    const bool limited = stream_sms > 0 && stream_sms < hp.sm_count;
+    if (mode != KVR_MODE_LAYER_PREFETCH || count != 1 || limited) return 0xFFFFFFFFu;
+    const uint64_t grid = (uint64_t)hp.items.size() * (uint64_t)slices;
+    return (uint32_t)(grid * KVR_PREFETCH_CTAS_EIGHTHS / 8);
+}
+
 KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const int32_t *dev_sbt,
                         const int32_t *dev_dbt, const float *dev_factors,
                         const uint64_t *dev_src_base, const uint64_t *dev_dst_base,
@@ -537,6 +545,7 @@ KvrArgs kvr_launch_args(const KvrHostPlan &hp, const KvrItem *dev_items, const i
     a.tasks_per_layer = (uint32_t)(hp.items.size() * (size_t)slices);
     a.div_tasks_per_layer = kvr_make_div(a.tasks_per_layer ? a.tasks_per_layer : 1);
     a.div_slices = kvr_make_div((uint32_t)slices);
+    a.prefetch_ctas = 0xFFFFFFFFu;
     return a;
 }
 

@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                 rows[r - w0] = make_ulonglong2(sa, da);
                 if (CONV != KVR_CONV_NONE) row_factor[r - w0] = a.factors[fidx];
             }
-            if (PF && CONV == KVR_CONV_NONE && !waited) {
+            if (PF && CONV == KVR_CONV_NONE && !waited && blockIdx.x < a.prefetch_ctas) {
                 // Before the grid-dependency wait, pull the prefill rows this
                 // thread just entered into L2, so the loads after the wait hit
                 // L2 instead of starting cold: the wait drains the previous
@@ -324,6 +324,11 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                 // previous grid: L2 is where writes from every SM meet, so rows
                 // a producer writes after this prefetch replace the prefetched
                 // lines there, and the loads after the wait see its writes.
+                // A single-layer launch on the whole device leaves it to its
+                // first CTAs (prefetch_ctas, kvr_prefetch_ctas): the later ones
+                // become resident only as the previous launch's CTAs exit,
+                // when issuing 256 bulk requests (~1 us) delays their copy more
+                // than the prefetch saves.
                 for (uint32_t r = w0 + threadIdx.x; r < w1; r += KVR_THREADS)
                     if (!KVR_SRC_DROPPED(rows[r - w0]))
                         prefetch_l2(rows[r - w0].x, (uint32_t)a.g.src_row_bytes);
@@ -472,21 +477,24 @@ KvrKernel pick_kernel(int32_t conv, int mode, bool rep, bool pairs) {
     }
 }
 
+// prefetch_ctas: KvrArgs::prefetch_ctas (kvr_prefetch_ctas).
 kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t slices,
-                  int32_t mode, void *stream, bool no_wait = false) {
+                  int32_t mode, void *stream, bool no_wait = false,
+                  uint32_t prefetch_ctas = 0xFFFFFFFFu) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVR_ERR_CUDA;
     if (dev != p->device) return KVR_ERR_INVALID_ARG;
     KvrArgs a = kvr_launch_args(p->host, p->dev_items, p->dev_sbt, p->dev_dbt, p->dev_factors,
                                 p->dev_src_base, p->dev_dst_base, layer0, slices);
     a.no_wait = no_wait ? 1 : 0;
+    a.prefetch_ctas = prefetch_ctas;
+    const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
 #ifdef KVR_DEVICE_CHECKS
     a.check_regions = p->dev_regions;
     a.n_src_regions = (int32_t)(p->host.src_regions.size() / 2);
     a.n_dst_regions = (int32_t)(p->host.dst_regions.size() / 2);
     a.check_error = p->dev_check_error;
 #endif
-    const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     if (grid == 0) return KVR_OK;
     // KVR_MODE_LAYER_PREFETCH (kvr_range_launch picks it): ordered per-layer
     // launches of one wave prefetch their first window's prefill rows into L2
@@ -776,8 +784,10 @@ extern "C" kvr_status kv_relayout_layers_ex(const kvr_plan *plan, int32_t first,
     int32_t slices = 1, mode = KVR_MODE_LAYER;
     // the stream's green context, if any, shapes the grid (a driver query that
     // measured no cost on back-to-back 70B layer launches)
-    kvr_range_launch(plan->host, count, kvr_stream_green_sms(stream), no_wait, &slices, &mode);
-    return launch(plan, first, count, slices, mode, stream, no_wait);
+    const int32_t green = kvr_stream_green_sms(stream);
+    kvr_range_launch(plan->host, count, green, no_wait, &slices, &mode);
+    return launch(plan, first, count, slices, mode, stream, no_wait,
+                  kvr_prefetch_ctas(plan->host, count, green, mode, slices));
 }
 
 extern "C" kvr_status kv_relayout_layers(const kvr_plan *plan, int32_t first, int32_t count,

@@ -340,6 +340,7 @@ extern "C" {
 
 // kvr_range_launch() for a plan built with the given residencies: out = [slices,
 // mode, grid (CTAs), items].
+// out: [slices, mode, grid, items per layer, CTAs that prefetch (kvr_prefetch_ctas)]
 int32_t emu_range_launch(const kvr_desc *d, int sm_count, int resident, int resident_pf,
                          int32_t count, int32_t stream_sms, int32_t no_wait, int64_t *out) {
     KvrHostPlan hp;
@@ -352,6 +353,7 @@ int32_t emu_range_launch(const kvr_desc *d, int sm_count, int resident, int resi
     out[1] = mode;
     out[2] = (int64_t)count * (int64_t)hp.items.size() * slices;
     out[3] = (int64_t)hp.items.size();
+    out[4] = kvr_prefetch_ctas(hp, count, stream_sms, mode, slices);
     return 0;
 }
 

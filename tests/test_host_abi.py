@@ -354,7 +354,8 @@ def test_launch_modes_and_grids_per_stream(emu):
     it with a grid inside that wave; no-wait launches never prefetch; a stream with
     fewer SMs gets a grid shaped for them; long ranges run the whole-prompt instance."""
     WHOLE, LAYER, PREFETCH = 0, 1, 2
-    out = (ctypes.c_int64 * 4)()
+    ALL = 0xFFFFFFFF
+    out = (ctypes.c_int64 * 5)()
 
     def shape(name, count, stream_sms=0, no_wait=False, res=4, res_pf=4):
         w = wl.get(name)
@@ -363,6 +364,10 @@ def test_launch_modes_and_grids_per_stream(emu):
         assert emu.emu_range_launch(ctypes.byref(desc.desc), SMS, res, res_pf, count,
                                     stream_sms, int(no_wait), out) == 0
         return out[0], out[1], out[2], out[3]
+
+    def prefetching(name, count, stream_sms=0, no_wait=False):
+        shape(name, count, stream_sms, no_wait)
+        return out[4]
 
     # 70B: 128 items per layer
     sl, mode, grid, items = shape("llama70b", 1)
@@ -387,6 +392,14 @@ def test_launch_modes_and_grids_per_stream(emu):
         assert mode == PREFETCH and 3 * SMS < grid <= SMS * 4, count
     assert shape("llama70b", 3)[1] == WHOLE
     assert shape("llama70b", 8)[1] == WHOLE
+    # which CTAs of an ordered launch prefetch: the first 5/8 of a single 70B
+    # layer on the whole device; every CTA on a green-context stream, in a range
+    # of layers and in a no-wait launch (whose instance does not prefetch)
+    assert prefetching("llama70b", 1) == 512 * 5 // 8
+    assert prefetching("llama70b", 1, stream_sms=96) == ALL
+    assert prefetching("llama70b", 1, stream_sms=SMS) == 512 * 5 // 8
+    assert prefetching("llama70b", 2) == ALL
+    assert prefetching("llama70b", 1, no_wait=True) == ALL
     # Qwen 32K layers hold 2048 items: several waves, no prefetch
     sl, mode, grid, items = shape("qwen32k", 1)
     assert items == 2048 and mode == LAYER and grid >= SMS * 4
