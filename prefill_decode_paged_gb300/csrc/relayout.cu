@@ -381,11 +381,11 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                             store_stream32(to[k], quant16(v[k][0], v[k][1], f[k]),
                                            quant16(v[k][2], v[k][3], f[k]));
                         } else {
-                            uint4 lo0, hi0, lo1, hi1;
-                            dequant16(v[k][0], f[k], &lo0, &hi0);
-                            dequant16(v[k][1], f[k], &lo1, &hi1);
-                            store_stream32(to[k], lo0, hi0);
-                            store_stream32(to[k] + 32, lo1, hi1);
+                            uint4 lo, hi;
+                            dequant16(v[k][0], f[k], &lo, &hi);
+                            store_stream32(to[k], lo, hi);
+                            dequant16(v[k][1], f[k], &lo, &hi);
+                            store_stream32(to[k] + 32, lo, hi);
                         }
                     }
                 }
