@@ -666,7 +666,7 @@ def targets_measure(timed, dev, stream, K, world, peak, windows, main_per_layer=
         ws, wd, conv = conversion_for(kind, w70)
         b = algorithmic_bytes(ws, conv)
         # fresh process (each rank its own GPU), then the slowest rank's time
-        whole_gbs, layer_gbs, us, child_windows = conversion_child(kind, K, W, dev.index)
+        whole_gbs, layer_gbs, _, child_windows = conversion_child(kind, K, W, dev.index)
         windows.extend(tuple(x) for x in child_windows)
         ms_whole = max_over_ranks(b * K / (whole_gbs * 1e9) * 1e3, world, dev)
         ms_layer = max_over_ranks(b * K / (layer_gbs * 1e9) * 1e3, world, dev)
