@@ -171,9 +171,9 @@ kvr_status kv_relayout_plan(const kvr_desc *desc, kvr_plan **out);
  * Requirements: every base 16-byte aligned and non-NULL; strides >= 0 and
  * multiples of 16 (a stride whose dimension has extent 1 is ignored).
  * Performance (not a requirement): when every base and stride of both sides is
- * a multiple of 32 bytes, the row moves an even number of 16-byte units (16
- * elements each when converting) and no head is replicated, the kernel moves
- * 32 bytes per access, which is the faster path; pools from the CUDA
+ * a multiple of 32 bytes and the row moves an even number of 16-byte units (16
+ * elements each when converting), the kernel moves 32 bytes per access, which
+ * is the faster path; pools from the CUDA
  * allocator (256-byte aligned) in the standard layout take it whenever the row
  * allows. On the
  * decode side the views must not alias: sorted by stride, each dimension

@@ -428,15 +428,15 @@ kvr_status kvr_build_host_plan(const kvr_desc *d, const kvr_layout *src_layout,
     hp->sm_count = sm_count;
 
     // Pairs of adjacent units per access (one 32-byte load or store where a unit
-    // has 16 bytes): no replicated heads, an even number of units per row, and
-    // every row of both sides 32-byte aligned (view bases, and the strides of
-    // dimensions with more than one position).
+    // has 16 bytes): an even number of units per row, and every row of both
+    // sides (every decode copy of a replicated head too) 32-byte aligned: view
+    // bases, and the strides of dimensions with more than one position.
     auto aligned32 = [](const std::vector<uint64_t> &bases) {
         for (uint64_t b : bases)
             if (b % 32 != 0) return false;
         return true;
     };
-    hp->pairs = !kvr_replicated(g) && row_units % 2 == 0 && aligned32(hp->src_base) &&
+    hp->pairs = row_units % 2 == 0 && aligned32(hp->src_base) &&
                 aligned32(hp->dst_base) && (Np <= 1 || g.s_block_stride % 32 == 0) &&
                 (Bp <= 1 || g.s_token_stride % 32 == 0) &&
                 (Hp <= 1 || g.s_head_stride % 32 == 0) &&

@@ -164,16 +164,16 @@ constexpr int kvr_min_ctas(int U, int CONV) {
 // A unit reads NL and writes NS 16-byte pieces (1 and 1 for a bit copy).
 // REP: the plan replicates heads (a TP degree above H; see kvr_row).
 // W: units per access. W = 2 (plans whose rows hold an even number of units and
-// lie 32 bytes aligned, no replication; kvr_launch_pairs): each thread moves a
-// pair of adjacent units of one row with 32-byte loads and stores, U / 2 pairs
-// in flight: one row lookup and address per pair halves the index work per
-// byte (70B, ordered per-layer launches: BF16 -> FP8 5281 -> 5568, FP8 -> BF16
-// 4605 -> 5513 GB/s; whole-prompt: quantizing 6901 -> 7080, Qwen3-32B 4 x 32K
-// bit copy 6864 -> 6956).
+// lie 32 bytes aligned; kvr_launch_pairs): each thread moves a pair of adjacent
+// units of one row with 32-byte loads and stores, U / 2 pairs in flight: one
+// row lookup and address per pair halves the index work per byte (70B, ordered
+// per-layer launches: BF16 -> FP8 5281 -> 5568, FP8 -> BF16 4605 -> 5513 GB/s;
+// whole-prompt: quantizing 6901 -> 7080, Qwen3-32B 4 x 32K bit copy 6864 ->
+// 6956; replicated MLA latent, TP8 -> TP8: 6678 -> 6767).
 template <int U, int CONV, int MODE, bool REP, int W>
 __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
     kvr_relayout_kernel(const __grid_constant__ KvrArgs a) {
-    static_assert(W == 1 || (W == 2 && !REP), "pairs of units only without replication");
+    static_assert(W == 1 || W == 2, "one unit or a pair of units per access");
     constexpr bool EARLY = MODE != KVR_MODE_WHOLE;
     constexpr bool PF = MODE == KVR_MODE_LAYER_PREFETCH;
     constexpr int NL = CONV == KVR_CONV_BF16_TO_E4M3 ? 2 : 1;
@@ -246,6 +246,73 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
             }
             __syncthreads();
             const uint32_t qa = max(q0, w0 * rc), qb = min(q1, w1 * rc);
+            if constexpr (W == 2) {
+                // pairs (q, q + 1), q even, of one prefill row, each loaded once and
+                // stored to every decode copy (the plan checked every row's 32-byte
+                // alignment)
+                constexpr int UP = U > 1 ? U / 2 : 1;
+                const uint32_t pa = qa >> 1, pb = qb >> 1;
+                for (uint32_t base = pa + threadIdx.x; base < pb; base += UP * KVR_THREADS) {
+                    uint4 v[UP][2 * NL];
+                    float f[UP];
+#pragma unroll
+                    for (int k = 0; k < UP; ++k) {
+                        const uint32_t pq = base + (uint32_t)k * KVR_THREADS;
+                        f[k] = 0.0f;
+                        if (pq < pb) {
+                            const uint32_t q = pq * 2u;
+                            const uint32_t r = a.g.div_rc.div(q);
+                            const uint32_t u = q - r * rc;
+                            const ulonglong2 p = rows[(r - w0) * dc];
+                            if (!KVR_SRC_DROPPED(p)) {
+#pragma unroll
+                                for (int j = 0; j < NL; ++j)
+                                    load_stream32((const unsigned char *)p.x + u * SU + 32u * j,
+                                                  &v[k][2 * j], &v[k][2 * j + 1]);
+                            }
+                            if (CONV != KVR_CONV_NONE) f[k] = row_factor[(r - w0) * dc];
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < UP; ++k) {
+                        const uint32_t pq = base + (uint32_t)k * KVR_THREADS;
+                        if (pq >= pb) continue;
+                        const uint32_t q = pq * 2u;
+                        const uint32_t r = a.g.div_rc.div(q);
+                        const uint32_t u = q - r * rc;
+                        const uint32_t ti = (r - w0) * dc;
+                        if (KVR_SRC_DROPPED(rows[ti])) continue;
+                        if (CONV == KVR_CONV_E4M3_TO_BF16) {
+                            // one unit's 32 BF16 bytes at a time (fewer live registers)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint4 lo, hi;
+                                dequant16(v[k][h], f[k], &lo, &hi);
+                                for (uint32_t c = 0; c < dc; ++c) {
+                                    if (KVR_DST_DROPPED(rows[ti + c])) continue;
+                                    store_stream32(
+                                        (unsigned char *)rows[ti + c].y + u * DU + 32u * h, lo, hi);
+                                }
+                            }
+                        } else {
+                            uint4 lo, hi;
+                            if (CONV == KVR_CONV_NONE) {
+                                lo = v[k][0];
+                                hi = v[k][1];
+                            } else {
+                                lo = quant16(v[k][0], v[k][1], f[k]);
+                                hi = quant16(v[k][2], v[k][3], f[k]);
+                            }
+                            for (uint32_t c = 0; c < dc; ++c) {
+                                if (KVR_DST_DROPPED(rows[ti + c])) continue;
+                                store_stream32((unsigned char *)rows[ti + c].y + u * DU, lo, hi);
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+                continue;
+            }
             for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
                 uint4 v[U][NL];
                 float f[U];
@@ -458,13 +525,12 @@ KvrKernel pick_instance(int32_t conv) {
 
 template <int MODE>
 KvrKernel pick_mode(int32_t conv, bool rep, bool pairs) {
-    return rep     ? pick_instance<MODE, true, 1>(conv)
-           : pairs ? pick_instance<MODE, false, 2>(conv)
-                   : pick_instance<MODE, false, 1>(conv);
+    if (rep) return pairs ? pick_instance<MODE, true, 2>(conv) : pick_instance<MODE, true, 1>(conv);
+    return pairs ? pick_instance<MODE, false, 2>(conv) : pick_instance<MODE, false, 1>(conv);
 }
 
-// `pairs`: the plan's rows allow pairs of units (KvrHostPlan::pairs; never with
-// replication); kvr_launch_pairs decides per instance.
+// `pairs`: the plan's rows allow pairs of units (KvrHostPlan::pairs);
+// kvr_launch_pairs decides per instance.
 KvrKernel pick_kernel(int32_t conv, int mode, bool rep, bool pairs) {
     pairs = kvr_launch_pairs(pairs, conv, mode);
     switch (mode) {

@@ -128,9 +128,10 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
             const uint32_t qb = q1 < w1 * rc ? q1 : w1 * rc;
             if (pairs) {
                 // pairs of adjacent units (q, q + 1), U / 2 in flight, one 32-byte
-                // access each: both units in one row, both addresses 32-byte aligned
+                // access each: both units in one row, both addresses 32-byte aligned,
+                // loaded once and stored to each of the dc decode copies
                 const uint32_t up = U > 1 ? U / 2 : 1, pa = qa / 2, pb = qb / 2;
-                if (rep || qa % 2 != 0 || qb % 2 != 0) ++bad;
+                if (qa % 2 != 0 || qb % 2 != 0) ++bad;
                 for (uint32_t tid = 0; tid < KVR_THREADS; ++tid)
                     for (uint32_t base = pa + tid; base < pb; base += up * KVR_THREADS)
                         for (uint32_t k = 0; k < up; ++k) {
@@ -139,22 +140,30 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
                             const uint32_t q = 2 * pq;
                             const uint32_t r = a.g.div_rc.div(q);
                             const uint32_t u = q - r * rc;
-                            visited += 2;
-                            if (r < w0 || r >= w1 || a.g.div_rc.div(q + 1) != r ||
-                                rows_src[r - w0] == UINT64_MAX) {
+                            if (r < w0 || r >= w1 || a.g.div_rc.div(q + 1) != r) {
                                 ++bad;
                                 continue;
                             }
-                            const uint64_t from = rows_src[r - w0] + (uint64_t)u * su;
-                            const uint64_t to = rows_dst[r - w0] + (uint64_t)u * du;
-                            if (from % 32 != 0 || to % 32 != 0 ||
-                                (u + 2) * su > (uint32_t)a.g.src_row_bytes ||
-                                (u + 2) * du > (uint32_t)a.g.dst_row_bytes) {
-                                ++bad;
-                                continue;
+                            const uint32_t ti = (r - w0) * dc;
+                            for (uint32_t c = 0; c < dc; ++c) {
+                                visited += 2;
+                                if (rows_src[ti + c] == UINT64_MAX ||
+                                    rows_src[ti + c] != rows_src[ti]) {
+                                    ++bad;
+                                    continue;
+                                }
+                                const uint64_t from = rows_src[ti] + (uint64_t)u * su;
+                                const uint64_t to = rows_dst[ti + c] + (uint64_t)u * du;
+                                if (from % 32 != 0 || to % 32 != 0 ||
+                                    (u + 2) * su > (uint32_t)a.g.src_row_bytes ||
+                                    (u + 2) * du > (uint32_t)a.g.dst_row_bytes) {
+                                    ++bad;
+                                    continue;
+                                }
+                                if (copy)
+                                    memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from,
+                                           32);
                             }
-                            if (copy)
-                                memcpy((void *)(uintptr_t)to, (const void *)(uintptr_t)from, 32);
                         }
                 continue;
             }

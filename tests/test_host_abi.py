@@ -582,9 +582,9 @@ def _pairs(emu, w, src, dst, convert=None):
 
 
 def test_pairs_of_units_only_where_every_row_allows_them(emu):
-    """Threads move pairs of adjacent units (32-byte accesses) exactly when no head is
-    replicated, rows hold an even number of units, and every row of both sides
-    starts on a 32-byte boundary."""
+    """Threads move pairs of adjacent units (32-byte accesses) exactly when rows hold
+    an even number of units and every row of both sides (every decode copy of a
+    replicated head too) starts on a 32-byte boundary."""
     emu.emu_plan_pairs.restype = ctypes.c_int32
     emu.emu_plan_pairs.argtypes = [ctypes.c_void_p] * 4
 
@@ -606,7 +606,9 @@ def test_pairs_of_units_only_where_every_row_allows_them(emu):
     w = case(head_dim=16, elem_bytes=1)                           # 16 B rows: one unit
     assert _pairs(emu, w, *fake_pools(w)) == 0
     w = case(kv_heads=2, src_tp=4)                                # replicated heads
-    assert _pairs(emu, w, *fake_pools(w)) == 0
+    s, d = fake_pools(w)
+    assert _pairs(emu, w, s, d) == 1
+    assert _pairs(emu, w, s, d[:3] + [d[3] + 16] + d[4:]) == 0    # one decode copy off
     # conversions: a unit is 16 elements (32 BF16 bytes, 16 FP8 bytes)
     w = case(head_dim=32)
     q = dict(src_dtype=1, dst_dtype=2, scales=np.ones(2 * 2, np.float32))
