@@ -310,52 +310,51 @@ __global__ void __launch_bounds__(KVR_THREADS, kvr_min_ctas(U, CONV))
                         }
                     }
                 }
-                __syncthreads();
-                continue;
-            }
-            for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
-                uint4 v[U][NL];
-                float f[U];
+            } else {
+                for (uint32_t base = qa + threadIdx.x; base < qb; base += U * KVR_THREADS) {
+                    uint4 v[U][NL];
+                    float f[U];
 #pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
-                    f[k] = 0.0f;
-                    if (q < qb) {
+                    for (int k = 0; k < U; ++k) {
+                        const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                        f[k] = 0.0f;
+                        if (q < qb) {
+                            const uint32_t r = a.g.div_rc.div(q);
+                            const uint32_t u = q - r * rc;
+                            const ulonglong2 p = rows[(r - w0) * dc];
+                            if (!KVR_SRC_DROPPED(p)) {
+#pragma unroll
+                                for (int j = 0; j < NL; ++j)
+                                    v[k][j] =
+                                        load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                            }
+                            if (CONV != KVR_CONV_NONE) f[k] = row_factor[(r - w0) * dc];
+                        }
+                    }
+                    // the unit's row and offset are recomputed here rather than kept
+                    // from the loads (fewer live registers across the loads)
+#pragma unroll
+                    for (int k = 0; k < U; ++k) {
+                        const uint32_t q = base + (uint32_t)k * KVR_THREADS;
+                        if (q >= qb) continue;
                         const uint32_t r = a.g.div_rc.div(q);
                         const uint32_t u = q - r * rc;
-                        const ulonglong2 p = rows[(r - w0) * dc];
-                        if (!KVR_SRC_DROPPED(p)) {
-#pragma unroll
-                            for (int j = 0; j < NL; ++j)
-                                v[k][j] =
-                                    load_stream((const unsigned char *)p.x + u * SU + 16u * j);
+                        const uint32_t ti = (r - w0) * dc;
+                        if (KVR_SRC_DROPPED(rows[ti])) continue;
+                        uint4 lo, hi;
+                        if (CONV == KVR_CONV_NONE) {
+                            lo = v[k][0];
+                        } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
+                            lo = quant16(v[k][0], v[k][NL - 1], f[k]);
+                        } else {
+                            dequant16(v[k][0], f[k], &lo, &hi);
                         }
-                        if (CONV != KVR_CONV_NONE) f[k] = row_factor[(r - w0) * dc];
-                    }
-                }
-                // the unit's row and offset are recomputed here rather than kept
-                // from the loads (fewer live registers across the loads)
-#pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const uint32_t q = base + (uint32_t)k * KVR_THREADS;
-                    if (q >= qb) continue;
-                    const uint32_t r = a.g.div_rc.div(q);
-                    const uint32_t u = q - r * rc;
-                    const uint32_t ti = (r - w0) * dc;
-                    if (KVR_SRC_DROPPED(rows[ti])) continue;
-                    uint4 lo, hi;
-                    if (CONV == KVR_CONV_NONE) {
-                        lo = v[k][0];
-                    } else if (CONV == KVR_CONV_BF16_TO_E4M3) {
-                        lo = quant16(v[k][0], v[k][NL - 1], f[k]);
-                    } else {
-                        dequant16(v[k][0], f[k], &lo, &hi);
-                    }
-                    for (uint32_t c = 0; c < dc; ++c) {
-                        if (KVR_DST_DROPPED(rows[ti + c])) continue;
-                        unsigned char *to = (unsigned char *)rows[ti + c].y + u * DU;
-                        store_stream(to, lo);
-                        if (CONV == KVR_CONV_E4M3_TO_BF16) store_stream(to + 16, hi);
+                        for (uint32_t c = 0; c < dc; ++c) {
+                            if (KVR_DST_DROPPED(rows[ti + c])) continue;
+                            unsigned char *to = (unsigned char *)rows[ti + c].y + u * DU;
+                            store_stream(to, lo);
+                            if (CONV == KVR_CONV_E4M3_TO_BF16) store_stream(to + 16, hi);
+                        }
                     }
                 }
             }
