@@ -120,12 +120,14 @@ struct KvrHostPlan {
                                        // (32-byte accesses): see kvr_build_host_plan
 };
 
-// Whether a launch of mode `mode` (KvrMode) of a plan moves pairs of units: every
-// instance where the plan's rows allow it, except the bit copy's prefetching
-// per-layer one (its loads mostly hit L2, and single units measured 0.7 %
-// faster there on the 70B workload).
-inline bool kvr_launch_pairs(bool plan_pairs, int32_t conv, int32_t mode) {
-    return plan_pairs && !(conv == KVR_CONV_NONE && mode == KVR_MODE_LAYER_PREFETCH);
+// Whether a launch of mode `mode` (KvrMode) over `layers` layers of a plan moves
+// pairs of units: every instance where the plan's rows allow it, except the bit
+// copy's prefetching instance outside 2-layer ranges (its loads mostly hit L2;
+// measured on 70B layers, single units against pairs: 1 layer 6190 / 6146 GB/s,
+// 2 layers 6140 / 6457, 4 layers 6089 / 5485).
+inline bool kvr_launch_pairs(bool plan_pairs, int32_t conv, int32_t mode, int32_t layers) {
+    return plan_pairs &&
+           !(conv == KVR_CONV_NONE && mode == KVR_MODE_LAYER_PREFETCH && layers != 2);
 }
 
 // Slices per item of a launch over `count` (>= 2) layers, shaped like a

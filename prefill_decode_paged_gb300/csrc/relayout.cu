@@ -529,9 +529,9 @@ KvrKernel pick_mode(int32_t conv, bool rep, bool pairs) {
 }
 
 // `pairs`: the plan's rows allow pairs of units (KvrHostPlan::pairs);
-// kvr_launch_pairs decides per instance.
-KvrKernel pick_kernel(int32_t conv, int mode, bool rep, bool pairs) {
-    pairs = kvr_launch_pairs(pairs, conv, mode);
+// kvr_launch_pairs decides per instance and range length (`layers`).
+KvrKernel pick_kernel(int32_t conv, int mode, bool rep, bool pairs, int32_t layers) {
+    pairs = kvr_launch_pairs(pairs, conv, mode, layers);
     switch (mode) {
         case KVR_MODE_LAYER:
             return pick_mode<KVR_MODE_LAYER>(conv, rep, pairs);
@@ -582,7 +582,7 @@ kvr_status launch(const kvr_plan *p, int32_t layer0, int32_t layers, int32_t sli
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg,
                               pick_kernel(p->host.g.conv, mode, kvr_replicated(p->host.g),
-                                          p->host.pairs),
+                                          p->host.pairs, layers),
                               a) == cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;
@@ -715,10 +715,10 @@ static kvr_status make_plan(const kvr_desc *desc, const kvr_layout *src_layout,
         // CTAs per SM of both per-layer instances (each shapes its own grids)
         auto occupancy = [&](bool pairs, int *resident, int *resident_pf) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    resident, pick_kernel(conv, KVR_MODE_LAYER, rep, pairs), KVR_THREADS, 0) !=
-                    cudaSuccess ||
+                    resident, pick_kernel(conv, KVR_MODE_LAYER, rep, pairs, 1), KVR_THREADS,
+                    0) != cudaSuccess ||
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    resident_pf, pick_kernel(conv, KVR_MODE_LAYER_PREFETCH, rep, pairs),
+                    resident_pf, pick_kernel(conv, KVR_MODE_LAYER_PREFETCH, rep, pairs, 1),
                     KVR_THREADS, 0) != cudaSuccess) {
                 cudaGetLastError();
                 *resident = *resident_pf = 0;
@@ -1044,7 +1044,7 @@ extern "C" kvr_status kv_relayout_all_prealloc(const kvr_desc *desc, void *strea
         return KVR_ERR_CUDA;
     return cudaLaunchKernelEx(&cfg,
                               pick_kernel(KVR_CONV_NONE, KVR_MODE_WHOLE, kvr_replicated(hp.g),
-                                          hp.pairs),
+                                          hp.pairs, hp.num_layers),
                               a) == cudaSuccess
                ? KVR_OK
                : KVR_ERR_CUDA;

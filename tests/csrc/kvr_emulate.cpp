@@ -77,7 +77,7 @@ int64_t walk(const kvr_desc *d, const kvr_layout *sl, const kvr_layout *dl, cons
     const uint64_t grid = (uint64_t)layers * a.tasks_per_layer;
     const uint32_t rc = (uint32_t)a.g.row_chunks;
     // units in flight per thread, as the kernel instance the launch picks
-    const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode);
+    const bool pairs = kvr_launch_pairs(hp.pairs, hp.g.conv, mode, layers);
     const uint32_t U = (uint32_t)kvr_units(hp.g.conv, mode, pairs);
     const uint32_t su = (uint32_t)a.g.src_unit_bytes, du = (uint32_t)a.g.dst_unit_bytes;
     const int64_t n_factors = (int64_t)hp.factors.size();
