@@ -282,15 +282,17 @@ def test_fuzzed_pack_then_unpack_equals_the_direct_relayout(seed):
             assert np.array_equal(t.cpu().numpy().view(dt), a), mode
 
 
+@pytest.mark.parametrize("geo", sorted(GEOS))
 @pytest.mark.parametrize("skew", [0, 16])
 @pytest.mark.parametrize("direction", ["copy", "quant", "dequant"])
 @pytest.mark.parametrize("mode", ["all", "layer"])
-def test_pairs_and_single_units_match_the_oracle(skew, direction, mode):
+def test_pairs_and_single_units_match_the_oracle(skew, direction, mode, geo):
     """Prefill pools on a 32-byte boundary (threads move pairs of adjacent units) and
-    16 bytes past one (single units): both equal the oracle, in every conversion."""
+    16 bytes past one (single units): both equal the oracle, in every conversion,
+    with heads split and with heads replicated on both sides."""
     import torch
     rng = np.random.default_rng(11)
-    w = _w(5, elem_bytes=1 if direction == "dequant" else 2)
+    w = _w(5, elem_bytes=1 if direction == "dequant" else 2, **GEOS[geo])
     shape = w.src_shape()
     if direction == "dequant":
         src_np = [rng.integers(0, 256, shape, dtype=np.uint8) for _ in range(w.src_tp)]
@@ -300,9 +302,9 @@ def test_pairs_and_single_units_match_the_oracle(skew, direction, mode):
             "quant": dict(src_dtype=DTYPE_BF16, dst_dtype=DTYPE_FP8_E4M3),
             "dequant": dict(src_dtype=DTYPE_FP8_E4M3, dst_dtype=DTYPE_BF16)}[direction]
     dt, fill = (np.uint8, 0xFF) if direction == "quant" else (np.uint16, 0xFFFF)
-    scales = rng.uniform(0.01, 2.0, w.num_layers * 2 * 8).astype(np.float32)
-    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block, 2,
-                               w.head_dim)
+    scales = rng.uniform(0.01, 2.0, w.num_layers * 2 * w.kv_heads).astype(np.float32)
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block,
+                               wl.heads_per_shard(w.kv_heads, w.src_tp), w.head_dim)
     ref_bufs, ref_views, _, _ = decode_family(w, "standard", dt, fill)
     extra = dict(per_head=1, scales=scales, **conv) if conv else {}
     oracle.relayout_general(sv, ref_views, **extra, **_tables(w))
