@@ -614,7 +614,8 @@ def conversion_child(kind, K, W, dev_index):
     --convert kind`` (whole prompt and ordered per-layer launches from a CUDA graph,
     K steps each after W warm-up steps) on this rank's GPU alone, its pools the
     first allocations of its CUDA context. Returns (GB/s whole, GB/s per layer, us
-    per launch, the child's timed host-clock windows)."""
+    per launch, the child's timed host-clock windows); raises RuntimeError with the
+    end of the child's stderr if it fails."""
     env = {k: v for k, v in os.environ.items()
            if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "LOCAL_WORLD_SIZE", "GROUP_RANK",
                         "ROLE_RANK", "MASTER_ADDR", "MASTER_PORT", "TORCHELASTIC_RUN_ID")}
@@ -626,7 +627,7 @@ def conversion_child(kind, K, W, dev_index):
            "--no-cpu-baseline", "--no-clocks", "--sm-sweep", "", "--report-windows"]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
-        raise SystemExit(f"bench.py: the {kind} child run failed: {r.stderr.strip()[-400:]}")
+        raise RuntimeError(f"the {kind} child run failed: {r.stderr.strip()[-400:]}")
     line = json.loads(r.stdout.strip().splitlines()[-1])
     g = line["per_layer"]["cuda_graph"]
     return line["value"], g["gbs"], g["us_per_launch"], line["run"]["timed_windows"]
@@ -665,13 +666,22 @@ def targets_measure(timed, dev, stream, K, world, peak, windows, main_per_layer=
     for kind in ("bf16_to_fp8", "fp8_to_bf16"):
         ws, wd, conv = conversion_for(kind, w70)
         b = algorithmic_bytes(ws, conv)
-        # fresh process (each rank its own GPU), then the slowest rank's time
-        whole_gbs, layer_gbs, _, child_windows = conversion_child(kind, K, W, dev.index)
-        windows.extend(tuple(x) for x in child_windows)
-        ms_whole = max_over_ranks(b * K / (whole_gbs * 1e9) * 1e3, world, dev)
-        ms_layer = max_over_ranks(b * K / (layer_gbs * 1e9) * 1e3, world, dev)
-        whole = _figures(b, ms_whole, K, world, peak)
-        layer = _figures(b, ms_layer, K, world, peak, ws.num_layers)
+        # fresh process (each rank its own GPU), then the slowest rank's time; a
+        # failed child leaves its figures out (and says why) rather than the line
+        try:
+            whole_gbs, layer_gbs, _, child_windows = conversion_child(kind, K, W, dev.index)
+            windows.extend(tuple(x) for x in child_windows)
+            failed = 0.0
+        except (RuntimeError, subprocess.TimeoutExpired, ValueError, KeyError) as e:
+            whole_gbs = layer_gbs = None
+            failed, why = 1.0, str(e)[-400:]
+        if max_over_ranks(failed, world, dev) > 0:
+            whole = layer = {"error": why if failed else "a child run failed on another rank"}
+        else:
+            ms_whole = max_over_ranks(b * K / (whole_gbs * 1e9) * 1e3, world, dev)
+            ms_layer = max_over_ranks(b * K / (layer_gbs * 1e9) * 1e3, world, dev)
+            whole = _figures(b, ms_whole, K, world, peak)
+            layer = _figures(b, ms_layer, K, world, peak, ws.num_layers)
         src, dst = ws.src_pools_torch(dev), wd.dst_pools_torch(dev)
         with RelayoutPlan(src, dst, convert=conv, **ws.geometry()) as plan:
             g = layer_graph(plan, ws.num_layers, dev, stream)
@@ -679,7 +689,7 @@ def targets_measure(timed, dev, stream, K, world, peak, windows, main_per_layer=
             del g
         out[f"llama70b_{kind}"] = {"whole": whole, "per_layer": layer,
                                    "per_layer_pools_allocated_late": late,
-                                   "met": layer["frac"] >= 0.8,
+                                   "met": layer.get("frac", 0.0) >= 0.8,
                                    "met_pools_allocated_late": late["frac"] >= 0.8}
         del src, dst
         torch.cuda.empty_cache()

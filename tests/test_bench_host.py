@@ -153,8 +153,8 @@ def test_conversion_targets_run_in_a_fresh_single_gpu_process(monkeypatch):
     assert cmd[cmd.index("--convert") + 1] == "bf16_to_fp8"
     assert cmd[cmd.index("--steps") + 1] == "200" and cmd[cmd.index("--warmup") + 1] == "20"
     assert "--report-windows" in cmd and cmd[cmd.index("--modes") + 1] == "all,graph"
-    # a failed child ends the run loudly
+    # a failed child raises with the end of its stderr (targets_measure records it)
     monkeypatch.setattr(bench.subprocess, "run", lambda cmd, **kw: subprocess.CompletedProcess(
         cmd, 1, stdout="", stderr="boom"))
-    with pytest.raises(SystemExit, match="boom"):
+    with pytest.raises(RuntimeError, match="boom"):
         bench.conversion_child("fp8_to_bf16", 200, 20, 0)
