@@ -330,3 +330,32 @@ def test_pairs_and_single_units_match_the_oracle(skew, direction, mode, geo):
         torch.cuda.synchronize()
     for ref, got in zip(ref_bufs, tbufs):
         assert np.array_equal(got.cpu().numpy().view(dt), ref)
+
+
+@pytest.mark.parametrize("mode", ["all", "layer"])
+def test_padded_head_stride_matches_the_oracle(mode):
+    """Decode heads 144 bytes apart (rows of 128 bytes padded to a 16-byte but not a
+    32-byte multiple, so the launches move one unit per access) equal the oracle."""
+    import torch
+    w = _w(6)
+    L, C, N, B, Hl, D = w.dst_shape()
+    pad = D + 8                                   # 144-byte head stride for BF16
+    src_np = w.src_pools_numpy()
+    sv = oracle.standard_views(src_np, w.num_layers, 2, w.src_num_blocks, w.src_block,
+                               wl.heads_per_shard(w.kv_heads, w.src_tp), w.head_dim)
+    ref = [np.full((L, C, N, B, Hl, pad), 0xFFFF, np.uint16) for _ in range(w.dst_tp)]
+    oracle.relayout_general(sv, [[[b[l, c, ..., :D] for c in range(C)] for l in range(L)]
+                                 for b in ref], **_tables(w))
+    got = [torch.full((L, C, N, B, Hl, pad), -1, dtype=torch.int16, device="cuda")
+           for _ in range(w.dst_tp)]
+    views = [[[g[l, c, ..., :D] for c in range(C)] for l in range(L)] for g in got]
+    with RelayoutPlan([_np_t(a) for a in src_np], None, dst_layout=layout_of_views(views),
+                      **w.geometry()) as plan:
+        if mode == "all":
+            plan.run_all()
+        else:
+            for l in range(L):
+                plan.run_layer(l)
+        torch.cuda.synchronize()
+    for a, g in zip(ref, got):
+        assert np.array_equal(g.cpu().numpy().view(np.uint16), a)
